@@ -1,0 +1,219 @@
+/*
+ * moe.h -- C ABI of libmoe: forward pass of one sparse Mixture-of-Experts
+ * FFN layer on an NVIDIA B300 (sm_103a).
+ *
+ * What the layer computes (the pages describe a gating network that picks a
+ * few experts per token -- kongchang.com, section "Architecture: The 40B
+ * Total vs. 2.5B Active Trade-off" -- with 256 routed experts, 6 selected per
+ * token and one always-active shared expert -- evermx.com review, section
+ * "Sparse architecture"; futurpulse.com, section "How does Flint use 39.8B
+ * parameters efficiently?"):
+ *
+ *   l[t][e]  = sum_i x[t][i] * Wr[e][i] + b[e]                 (fp32 router)
+ *   idx[t]   = the k experts with the largest l[t][.], larger logit first,
+ *              lower expert index first on equal logits
+ *   gate[t]  = softmax of l[t][idx[t][0..k)]   (renormalised top-k gates)
+ *   E_e(v)   = Wd_e ( silu(Wg_e v) * (Wu_e v) ),  silu(z) = z / (1 + e^-z)
+ *   y[t]     = sum_j gate[t][j] * E_{idx[t][j]}(x[t])  +  S(x[t])  [+ x[t]]
+ *
+ * where S is the shared expert (same SwiGLU form, weight 1).  The pages give
+ * counts, not the router function, gate normalisation or activation; the
+ * readings above are the ones this library implements.
+ *
+ * Conventions for every function below:
+ *  - Pointers named *_host are host memory; every other data pointer is
+ *    device memory of the current CUDA device.
+ *  - Nothing throws, exits or traps.  Argument errors are found on the host
+ *    before any launch and leave no side effect.
+ *  - Work is enqueued on the caller's stream; moe_route and moe_forward do
+ *    not synchronise and do not allocate.  One handle serves one stream at
+ *    a time (the handle's workspace is reused by every call).
+ *  - T == 0 is a no-op returning MOE_OK.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_H__
+typedef struct CUstream_st* cudaStream_t;
+#endif
+
+typedef struct moe_layer* moe_handle;          /* opaque, owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL where a pointer is required, bad size, T > max_tokens, misaligned */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape or dtype combination this build does not implement */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch error, no device, ...) */
+  MOE_ERR_OOM = 4,           /* workspace allocation failed in moe_create */
+  MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out (reported by moe_check) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
+
+/* Which expert-FFN kernels moe_forward uses. */
+typedef enum {
+  MOE_PATH_AUTO = 0,   /* weight-streaming GEMV for small T, tcgen05 grouped GEMM above it */
+  MOE_PATH_GEMV = 1,   /* always the weight-streaming GEMV kernels */
+  MOE_PATH_TC = 2      /* always the tcgen05 grouped GEMM (bf16 weights and activations only) */
+} moe_path;
+
+typedef struct {
+  int32_t d;             /* hidden width; multiple of 64 */
+  int32_t ffn;           /* routed expert FFN width F; multiple of 64 */
+  int32_t shared_ffn;    /* shared expert FFN width F_s (multiple of 64), 0 = no shared expert */
+  int32_t num_experts;   /* E, 1..512 */
+  int32_t top_k;         /* k, 1..8, k <= E */
+  int32_t max_tokens;    /* largest T any call will pass; sizes the workspace */
+  int32_t act_dtype;     /* MOE_F32 or MOE_BF16: type of x and y */
+  int32_t weight_dtype;  /* MOE_F32 (with F32 activations), MOE_BF16 or MOE_NVFP4 (with BF16 activations) */
+  int32_t add_residual;  /* nonzero: y = x + moe(x) */
+  int32_t path;          /* moe_path */
+  int32_t gemv_max_tokens; /* MOE_PATH_AUTO: T <= this uses the GEMV kernels; 0 = library default (64) */
+  int32_t wait_timeout_ms; /* limit of every device-side spin wait; 0 = default (2000 ms) */
+} moe_config;
+
+/*
+ * Weights, borrowed: device pointers that must stay valid and unchanged for
+ * the handle's lifetime (no copy is made).  All are 16-byte aligned.
+ *
+ * F32 / BF16 weights (row-major, the reduction dimension contiguous):
+ *   router_w [E][d] fp32, router_b [E] fp32 or NULL (= zeros)
+ *   w_gate, w_up [E][F][d];  w_down [E][d][F]
+ *   ws_gate, ws_up [F_s][d]; ws_down [d][F_s]     (ignored when shared_ffn == 0)
+ * NVFP4 weights: the same pointers hold packed e2m1 codes, two per byte,
+ *   element 2i in the low nibble, rows of K/2 bytes (K = reduction width);
+ *   s_* hold one e4m3 scale per 16 consecutive elements of a row
+ *   ([rows][K/16] bytes); t_* hold one fp32 scale per matrix ([E] for
+ *   routed experts, [1] for the shared expert).  Weight = e2m1 * e4m3 * fp32.
+ */
+typedef struct {
+  const float* router_w;
+  const float* router_b;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const void* ws_gate;
+  const void* ws_up;
+  const void* ws_down;
+  const uint8_t* s_gate;
+  const uint8_t* s_up;
+  const uint8_t* s_down;
+  const uint8_t* ss_gate;
+  const uint8_t* ss_up;
+  const uint8_t* ss_down;
+  const float* t_gate;
+  const float* t_up;
+  const float* t_down;
+  const float* ts_gate;
+  const float* ts_up;
+  const float* ts_down;
+} moe_weights;
+
+/* Human-readable name of a status; never NULL. */
+const char* moe_status_string(moe_status s);
+
+/*
+ * Validate cfg and w, allocate the workspace for cfg->max_tokens tokens and
+ * build the tensor maps over the weights.  On success *out owns that
+ * memory until moe_destroy.  On failure *out is NULL and nothing is held.
+ * `stream` is used for the workspace's initial clearing (synchronised
+ * before return).
+ */
+moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t stream,
+                      moe_handle* out);
+
+/* Free the handle and its workspace (synchronises the device first). NULL is a no-op. */
+moe_status moe_destroy(moe_handle h);
+
+/*
+ * Routing only.  x [T][d] (act_dtype), 16-byte aligned.  Writes idx [T][k]
+ * int32 (larger gate first) and gate [T][k] fp32 (required), and counts [E]
+ * int32 = tokens routed to each expert (optional, NULL to skip).
+ */
+moe_status moe_route(moe_handle h, const void* x, int32_t T, int32_t* idx, float* gate,
+                     int32_t* counts, cudaStream_t stream);
+
+/*
+ * Full layer.  x [T][d] and y [T][d] in act_dtype, 16-byte aligned, not
+ * overlapping.  idx_out [T][k] and gate_out [T][k] receive the routing when
+ * non-NULL.  T <= max_tokens.
+ */
+moe_status moe_forward(moe_handle h, const void* x, int32_t T, void* y, int32_t* idx_out,
+                       float* gate_out, cudaStream_t stream);
+
+/*
+ * Full layer on host buffers: copies x_host [T][d] to the device, runs
+ * moe_forward and copies y back to y_host [T][d]; returns after y_host is
+ * written (synchronises `stream`).  Page-locked host memory makes the copies
+ * asynchronous DMA; pageable memory works but is slower.
+ */
+moe_status moe_forward_host(moe_handle h, const void* x_host, int32_t T, void* y_host,
+                            cudaStream_t stream);
+
+/*
+ * The token-slot grouping of the last moe_route / moe_forward call on this
+ * handle (with the same T): offsets [E+1] (exclusive scan of counts),
+ * tok_of_slot [T*k] (token of each grouped slot; slots of one expert are
+ * contiguous and in (token, j) order) and slot_of [T][k] (grouped position
+ * of slot (t, j)).  Any output may be NULL.  Enqueued on `stream`.
+ */
+moe_status moe_get_grouping(moe_handle h, int32_t T, int32_t* offsets, int32_t* tok_of_slot,
+                            int32_t* slot_of, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then report and clear the device error word:
+ * MOE_ERR_TIMEOUT if a bounded wait ran out since the last check,
+ * MOE_ERR_CUDA if the stream reported an error, else MOE_OK.
+ */
+moe_status moe_check(moe_handle h, cudaStream_t stream);
+
+/*
+ * Failure-detection self-test (no counterpart on the pages): launch one
+ * kernel whose thread waits on an mbarrier that nothing completes, with the
+ * wait limited to timeout_us microseconds (1..5,000,000).  The wait runs out,
+ * the kernel records MOE_ERR_TIMEOUT in the device error word and returns;
+ * moe_check then reports it.  The GPU is not hung and the context stays usable.
+ */
+moe_status moe_debug_expire_wait(moe_handle h, int32_t timeout_us, cudaStream_t stream);
+
+/* Kernels of the layer, as counted by the profiling calls below. */
+typedef enum {
+  MOE_K_ROUTE = 0,         /* router + top-k + grouping */
+  MOE_K_GEMV_GATEUP = 1,   /* weight-streaming gate/up + SwiGLU */
+  MOE_K_GEMV_DOWN = 2,     /* weight-streaming down + gated combine */
+  MOE_K_TC_GATHER = 3,     /* slot-ordered copy of routed activations */
+  MOE_K_TC_GATEUP = 4,     /* tcgen05 gate/up + SwiGLU */
+  MOE_K_TC_DOWN = 5,       /* tcgen05 down + gated accumulate */
+  MOE_K_TC_FINALIZE = 6,   /* fp32 accumulator -> output */
+  MOE_K_COUNT = 7
+} moe_kernel_id;
+
+/*
+ * Per-kernel timing (no counterpart on the pages; measurement support).
+ * enable != 0: every later moe_route / moe_forward on this handle records a
+ * CUDA event pair around each kernel it launches (pairs come from a pool of
+ * max_launches created here; launches beyond it are not timed).  Recording
+ * events between kernels serialises them, so timed calls lose the overlap
+ * that programmatic dependent launch gives untimed ones.  enable == 0 stops
+ * recording and frees the pool.
+ */
+moe_status moe_profile_enable(moe_handle h, int32_t enable, int32_t max_launches);
+
+/*
+ * Synchronise the device, then write per kernel id the summed duration in
+ * milliseconds (ms[MOE_K_COUNT]) and the number of timed launches
+ * (launches[MOE_K_COUNT]) since the last read, and reset the counts.
+ */
+moe_status moe_profile_read(moe_handle h, float* ms, int32_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,489 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// for batches large enough that each expert sees many tokens (prefill).
+//
+// The layer is y_t = sum_j g_j E_{idx_j}(x_t) + S(x_t) with SwiGLU experts
+// (readings of the evermx.com review, section "Sparse architecture").  After
+// grouping, the token-slots of expert e are contiguous, so each expert is a
+// small dense GEMM whose weights are read from HBM once per call.
+//
+// Tiles put the weights on the MMA's M side (128 weight rows per tile) and
+// the tokens on the N side (up to 128 tokens, rounded up to 16), so an
+// expert's ~100 tokens are not padded to 128 rows of wasted A traffic.
+//
+//  * pass 1 (gate/up): D_g = Wg[rows] . X^T and D_u = Wu[rows] . X^T into two
+//    TMEM accumulators; the epilogue writes h = silu(D_g) * D_u (bf16) per
+//    slot.  The routed slots read a slot-ordered copy of x (made by a small
+//    gather kernel) with plain tiled TMA loads; the shared expert reads x.
+//  * pass 2 (down): D = Wd[rows] . H^T; the epilogue multiplies by the
+//    slot's gate and adds into an fp32 accumulator y_acc[t][row] with
+//    red.global.add (order of the adds is not fixed: the fp32 sum is
+//    deterministic up to rounding order).
+//  * finalise: y = bf16(y_acc (+ x)).
+//
+// One persistent CTA per SM, 6 warps: warp 0 issues TMA into a ring of
+// shared-memory stages, warp 1 (one thread) issues tcgen05.mma and commits to
+// mbarriers, warps 2-5 drain TMEM (double-buffered accumulators) while the
+// next tile's MMAs run.  Every wait is bounded (see ptx.cuh).
+#include <utility>
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreadsTc = 192;
+
+template <int MODE> struct TcCfg;
+template <> struct TcCfg<0> {     // gate/up: A_g + A_u + B per stage
+  static constexpr int STAGES = 4;
+  static constexpr int STAGE_BYTES = 2 * kTcBM * 128 + kTcBN * 128;
+  static constexpr int ACC_COLS = 2 * kTcBN;          // per buffer: gate then up
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;      // two buffers
+};
+template <> struct TcCfg<1> {     // down: A + B per stage
+  static constexpr int STAGES = 6;
+  static constexpr int STAGE_BYTES = kTcBM * 128 + kTcBN * 128;
+  static constexpr int ACC_COLS = kTcBN;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+};
+
+struct TcParams {
+  CUtensorMap tm_a0, tm_a1;   // routed weights (pass 1: gate, up; pass 2: down)
+  CUtensorMap tm_sa0, tm_sa1; // shared expert weights
+  CUtensorMap tm_b;           // routed B operand: pass 1 slot-ordered x copy, pass 2 h
+  CUtensorMap tm_sb;          // shared-expert B operand: pass 1 x, pass 2 h
+  int T, d, F, Fs, E, k, Fmax;
+  int K, Ks;                  // reduction width, routed / shared
+  int mt, mt_s;               // weight-row tiles per expert, routed / shared
+  int n_pre;                  // units that need no routing (shared expert, pass 1)
+  const int32_t* tok_of_slot;
+  const int32_t* src_of_slot;
+  const float* gate;
+  const TcUnit* units;
+  const int32_t* n_units;
+  __nv_bfloat16* h16;
+  float* yacc;
+  unsigned int* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ TcUnit get_unit(const TcParams& p, int u) {
+  if (u < p.n_pre) {
+    const int tb = u / p.mt_s, m = u % p.mt_s;
+    return TcUnit{p.E, m, tb * kTcBN, min(kTcBN, p.T - tb * kTcBN)};
+  }
+  return p.units[u];
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies in flight
+// before the CTA leaves after an abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return;
+}
+
+// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and on
+// success every lane observes the completed phase itself.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (ok)
+    while (!mbar_try_wait(bar, parity)) {
+    }
+  return ok != 0;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<MODE>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = dsm;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + S * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_a0);
+    tma_prefetch_desc(&p.tm_b);
+    tma_prefetch_desc(&p.tm_sb);
+    tma_prefetch_desc(&p.tm_sa0);
+    if (MODE == 0) {
+      tma_prefetch_desc(&p.tm_a1);
+      tma_prefetch_desc(&p.tm_sa1);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+
+  if (MODE == 1) pdl_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t last_par[S];
+    bool issued[S];
+    for (int i = 0; i < S; ++i) issued[i] = false;
+    int n_total = p.n_pre;
+    bool waited = MODE == 1;
+    if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+    bool ok = true;
+    for (int u = blockIdx.x; ok; u += gridDim.x) {
+      if (u >= n_total) {
+        if (waited) break;
+        pdl_wait();
+        waited = true;
+        n_total = __ldcg(p.n_units + MODE);
+        if (u >= n_total) break;
+      }
+      const TcUnit un = get_unit(p, u);
+      const bool sh = un.expert == p.E;
+      const int n_pad = (un.n + 15) & ~15;
+      const int K = sh ? p.Ks : p.K;
+      const int arow = sh ? un.m_tile * kTcBM : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * kTcBM;
+      const CUtensorMap* ma0 = sh ? &p.tm_sa0 : &p.tm_a0;
+      const CUtensorMap* ma1 = sh ? &p.tm_sa1 : &p.tm_a1;
+      const uint32_t bytes = (MODE == 0 ? 2 : 1) * kTcBM * 128 + kTcBN * 128;
+      const CUtensorMap* mb = sh ? &p.tm_sb : &p.tm_b;
+      const int brow = (MODE == 1 && sh) ? p.T * p.k + un.slot0 : un.slot0;
+      for (int k0 = 0; k0 < K; k0 += kTcBK) {
+        if (!warp_wait(&empty[stage], phase ^ 1, wc)) { ok = false; break; }
+        uint8_t* st = stages + stage * C::STAGE_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(st, ma0, k0, arow, &full[stage]);
+          if (MODE == 0) tma_load_2d(st + kTcBM * 128, ma1, k0, arow, &full[stage]);
+          tma_load_2d(st + (MODE == 0 ? 2 : 1) * kTcBM * 128, mb, k0, brow, &full[stage]);
+        }
+        __syncwarp();
+        issued[stage] = true;
+        last_par[stage] = phase;
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int i = 0; i < S; ++i)
+        if (issued[i]) drain_wait(&full[i], last_par[i], p.wait_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tph[2] = {0, 0};
+      int buf = 0;
+      int n_total = p.n_pre;
+      bool waited = MODE == 1;
+      if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+      bool ok = true;
+      uint64_t* last_commit = nullptr;
+      uint32_t last_commit_par = 0;
+      for (int u = blockIdx.x; ok; u += gridDim.x) {
+        if (u >= n_total) {
+          if (waited) break;
+          pdl_wait();
+          waited = true;
+          n_total = __ldcg(p.n_units + MODE);
+          if (u >= n_total) break;
+        }
+        const TcUnit un = get_unit(p, u);
+        const bool sh = un.expert == p.E;
+        const int n_pad = (un.n + 15) & ~15;
+        const int K = sh ? p.Ks : p.K;
+        const uint32_t idesc = idesc_bf16_f32(kTcBM, n_pad);
+        if (!mbar_wait(&tempty[buf], tph[buf] ^ 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * C::ACC_COLS;
+        for (int k0 = 0; k0 < K; k0 += kTcBK) {
+          if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stages + stage * C::STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const uint32_t accum = (k0 > 0 || kk > 0) ? 1u : 0u;
+            if (MODE == 0) {
+              const uint64_t bd = sdesc_sw128(st + 2 * kTcBM * 128 + kk * 32);
+              tc_mma_f16(acc, sdesc_sw128(st + kk * 32), bd, idesc, accum);
+              tc_mma_f16(acc + kTcBN, sdesc_sw128(st + kTcBM * 128 + kk * 32), bd, idesc, accum);
+            } else {
+              tc_mma_f16(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + kTcBM * 128 + kk * 32), idesc, accum);
+            }
+          }
+          tc_commit(&empty[stage]);
+          last_commit = &empty[stage];
+          last_commit_par = phase;
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+        tph[buf] ^= 1;
+        buf ^= 1;
+      }
+      if (!ok && last_commit) drain_wait(last_commit, last_commit_par, p.wait_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-5)
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int ept = threadIdx.x - 64;        // 0..127
+    if (MODE == 0) {
+      // clear the fp32 accumulator of pass 2 (x-independent, needs no routing)
+      float4* ya = reinterpret_cast<float4*>(p.yacc);
+      const size_t n4 = (size_t)p.T * p.d / 4;
+      for (size_t i = (size_t)blockIdx.x * 128 + ept; i < n4; i += (size_t)gridDim.x * 128)
+        ya[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint32_t tph[2] = {0, 0};
+    int buf = 0;
+    int n_total = p.n_pre;
+    bool waited = MODE == 1;
+    if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+    for (int u = blockIdx.x;; u += gridDim.x) {
+      if (u >= n_total) {
+        if (waited) break;
+        pdl_wait();
+        waited = true;
+        n_total = __ldcg(p.n_units + MODE);
+        if (u >= n_total) break;
+      }
+      const TcUnit un = get_unit(p, u);
+      const bool sh = un.expert == p.E;
+      const int n_pad = (un.n + 15) & ~15;
+      if (!warp_wait(&tfull[buf], tph[buf], wc)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
+      const int row = un.m_tile * kTcBM + q * 32 + lane;
+      for (int c0 = 0; c0 < n_pad; c0 += 16) {
+        if (MODE == 0) {
+          uint32_t g[16], v[16];
+          tmem_ld16(acc + c0, g);
+          tmem_ld16(acc + kTcBN + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            if (col < un.n) {
+              const float a = __uint_as_float(g[i]);
+              const float h = a / (1.f + __expf(-a)) * __uint_as_float(v[i]);
+              const int hs = sh ? p.T * p.k + un.slot0 + col : un.slot0 + col;
+              p.h16[(size_t)hs * p.Fmax + row] = __float2bfloat16_rn(h);
+            }
+          }
+        } else {
+          uint32_t v[16];
+          tmem_ld16(acc + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            if (col < un.n) {
+              int t;
+              float g;
+              if (sh) {
+                t = un.slot0 + col;
+                g = 1.f;
+              } else {
+                const int src = __ldcg(p.src_of_slot + un.slot0 + col);
+                t = src / p.k;
+                g = __ldcg(p.gate + src);
+              }
+              red_add_f32(p.yacc + (size_t)t * p.d + row, g * __uint_as_float(v[i]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+      tph[buf] ^= 1;
+      buf ^= 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Slot-ordered copy of the routed tokens' activations: xp[slot] = x[tok_of_slot[slot]].
+__global__ void __launch_bounds__(256) tc_gather_kernel(const __nv_bfloat16* __restrict__ x,
+                                                        const int32_t* __restrict__ tok_of_slot,
+                                                        __nv_bfloat16* __restrict__ xp, int slots, int d) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int per_row = d / 8;                       // 16-byte pieces per row
+  const size_t n = (size_t)slots * per_row;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int s = (int)(i / per_row), c = (int)(i % per_row);
+    const int t = __ldg(tok_of_slot + s);
+    reinterpret_cast<uint4*>(xp)[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c);
+  }
+}
+
+// y = bf16(y_acc (+ x)), 8 values per thread.
+__global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restrict__ yacc,
+                                                          const __nv_bfloat16* __restrict__ x,
+                                                          __nv_bfloat16* __restrict__ y, size_t n8, int residual) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(yacc) + 2 * i);
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(yacc) + 2 * i + 1);
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (residual) {
+      const uint4 xr = __ldg(reinterpret_cast<const uint4*>(x) + i);
+      const uint32_t xs[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] += __uint_as_float(xs[j] << 16);
+        v[2 * j + 1] += __uint_as_float(xs[j] & 0xFFFF0000u);
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      op[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(y)[i] = o;
+  }
+}
+
+template <int MODE>
+size_t tc_smem_bytes() {
+  using C = TcCfg<MODE>;
+  return 1024 + C::STAGES * C::STAGE_BYTES + (2 * C::STAGES + 4) * 8 + 16;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace
+
+int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k) {
+  (void)d;
+  const long long routed = (long long)(F / kTcBM) * ((long long)T * k / kTcBN + E);
+  const long long shared = (long long)(Fs / kTcBM) * ((T + kTcBN - 1) / kTcBN);
+  return (int)(routed + shared);
+}
+int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k) {
+  (void)F;
+  const long long routed = (long long)(d / kTcBM) * ((long long)T * k / kTcBN + E);
+  const long long shared = Fs > 0 ? (long long)(d / kTcBM) * ((T + kTcBN - 1) / kTcBN) : 0;
+  return (int)(routed + shared);
+}
+
+cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc_smem_bytes<0>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<1>());
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int Fmax = a.F > a.Fs ? a.F : a.Fs;
+  TcParams p;
+  p.T = a.T; p.d = a.d; p.F = a.F; p.Fs = a.Fs; p.E = a.E; p.k = a.k; p.Fmax = Fmax;
+  p.tok_of_slot = a.ws.tok_of_slot;
+  p.src_of_slot = a.ws.src_of_slot;
+  p.gate = a.gate;
+  p.h16 = a.ws.h16;
+  p.yacc = a.ws.yacc;
+  p.err = a.ws.err;
+  p.wait_ns = a.wait_ns;
+  p.n_units = a.ws.n_units;
+  // slot-ordered copy of the routed activations
+  const size_t gpieces = (size_t)a.T * a.k * (a.d / 8);
+  const int gg = (int)((gpieces + 255) / 256 < (size_t)num_sms * 8 ? (gpieces + 255) / 256 : (size_t)num_sms * 8);
+  if (prof) prof->begin(MOE_K_TC_GATHER, s);
+  cudaError_t e = launch_ex(tc_gather_kernel, gg > 0 ? gg : 1, 256, 0, s,
+                            static_cast<const __nv_bfloat16*>(a.x), (const int32_t*)a.ws.tok_of_slot,
+                            a.ws.xp, a.T * a.k, a.d);
+  if (prof) prof->end(s);
+  if (e != cudaSuccess) return e;
+  // pass 1: gate/up
+  p.tm_a0 = *a.tm_wg; p.tm_a1 = *a.tm_wu;
+  if (a.Fs > 0) { p.tm_sa0 = *a.tm_sg; p.tm_sa1 = *a.tm_su; } else { p.tm_sa0 = *a.tm_wg; p.tm_sa1 = *a.tm_wu; }
+  p.tm_b = *a.tm_xp;
+  p.tm_sb = *a.tm_x;
+  p.K = a.d; p.Ks = a.d;
+  p.mt = a.F / kTcBM;
+  p.mt_s = a.Fs > 0 ? a.Fs / kTcBM : 1;
+  p.n_pre = a.Fs > 0 ? (a.Fs / kTcBM) * ((a.T + kTcBN - 1) / kTcBN) : 0;
+  p.units = a.ws.units_gu;
+  const int grid1 = num_sms < a.max_units_gu ? num_sms : (a.max_units_gu > 0 ? a.max_units_gu : 1);
+  if (prof) prof->begin(MOE_K_TC_GATEUP, s);
+  e = launch_ex(tc_kernel<0>, grid1, kThreadsTc, tc_smem_bytes<0>(), s, p);
+  if (prof) prof->end(s);
+  if (e != cudaSuccess) return e;
+  // pass 2: down
+  p.tm_a0 = *a.tm_wd; p.tm_a1 = *a.tm_wd;
+  p.tm_sa0 = a.Fs > 0 ? *a.tm_sd : *a.tm_wd; p.tm_sa1 = p.tm_sa0;
+  p.tm_b = *a.tm_h;
+  p.tm_sb = *a.tm_h;
+  p.K = a.F; p.Ks = a.Fs > 0 ? a.Fs : a.F;
+  p.mt = a.d / kTcBM;
+  p.mt_s = a.d / kTcBM;
+  p.n_pre = 0;
+  p.units = a.ws.units_dn;
+  const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
+  if (prof) prof->begin(MOE_K_TC_DOWN, s);
+  e = launch_ex(tc_kernel<1>, grid2, kThreadsTc, tc_smem_bytes<1>(), s, p);
+  if (prof) prof->end(s);
+  if (e != cudaSuccess) return e;
+  // finalise
+  const size_t n8 = (size_t)a.T * a.d / 8;
+  const int grid3 = (int)((n8 + 255) / 256 < (size_t)num_sms * 4 ? (n8 + 255) / 256 : (size_t)num_sms * 4);
+  if (prof) prof->begin(MOE_K_TC_FINALIZE, s);
+  e = launch_ex(tc_finalize_kernel, grid3 > 0 ? grid3 : 1, 256, 0, s, (const float*)a.ws.yacc,
+                static_cast<const __nv_bfloat16*>(a.x), static_cast<__nv_bfloat16*>(a.y), n8,
+                (int)a.add_residual);
+  if (prof) prof->end(s);
+  return e;
+}
+
+}  // namespace moe

@@ -1,0 +1,467 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace ownership, tensor maps, kernel sequencing on the caller's stream.
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_layer {
+  moe_config cfg;
+  moe_weights w;
+  Workspace ws;
+  int device = 0;
+  int num_sms = 0;
+  bool tc_capable = false;
+  uint64_t wait_ns = 0;
+  int max_units_gu = 0, max_units_dn = 0;
+  CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp;
+  void* block = nullptr;
+  Prof prof;
+};
+
+namespace {
+
+inline size_t act_bytes(const moe_config& c) { return c.act_dtype == MOE_F32 ? 4 : 2; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Largest 16-byte chunk counts the GEMV kernels are built for (see gemv.cu).
+bool gemv_shape_ok(const moe_config& c) {
+  const int kmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
+  const int es2 = c.weight_dtype == MOE_F32 ? 8 : c.weight_dtype == MOE_BF16 ? 4 : 1;  // 2 x bytes/elem
+  const int row_b = c.d * es2 / 2, drow_b = kDownRPW * kmax * es2 / 2;
+  const int cap = c.weight_dtype == MOE_NVFP4 ? 8 : 16;
+  return (row_b + 511) / 512 <= cap && (drow_b + 511) / 512 <= cap;
+}
+
+bool tc_shape_ok(const moe_config& c) {
+  return c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.d % kTcBM == 0 && c.ffn % kTcBM == 0 &&
+         c.shared_ffn % kTcBM == 0;
+}
+
+moe_status validate_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->ffn <= 0 || c->shared_ffn < 0 || c->max_tokens <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->num_experts < 1 || c->top_k < 1 || c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC || c->gemv_max_tokens < 0 || c->wait_timeout_ms < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->d % 64 || c->ffn % 64 || c->shared_ffn % 64) return MOE_ERR_UNSUPPORTED;
+  if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  const bool combo = (c->act_dtype == MOE_F32 && c->weight_dtype == MOE_F32) ||
+                     (c->act_dtype == MOE_BF16 && (c->weight_dtype == MOE_BF16 || c->weight_dtype == MOE_NVFP4));
+  if (!combo) return MOE_ERR_UNSUPPORTED;
+  if (!gemv_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
+  if (c->path == MOE_PATH_TC && !tc_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c->max_tokens * c->top_k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status validate_weights(const moe_config& c, const moe_weights* w) {
+  if (!w || !w->router_w || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  const void* need[] = {w->router_w, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : need)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (w->router_b && (reinterpret_cast<uintptr_t>(w->router_b) & 3u)) return MOE_ERR_INVALID_ARG;
+  if (c.shared_ffn > 0) {
+    if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)) return MOE_ERR_INVALID_ARG;
+  }
+  if (c.weight_dtype == MOE_NVFP4) {
+    const void* s[] = {w->s_gate, w->s_up, w->s_down, w->t_gate, w->t_up, w->t_down};
+    for (const void* p : s)
+      if (!p || (reinterpret_cast<uintptr_t>(p) & 1u)) return MOE_ERR_INVALID_ARG;
+    if (c.shared_ffn > 0) {
+      const void* ss[] = {w->ss_gate, w->ss_up, w->ss_down, w->ts_gate, w->ts_up, w->ts_down};
+      for (const void* p : ss)
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 1u)) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  return MOE_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box {box_cols, box_rows}, 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+RouteArgs route_args(const moe_layer* h, const void* x, int T, int32_t* idx, float* gate, int32_t* counts,
+                     bool tc_units) {
+  RouteArgs a;
+  a.x = x;
+  a.T = T;
+  a.d = h->cfg.d;
+  a.E = h->cfg.num_experts;
+  a.k = h->cfg.top_k;
+  a.act_bf16 = h->cfg.act_dtype == MOE_BF16;
+  a.Wr = h->w.router_w;
+  a.b = h->w.router_b;
+  a.idx = idx;
+  a.gate = gate;
+  a.counts_out = counts;
+  a.ws = h->ws;
+  a.build_tc_units = tc_units ? 1 : 0;
+  a.F = h->cfg.ffn;
+  a.Fs = h->cfg.shared_ffn;
+  a.has_shared = h->cfg.shared_ffn > 0;
+  return a;
+}
+
+GemvArgs gemv_args(const moe_layer* h, const void* x, void* y, const float* gate, int T) {
+  GemvArgs a;
+  const moe_weights& w = h->w;
+  a.x = x;
+  a.y = y;
+  a.idx = nullptr;
+  a.gate = gate;
+  a.T = T;
+  a.d = h->cfg.d;
+  a.F = h->cfg.ffn;
+  a.Fs = h->cfg.shared_ffn;
+  a.E = h->cfg.num_experts;
+  a.k = h->cfg.top_k;
+  a.act_bf16 = h->cfg.act_dtype == MOE_BF16;
+  a.add_residual = h->cfg.add_residual != 0;
+  a.wg = w.w_gate; a.wu = w.w_up; a.wd = w.w_down;
+  a.sg = w.ws_gate; a.su = w.ws_up; a.sd = w.ws_down;
+  a.sc_g = w.s_gate; a.sc_u = w.s_up; a.sc_d = w.s_down;
+  a.ssc_g = w.ss_gate; a.ssc_u = w.ss_up; a.ssc_d = w.ss_down;
+  a.ts_g = w.t_gate; a.ts_u = w.t_up; a.ts_d = w.t_down;
+  a.tss_g = w.ts_gate; a.tss_u = w.ts_up; a.tss_d = w.ts_down;
+  a.ws = h->ws;
+  return a;
+}
+
+moe_status check_call(const moe_layer* h, const void* x, int32_t T) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !aligned16(x))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
+                       cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  int32_t* idx = idx_out ? idx_out : h->ws.idx;
+  float* gate = gate_out ? gate_out : h->ws.gate;
+  const int gemv_max = c.gemv_max_tokens > 0 ? c.gemv_max_tokens : kSmallT;
+  const bool tc = c.path == MOE_PATH_TC || (c.path == MOE_PATH_AUTO && h->tc_capable && T > gemv_max);
+  if (tc) {
+    moe_status st = cuda_status(launch_route(route_args(h, x, T, idx, gate, nullptr, true), h->num_sms, s, &h->prof));
+    if (st != MOE_OK) return st;
+    CUtensorMap tm_x;
+    if (!make_map_bf16(&tm_x, x, (uint64_t)T, (uint64_t)c.d, kTcBN, kTcBK)) return MOE_ERR_CUDA;
+    TcArgs a;
+    a.tm_x = &tm_x;
+    a.tm_xp = &h->tm_xp;
+    a.tm_wg = &h->tm_wg; a.tm_wu = &h->tm_wu; a.tm_sg = &h->tm_sg; a.tm_su = &h->tm_su;
+    a.tm_wd = &h->tm_wd; a.tm_sd = &h->tm_sd; a.tm_h = &h->tm_h;
+    a.x = x;
+    a.y = y;
+    a.gate = gate;
+    a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+    a.add_residual = c.add_residual != 0;
+    a.ws = h->ws;
+    a.wait_ns = h->wait_ns;
+    a.max_units_gu = tc_max_units_gu(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+    a.max_units_dn = tc_max_units_dn(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+    return cuda_status(launch_tc(a, h->num_sms, s, &h->prof));
+  }
+  const size_t es = act_bytes(c);
+  for (int t0 = 0; t0 < T; t0 += kGemvChunkT) {
+    const int tc_ = T - t0 < kGemvChunkT ? T - t0 : kGemvChunkT;
+    const uint8_t* xc = static_cast<const uint8_t*>(x) + (size_t)t0 * c.d * es;
+    uint8_t* yc = static_cast<uint8_t*>(y) + (size_t)t0 * c.d * es;
+    int32_t* ic = idx + (size_t)t0 * c.top_k;
+    float* gc = gate + (size_t)t0 * c.top_k;
+    moe_status st = cuda_status(launch_route(route_args(h, xc, tc_, ic, gc, nullptr, false), h->num_sms, s, &h->prof));
+    if (st != MOE_OK) return st;
+    st = cuda_status(launch_gemv(gemv_args(h, xc, yc, gc, tc_), c.weight_dtype, h->num_sms, s, &h->prof));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape or dtype not supported";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM: device allocation failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: device-side wait ran out";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t stream, moe_handle* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status st = validate_config(cfg);
+  if (st != MOE_OK) return st;
+  st = validate_weights(*cfg, w);
+  if (st != MOE_OK) return st;
+
+  moe_layer* h = new (std::nothrow) moe_layer();
+  if (!h) return MOE_ERR_OOM;
+  h->cfg = *cfg;
+  h->w = *w;
+  const moe_config& c = h->cfg;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  h->tc_capable = tc_shape_ok(c) && cc_major == 10;
+  if (c.path == MOE_PATH_TC && !h->tc_capable) {
+    delete h;
+    return MOE_ERR_UNSUPPORTED;
+  }
+  h->wait_ns = (uint64_t)(c.wait_timeout_ms > 0 ? c.wait_timeout_ms : 2000) * 1000000ull;
+
+  const size_t Tm = (size_t)c.max_tokens, E = c.num_experts, k = c.top_k, d = c.d;
+  const size_t Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
+  const size_t Tg = Tm < (size_t)kGemvChunkT ? Tm : (size_t)kGemvChunkT;
+  const size_t nblk = (Tm + 31) / 32;
+  if (h->tc_capable) {
+    h->max_units_gu = tc_max_units_gu(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+    h->max_units_dn = tc_max_units_dn(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+  }
+  struct Part { void** dst; size_t bytes; };
+  Workspace& ws = h->ws;
+  Part parts[] = {
+      {(void**)&ws.idx, Tm * k * 4},
+      {(void**)&ws.gate, Tm * k * 4},
+      {(void**)&ws.logits, (size_t)kSmallT * E * 4},
+      {(void**)&ws.sel, 2 * nblk * E * 4},
+      {(void**)&ws.counts, (E + 1) * 4},
+      {(void**)&ws.offsets, (E + 2) * 4},
+      {(void**)&ws.tok_of_slot, Tm * k * 4},
+      {(void**)&ws.src_of_slot, Tm * k * 4},
+      {(void**)&ws.slot_of, Tm * k * 4},
+      {(void**)&ws.active, (E + 1) * 4},
+      {(void**)&ws.units_gu, (size_t)(h->max_units_gu > 0 ? h->max_units_gu : 1) * sizeof(TcUnit)},
+      {(void**)&ws.units_dn, (size_t)(h->max_units_dn > 0 ? h->max_units_dn : 1) * sizeof(TcUnit)},
+      {(void**)&ws.n_units, 2 * 4},
+      {(void**)&ws.h32, Tg * (k + 1) * Fmax * 4},
+      {(void**)&ws.h16, h->tc_capable ? Tm * (k + 1) * Fmax * 2 : 16},
+      {(void**)&ws.xp, h->tc_capable ? Tm * k * d * 2 : 16},
+      {(void**)&ws.ypart, Tg * (k + 1) * d * 4},
+      {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
+      {(void**)&ws.counters, (1 + d / kFinRows + 64) * 4},
+      {(void**)&ws.err, 16},
+      {&ws.x_stage, Tm * d * act_bytes(c)},
+      {&ws.y_stage, Tm * d * act_bytes(c)},
+  };
+  size_t total = 0;
+  for (const Part& p : parts) total += up256(p.bytes);
+  ws.bytes = total;
+  if (cudaMalloc(&h->block, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_OOM;
+  }
+  size_t off = 0;
+  for (const Part& p : parts) {
+    *p.dst = static_cast<uint8_t*>(h->block) + off;
+    off += up256(p.bytes);
+  }
+  // Counters and the error word start at zero; the rest is written before it is read.
+  cudaError_t e = cudaMemsetAsync(ws.counters, 0, (1 + d / kFinRows + 64) * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.err, 0, 16, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->block);
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  if (h->tc_capable) {
+    const uint64_t F = c.ffn, Fs = c.shared_ffn;
+    bool ok = make_map_bf16(&h->tm_wg, w->w_gate, E * F, d, kTcBM, kTcBK) &&
+              make_map_bf16(&h->tm_wu, w->w_up, E * F, d, kTcBM, kTcBK) &&
+              make_map_bf16(&h->tm_wd, w->w_down, E * d, F, kTcBM, kTcBK) &&
+              make_map_bf16(&h->tm_h, ws.h16, Tm * (k + 1), Fmax, kTcBN, kTcBK) &&
+              make_map_bf16(&h->tm_xp, ws.xp, Tm * k, d, kTcBN, kTcBK);
+    if (ok && Fs > 0)
+      ok = make_map_bf16(&h->tm_sg, w->ws_gate, Fs, d, kTcBM, kTcBK) &&
+           make_map_bf16(&h->tm_su, w->ws_up, Fs, d, kTcBM, kTcBK) &&
+           make_map_bf16(&h->tm_sd, w->ws_down, d, Fs, kTcBM, kTcBK);
+    if (!ok) {
+      if (c.path == MOE_PATH_TC) {
+        cudaFree(h->block);
+        delete h;
+        return MOE_ERR_CUDA;
+      }
+      h->tc_capable = false;
+    }
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_destroy(moe_handle h) {
+  if (!h) return MOE_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  for (cudaEvent_t ev : h->prof.ev) cudaEventDestroy(ev);
+  cudaError_t f = cudaFree(h->block);
+  delete h;
+  return (e == cudaSuccess && f == cudaSuccess) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_route(moe_handle h, const void* x, int32_t T, int32_t* idx, float* gate, int32_t* counts,
+                     cudaStream_t stream) {
+  moe_status st = check_call(h, x, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!idx || !gate) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(gate) & 3u) ||
+      (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(route_args(h, x, T, idx, gate, counts, false), h->num_sms, stream, &h->prof));
+}
+
+moe_status moe_forward(moe_handle h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
+                       cudaStream_t stream) {
+  moe_status st = check_call(h, x, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!y || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  const size_t nb = (size_t)T * h->cfg.d * act_bytes(h->cfg);
+  if (ranges_overlap(x, nb, y, nb)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx_out) & 3u) || (reinterpret_cast<uintptr_t>(gate_out) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  return run_forward(h, x, T, y, idx_out, gate_out, stream);
+}
+
+moe_status moe_forward_host(moe_handle h, const void* x_host, int32_t T, void* y_host, cudaStream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  const size_t nb = (size_t)T * h->cfg.d * act_bytes(h->cfg);
+  cudaError_t e = cudaMemcpyAsync(h->ws.x_stage, x_host, nb, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status st = run_forward(h, h->ws.x_stage, T, h->ws.y_stage, nullptr, nullptr, stream);
+  if (st != MOE_OK) return st;
+  e = cudaMemcpyAsync(y_host, h->ws.y_stage, nb, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return cuda_status(e);
+}
+
+moe_status moe_get_grouping(moe_handle h, int32_t T, int32_t* offsets, int32_t* tok_of_slot, int32_t* slot_of,
+                            cudaStream_t stream) {
+  if (!h || T < 0 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  const size_t n = (size_t)T * h->cfg.top_k * 4;
+  cudaError_t e = cudaSuccess;
+  if (offsets)
+    e = cudaMemcpyAsync(offsets, h->ws.offsets, (h->cfg.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess && tok_of_slot && n)
+    e = cudaMemcpyAsync(tok_of_slot, h->ws.tok_of_slot, n, cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess && slot_of && n)
+    e = cudaMemcpyAsync(slot_of, h->ws.slot_of, n, cudaMemcpyDeviceToDevice, stream);
+  return cuda_status(e);
+}
+
+moe_status moe_check(moe_handle h, cudaStream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, h->ws.err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (word) {
+    e = cudaMemset(h->ws.err, 0, sizeof(word));
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+moe_status moe_debug_expire_wait(moe_handle h, int32_t timeout_us, cudaStream_t stream) {
+  if (!h || timeout_us < 1 || timeout_us > 5000000) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_wait(h->ws.err, (uint64_t)timeout_us * 1000ull, stream));
+}
+
+moe_status moe_profile_enable(moe_handle h, int32_t enable, int32_t max_launches) {
+  if (!h || (enable && (max_launches < 1 || max_launches > (1 << 20)))) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  for (cudaEvent_t ev : h->prof.ev) cudaEventDestroy(ev);
+  h->prof.ev.clear();
+  h->prof.kid.clear();
+  if (!enable) return MOE_OK;
+  h->prof.ev.resize(2 * (size_t)max_launches);
+  for (auto& ev : h->prof.ev) {
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+      cudaGetLastError();
+      ev = nullptr;
+      for (cudaEvent_t e : h->prof.ev)
+        if (e) cudaEventDestroy(e);
+      h->prof.ev.clear();
+      return MOE_ERR_CUDA;
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_handle h, float* ms, int32_t* launches) {
+  if (!h || !ms || !launches) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_K_COUNT; ++i) {
+    ms[i] = 0.f;
+    launches[i] = 0;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  for (size_t i = 0; i < h->prof.kid.size(); ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, h->prof.ev[2 * i], h->prof.ev[2 * i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+    ms[h->prof.kid[i]] += t;
+    launches[h->prof.kid[i]] += 1;
+  }
+  h->prof.kid.clear();
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,420 @@
+// Router, top-k selection and token-slot grouping.
+//
+// The gating network scores each token against every routed expert and keeps
+// a few of them (kongchang.com, section "Architecture: The 40B Total vs. 2.5B
+// Active Trade-off"; 256 experts, 6 per token: evermx.com review, section
+// "Sparse architecture").  Readings implemented here: fp32 logits
+// l = x.Wr + b, selection of the k largest logits with the lower index first
+// on ties, gates = softmax over the k selected logits.  The grouping puts the
+// token-slots of each expert next to each other, in (token, j) order, which is
+// what lets each expert's weights be streamed once per call.
+//
+// Two variants:
+//  * route_small (T <= 64): one warp per expert computes the logits of all
+//    tokens; the last CTA to finish (atomic ticket) selects, groups and
+//    writes everything.  One launch.
+//  * route_large: one CTA per 32 tokens computes all E logits of its tokens
+//    (fp32 SIMT tile), selects the top k and writes one selection-bitmap word
+//    per expert; the last CTA scans the bitmap into the grouping.
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kLargeBT = 32;     // tokens per CTA in route_large
+
+__device__ __forceinline__ void load_x4(const void* x, int act_bf16, size_t off, float (&v)[4]) {
+  if (act_bf16) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(x) + off));
+    v[0] = __uint_as_float(r.x << 16);
+    v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(r.y << 16);
+    v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+  } else {
+    const float4 r = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + off));
+    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// (value, index) order of the selection: larger value first, lower index on ties.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Top-k of one token's E logits by one warp.  vals[i] holds expert lane + 32 i.
+// Writes idx/gate for the token.  NaN logits are ordered below every number.
+template <int NPL>
+__device__ void warp_topk(float (&vals)[NPL], int E, int k, int32_t* idx_t, float* gate_t, int32_t* sidx_t) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;
+  float selv[kMaxTopK];
+  int seli[kMaxTopK];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (isnan(vals[i])) vals[i] = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && better(vals[i], e, bv, bi)) { bv = vals[i]; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    selv[j] = bv;
+    seli[j] = bi;
+  }
+  if (lane == 0) {
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) z += expf(selv[j] - selv[0]);
+    const float inv = 1.f / z;
+    for (int j = 0; j < k; ++j) {
+      idx_t[j] = seli[j];
+      gate_t[j] = expf(selv[j] - selv[0]) * inv;
+      if (sidx_t) sidx_t[j] = seli[j];
+    }
+  }
+}
+
+// Exclusive scan of n <= 4 * blockDim ints in shared memory, in place; returns the total.
+__device__ int block_exclusive_scan(int* a, int n) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int beg = min(n, tid * per), end = min(n, beg + per);
+  int s = 0;
+  for (int i = beg; i < end; ++i) s += a[i];
+  int incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    if (lane < nwarps) warp_tot[lane] = wi - w;
+    if (lane == 31) total = wi;
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - s;
+  for (int i = beg; i < end; ++i) {
+    const int v = a[i];
+    a[i] = run;
+    run += v;
+  }
+  __syncthreads();
+  return total;
+}
+
+// Everything after the counts are known: offsets, active-expert list, tcgen05
+// unit lists.  cnt: smem [E] counts; offs: smem [E + 1].  Runs in one CTA.
+__device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* scratch) {
+  const int E = a.E, tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) offs[e] = cnt[e];
+  __syncthreads();
+  const int total = block_exclusive_scan(offs, E);
+  if (tid == 0) offs[E] = total;
+  // active experts
+  for (int e = tid; e < E; e += blockDim.x) scratch[e] = cnt[e] > 0 ? 1 : 0;
+  __syncthreads();
+  const int n_act = block_exclusive_scan(scratch, E);
+  for (int e = tid; e < E; e += blockDim.x) {
+    if (cnt[e] > 0) a.ws.active[scratch[e]] = e;
+    a.ws.counts[e] = cnt[e];
+    a.ws.offsets[e] = offs[e];
+    if (a.counts_out) a.counts_out[e] = cnt[e];
+  }
+  if (tid == 0) {
+    a.ws.active[E] = n_act;
+    a.ws.offsets[E] = total;
+    a.ws.counts[E] = a.T;
+  }
+  __syncthreads();
+  if (!a.build_tc_units) return;
+  // tcgen05 units: shared expert first, then routed experts in index order.
+  const int mt_gu = a.F / kTcBM, mt_dn = a.d / kTcBM;
+  const int sh_tb = a.has_shared ? (a.T + kTcBN - 1) / kTcBN : 0;
+  const int sh_mt_gu = a.has_shared ? a.Fs / kTcBM : 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int mt = pass == 0 ? mt_gu : mt_dn;
+    const int sh_mt = pass == 0 ? sh_mt_gu : mt_dn;
+    TcUnit* out = pass == 0 ? a.ws.units_gu : a.ws.units_dn;
+    for (int e = tid; e < E; e += blockDim.x) scratch[e] = mt * ((cnt[e] + kTcBN - 1) / kTcBN);
+    __syncthreads();
+    const int n_routed = block_exclusive_scan(scratch, E);
+    const int sh_units = sh_mt * sh_tb;
+    for (int u = tid; u < sh_units; u += blockDim.x) {
+      const int tb = u / sh_mt, m = u % sh_mt;
+      out[u] = TcUnit{E, m, tb * kTcBN, min(kTcBN, a.T - tb * kTcBN)};
+    }
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int c = cnt[e];
+      int u = sh_units + scratch[e];
+      for (int tb = 0; tb * kTcBN < c; ++tb)
+        for (int m = 0; m < mt; ++m) out[u++] = TcUnit{e, m, offs[e] + tb * kTcBN, min(kTcBN, c - tb * kTcBN)};
+    }
+    if (tid == 0) a.ws.n_units[pass] = sh_units + n_routed;
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ small T
+__global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, d = a.d, T = a.T, k = a.k;
+  const int e = blockIdx.x * (kRouteThreads / 32) + warp;
+  if (e < E) {
+    const float* w = a.Wr + (size_t)e * d;
+    const float be = a.b ? a.b[e] : 0.f;
+    for (int t = 0; t < T; ++t) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int c = lane * 4; c < d; c += 128) {
+        const float4 wv = __ldg(reinterpret_cast<const float4*>(w + c));
+        float xv[4];
+        load_x4(a.x, a.act_bf16, (size_t)t * d + c, xv);
+        acc = fmaf(wv.x, xv[0], acc);
+        acc = fmaf(wv.y, xv[1], acc);
+        acc = fmaf(wv.z, xv[2], acc);
+        acc = fmaf(wv.w, xv[3], acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) a.ws.logits[(size_t)t * E + e] = acc + be;
+    }
+  }
+  // Last CTA to finish does the selection and grouping.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
+    s_last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ int32_t s_idx[kSmallT * kMaxTopK];
+  __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
+  __shared__ uint32_t bm[kMaxExperts][2];
+  for (int t = warp; t < T; t += kRouteThreads / 32) {
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int ee = lane + 32 * i;
+      v[i] = ee < E ? __ldcg(a.ws.logits + (size_t)t * E + ee) : -INFINITY;
+    }
+    warp_topk<kMaxExperts / 32>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + t * k);
+  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x) { cnt[i] = 0; bm[i][0] = 0; bm[i][1] = 0; }
+  __syncthreads();
+  for (int s = threadIdx.x; s < T * k; s += blockDim.x) {
+    const int ee = s_idx[s], t = s / k;
+    atomicAdd(&cnt[ee], 1);
+    atomicOr(&bm[ee][t >> 5], 1u << (t & 31));
+  }
+  __syncthreads();
+  finish_grouping(a, cnt, offs, scratch);
+  for (int s = threadIdx.x; s < T * k; s += blockDim.x) {
+    const int ee = s_idx[s], t = s / k, wd = t >> 5;
+    const int rank = (wd ? __popc(bm[ee][0]) : 0) + __popc(bm[ee][wd] & ((1u << (t & 31)) - 1u));
+    const int slot = offs[ee] + rank;
+    a.ws.tok_of_slot[slot] = t;
+    a.ws.src_of_slot[slot] = s;
+    a.ws.slot_of[s] = slot;
+  }
+  if (threadIdx.x == 0) a.ws.counters[0] = 0;
+}
+
+// ------------------------------------------------------------------ large T
+// Logit tile of 32 tokens x E experts: thread (ty, tx) owns tokens 4 ty .. 4 ty + 3
+// and experts 4 tx + 128 j .. + 3 for j < E / 128.
+template <int EJ>
+__global__ void __launch_bounds__(kRouteThreads) route_large_kernel(RouteArgs a) {
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) float dsm[];
+  const int E = a.E, d = a.d, T = a.T, k = a.k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kLargeBT;
+  const int Ep = EJ * 128;                  // E rounded up to 128
+  float* xs = dsm;                          // [32 tok][32 kk]
+  float* wsT = dsm + 32 * 32;               // [32 kk][Ep]
+  const int ty = tid >> 5, tx = tid & 31;
+  float acc[4][EJ][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < EJ; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
+
+  for (int k0 = 0; k0 < d; k0 += 32) {
+    // x tile: 32 tokens x 32 values
+    for (int i = tid; i < 32 * 8; i += kRouteThreads) {
+      const int tt = i >> 3, c4 = (i & 7) * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t0 + tt < T) load_x4(a.x, a.act_bf16, (size_t)(t0 + tt) * d + k0 + c4, v);
+      *reinterpret_cast<float4*>(xs + tt * 32 + c4) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    // router tile, transposed: wsT[kk][e]
+    for (int i = tid; i < Ep * 8; i += kRouteThreads) {
+      const int ee = i >> 3, c4 = (i & 7) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ee < E) v = __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)ee * d + k0 + c4));
+      wsT[(c4 + 0) * Ep + ee] = v.x;
+      wsT[(c4 + 1) * Ep + ee] = v.y;
+      wsT[(c4 + 2) * Ep + ee] = v.z;
+      wsT[(c4 + 3) * Ep + ee] = v.w;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < 32; ++kk) {
+      float xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs[(ty * 4 + i) * 32 + kk];
+#pragma unroll
+      for (int j = 0; j < EJ; ++j) {
+        const float4 wv = *reinterpret_cast<const float4*>(wsT + kk * Ep + 128 * j + 4 * tx);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i][j][0] = fmaf(xv[i], wv.x, acc[i][j][0]);
+          acc[i][j][1] = fmaf(xv[i], wv.y, acc[i][j][1]);
+          acc[i][j][2] = fmaf(xv[i], wv.z, acc[i][j][2]);
+          acc[i][j][3] = fmaf(xv[i], wv.w, acc[i][j][3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // logits to shared memory [32][Ep] (reuses the router tile space)
+  float* lg = wsT;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < EJ; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ee = 128 * j + 4 * tx + q;
+        lg[(ty * 4 + i) * Ep + ee] = acc[i][j][q] + ((ee < E && a.b) ? a.b[ee] : 0.f);
+      }
+  __shared__ uint32_t word[kMaxExperts];
+  __shared__ int32_t s_idx[kLargeBT * kMaxTopK];
+  for (int i = tid; i < E; i += kRouteThreads) word[i] = 0;
+  __syncthreads();
+  for (int tt = warp; tt < kLargeBT; tt += kRouteThreads / 32) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    float v[EJ * 4];
+#pragma unroll
+    for (int i = 0; i < EJ * 4; ++i) {
+      const int ee = lane + 32 * i;
+      v[i] = ee < E ? lg[tt * Ep + ee] : -INFINITY;
+    }
+    warp_topk<EJ * 4>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + tt * k);
+  }
+  __syncthreads();
+  for (int s = tid; s < kLargeBT * k; s += kRouteThreads) {
+    const int tt = s / k;
+    if (t0 + tt < T) atomicOr(&word[s_idx[s]], 1u << tt);
+  }
+  __syncthreads();
+  for (int i = tid; i < E; i += kRouteThreads) a.ws.sel[(size_t)blockIdx.x * E + i] = word[i];
+
+  // Last CTA: counts, word prefixes, offsets, slots.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
+    s_last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
+  const int nblk = gridDim.x;
+  int32_t* wpref = reinterpret_cast<int32_t*>(a.ws.sel) + (size_t)nblk * E;   // [nblk][E] prefixes
+  for (int ee = tid; ee < E; ee += kRouteThreads) {
+    int run = 0;
+    for (int bk = 0; bk < nblk; ++bk) {
+      wpref[(size_t)bk * E + ee] = run;
+      run += __popc(__ldcg(a.ws.sel + (size_t)bk * E + ee));
+    }
+    cnt[ee] = run;
+  }
+  __syncthreads();
+  finish_grouping(a, cnt, offs, scratch);
+  __threadfence_block();
+  for (int s = tid; s < T * k; s += kRouteThreads) {
+    const int t = s / k, bk = t >> 5;
+    const int ee = __ldcg(a.idx + s);
+    const uint32_t w = __ldcg(a.ws.sel + (size_t)bk * E + ee);
+    const int slot = offs[ee] + wpref[(size_t)bk * E + ee] + __popc(w & ((1u << (t & 31)) - 1u));
+    a.ws.tok_of_slot[slot] = t;
+    a.ws.src_of_slot[slot] = s;
+    a.ws.slot_of[s] = slot;
+  }
+  if (tid == 0) a.ws.counters[0] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
+  (void)num_sms;
+  if (prof) prof->begin(MOE_K_ROUTE, s);
+  if (a.T <= kSmallT) {
+    const int grid = (a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+    route_small_kernel<<<grid, kRouteThreads, 0, s>>>(a);
+    if (prof) prof->end(s);
+    return cudaGetLastError();
+  }
+  const int grid = (a.T + kLargeBT - 1) / kLargeBT;
+  const int ej = (a.E + 127) / 128;
+  const size_t smem = (32 * 32 + 32 * ej * 128) * sizeof(float);
+  switch (ej) {
+#define MOE_RL(N)                                                                                   \
+  case N: {                                                                                         \
+    static bool attr_set = false;  /* once, before any stream capture */                            \
+    if (!attr_set) {                                                                                \
+      if (cudaFuncSetAttribute(route_large_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                               (int)((32 * 32 + 32 * N * 128) * sizeof(float))) != cudaSuccess)     \
+        return cudaGetLastError();                                                                  \
+      attr_set = true;                                                                              \
+    }                                                                                               \
+    route_large_kernel<N><<<grid, kRouteThreads, smem, s>>>(a);                                     \
+    break;                                                                                          \
+  }
+    MOE_RL(1) MOE_RL(2) MOE_RL(3) MOE_RL(4)
+#undef MOE_RL
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (prof) prof->end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

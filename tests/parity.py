@@ -1,0 +1,86 @@
+"""Comparison of the CUDA layer's outputs with the CPU oracle.
+
+Tolerances (the layer's acceptance bounds):
+  - routed expert indices bit-exact for every token whose 6th/7th (k-th /
+    (k+1)-th) logit gap exceeds 1e-4; inside a near-tie the library's choice
+    must lie in the near-tied set, and that token's reference output is then
+    recomputed with the library's routing;
+  - gates within 2e-5 absolute of the float64 softmax of the same logits
+    (fp32 logits and an fp32 exp/divide: a few units of fp32 rounding);
+  - output max-abs <= 2e-2 and rel-L2 <= 1e-2 for bf16 weights, rel-L2 <=
+    5e-2 for NVFP4 weights; rel-L2 = ||y_gpu - y_ref||_2 / ||y_ref||_2.
+"""
+import numpy as np
+import torch
+
+from oracle.moe_oracle import LayerWeights, moe_forward_with_routing, router_logits, select_topk, topk_gates
+from oracle.moe_oracle import _widen
+
+GAP = 1e-4
+GATE_ATOL = 2e-5
+MAX_ABS = 2e-2
+REL_L2 = {"f32": 1e-2, "bf16": 1e-2, "nvfp4": 5e-2}
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def to_torch_x(x: np.ndarray, device="cuda") -> torch.Tensor:
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(x).to(device)
+
+
+def check_routing(l: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, k: int):
+    """Returns (idx_use, gate_use, n_near): the routing the reference output uses."""
+    T, E = l.shape
+    srt = -np.sort(-l, axis=1)
+    gap = srt[:, k - 1] - srt[:, k] if E > k else np.full(T, np.inf)
+    idx_ref = select_topk(l, k)
+    idx_use = idx_ref.copy()
+    n_near = 0
+    for t in range(T):
+        g = idx_gpu[t]
+        assert len(set(g.tolist())) == k and all(0 <= e < E for e in g), (t, g)
+        if gap[t] > GAP:
+            assert set(g.tolist()) == set(idx_ref[t].tolist()), (t, g, idx_ref[t], gap[t])
+        else:
+            n_near += 1
+            assert all(l[t, e] >= srt[t, k - 1] - GAP for e in g), (t, g)
+            idx_use[t] = g
+        # descending by logit up to the tie tolerance
+        lv = l[t, g]
+        assert np.all(lv[:-1] >= lv[1:] - 1e-5), (t, g, lv)
+    gate_use = topk_gates(l, idx_use)
+    # gates, matched by expert
+    for t in range(T):
+        ref = dict(zip(idx_use[t].tolist(), gate_use[t].tolist()))
+        for j in range(k):
+            e = int(idx_gpu[t, j])
+            if e in ref:
+                assert abs(gate_gpu[t, j] - ref[e]) <= GATE_ATOL, (t, j, gate_gpu[t, j], ref[e])
+    return idx_use, gate_use, n_near
+
+
+def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tensor, gate_gpu: torch.Tensor,
+                k: int, fmt: str, residual: bool = False, tokens=None):
+    """Full-layer parity on `tokens` (all when None). Returns a dict of error figures."""
+    W = LayerWeights(L)
+    xf = _widen(x)
+    sel = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
+    xs = xf[sel]
+    l = router_logits(xs, W.Wr, W.b)
+    ig = idx_gpu.cpu().numpy()[sel].astype(np.int64)
+    gg = gate_gpu.cpu().numpy()[sel].astype(np.float64)
+    idx_use, gate_use, n_near = check_routing(l, ig, gg, k)
+    y_ref = moe_forward_with_routing(xs, W, idx_use, gate_use, residual=residual)
+    yg = to_f64(y_gpu)[sel]
+    err = yg - y_ref
+    max_abs = float(np.max(np.abs(err)))
+    rel = float(np.linalg.norm(err) / max(np.linalg.norm(y_ref), 1e-30))
+    assert np.all(np.isfinite(yg))
+    assert max_abs <= MAX_ABS, (max_abs, rel)
+    assert rel <= REL_L2[fmt], (max_abs, rel)
+    return {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near}

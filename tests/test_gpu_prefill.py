@@ -1,0 +1,92 @@
+"""Prefill-sized batches (tcgen05 grouped-GEMM path) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from parity import check_layer, check_routing, to_torch_x
+from oracle.moe_oracle import LayerWeights, group_slots, router_logits
+from sparse_moe_transformer_02_b300 import binding as B
+from sparse_moe_transformer_02_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+SMALL = I.LayerSpec(d=256, ffn=256, shared_ffn=128, num_experts=16, top_k=4)
+NOSHARED = I.LayerSpec(d=256, ffn=128, shared_ffn=0, num_experts=8, top_k=2)
+
+
+def run(spec, dev, x_np, max_tokens, **kw):
+    layer = B.layer_from_spec(spec, dev, max_tokens, **kw)
+    x = to_torch_x(x_np)
+    T = x.shape[0]
+    y = torch.empty_like(x)
+    idx = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    layer.forward(x, y, idx, gate)
+    torch.cuda.synchronize()
+    assert layer.check() == B.MOE_OK
+    return layer, y, idx, gate
+
+
+@pytest.fixture(scope="module")
+def small():
+    L = I.make_layer(SMALL, seed=1)
+    return L, B.upload_layer(L)
+
+
+@pytest.mark.parametrize("T", [1, 17, 100, 300])
+def test_small_tc_path(small, T):
+    L, dev = small
+    x = I.make_tokens(SMALL, seed=T, T=T)
+    _, y, idx, gate = run(SMALL, dev, x, 300, path=B.MOE_PATH_TC)
+    r = check_layer(L, x, y, idx, gate, SMALL.top_k, "bf16")
+    print("small tc", T, r)
+
+
+def test_no_shared_expert_tc_and_gemv():
+    L = I.make_layer(NOSHARED, seed=2)
+    dev = B.upload_layer(L)
+    x = I.make_tokens(NOSHARED, seed=2, T=200)
+    for path in (B.MOE_PATH_TC, B.MOE_PATH_GEMV):
+        _, y, idx, gate = run(NOSHARED, dev, x, 200, path=path)
+        check_layer(L, x, y, idx, gate, NOSHARED.top_k, "bf16")
+
+
+def test_tc_and_gemv_paths_agree(flint_bf16):
+    spec, L, dev = flint_bf16
+    x = I.make_tokens(spec, seed=9, T=64)
+    _, y_tc, idx_tc, _ = run(spec, dev, x, 64, path=B.MOE_PATH_TC)
+    _, y_gv, idx_gv, gate = run(spec, dev, x, 64, path=B.MOE_PATH_GEMV)
+    assert torch.equal(idx_tc, idx_gv)
+    check_layer(L, x, y_tc, idx_gv, gate, spec.top_k, "bf16")
+    d = (y_tc.double() - y_gv.double()).norm() / y_gv.double().norm()
+    assert d < 1e-2
+
+
+def test_flint_prefill_4096(flint_bf16):
+    spec, L, dev = flint_bf16
+    T = 4096
+    x = I.make_tokens(spec, seed=4096, T=T)
+    layer, y, idx, gate = run(spec, dev, x, T)
+    # routing and grouping on every token, outputs on a seeded sample
+    W = LayerWeights(L)
+    l = router_logits(x.astype(np.float64) if x.dtype != np.uint16 else
+                      (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64), W.Wr, W.b)
+    ig = idx.cpu().numpy().astype(np.int64)
+    check_routing(l, ig, gate.cpu().numpy().astype(np.float64), spec.top_k)
+    offs, tos, so = layer.grouping(T, "cuda")
+    counts, offsets, tok_of_slot, slot_of = group_slots(ig, spec.num_experts)
+    assert np.array_equal(offs.cpu().numpy(), offsets)
+    assert np.array_equal(tos.cpu().numpy(), tok_of_slot)
+    assert np.array_equal(so.cpu().numpy(), slot_of)
+    sample = np.sort(np.random.default_rng(0).choice(T, 64, replace=False))
+    sample[-1] = T - 1
+    r = check_layer(L, x, y, idx, gate, spec.top_k, "bf16", tokens=sample)
+    print("flint prefill 4096", r)
+
+
+def test_flint_prefill_ragged_with_residual(flint_bf16):
+    spec, L, dev = flint_bf16
+    T = 1000
+    x = I.make_tokens(spec, seed=1000, T=T)
+    _, y, idx, gate = run(spec, dev, x, T, add_residual=True)
+    check_layer(L, x, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=np.arange(0, T, 31))
