@@ -256,6 +256,7 @@ def upload_layer(L: dict, device="cuda") -> dict:
 
 def layer_from_spec(spec, weights: dict, max_tokens: int, **kw) -> MoeLayer:
     """MoeLayer for an ``inputs.LayerSpec`` and device weights from ``upload_layer``."""
+    kw.setdefault("add_residual", spec.add_residual)
     return MoeLayer(d=spec.d, ffn=spec.ffn, shared_ffn=spec.shared_ffn, num_experts=spec.num_experts,
                     top_k=spec.top_k, max_tokens=max_tokens, act=spec.act, weight=spec.weight,
-                    weights=weights, add_residual=spec.add_residual, **kw)
+                    weights=weights, **kw)
