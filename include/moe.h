@@ -212,6 +212,32 @@ moe_status moe_profile_enable(moe_handle h, int32_t enable, int32_t max_launches
  */
 moe_status moe_profile_read(moe_handle h, float* ms, int32_t* launches);
 
+/*
+ * Routing without any device allocation (no counterpart on the pages).
+ *
+ * For callers that cannot call cudaMalloc -- plugins whose host process owns
+ * all device memory, runtimes that forbid allocation after start-up, or
+ * latency-critical paths that must not enter an allocator, which may
+ * synchronise the device -- and so cannot create a handle.  Computes what
+ * moe_route computes (same kernel and arithmetic): idx [T][k] int32, gate
+ * [T][k] fp32, and optionally counts [E] int32, from x [T][d] (act_dtype
+ * MOE_F32 or MOE_BF16, 16-byte aligned), router_w [E][d] fp32 (16-byte
+ * aligned) and router_b [E] fp32 or NULL.
+ *
+ * Limits: 1 <= T <= 64, E <= 512, k <= 8 (k <= E), d a multiple of 64; larger
+ * sizes return MOE_ERR_INVALID_ARG.  Scratch lives in one fixed array of about
+ * 144 KiB inside the library's device image; every device that loads the
+ * library holds it until the process exits.  The first call on a device looks
+ * up that array's device address (cudaGetSymbolAddress) once, so make the
+ * first call on each device before any stream capture.  All calls share the
+ * array and it keeps the last call's contents: calls that overlap on the GPU
+ * (other streams, other host threads) race and must be serialised.  Calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ */
+moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int32_t num_experts, int32_t top_k,
+                             int32_t act_dtype, const float* router_w, const float* router_b,
+                             int32_t* idx, float* gate, int32_t* counts, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

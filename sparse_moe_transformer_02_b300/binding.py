@@ -20,7 +20,7 @@ MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_TC = 0, 1, 2
 
 EXPORTED = ["moe_status_string", "moe_create", "moe_destroy", "moe_route", "moe_forward",
             "moe_forward_host", "moe_get_grouping", "moe_check", "moe_debug_expire_wait",
-            "moe_profile_enable", "moe_profile_read"]
+            "moe_profile_enable", "moe_profile_read", "moe_route_noalloc"]
 KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize"]
 
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_enable.argtypes = [vp, i32, i32]
         L.moe_profile_read.restype = ctypes.c_int
         L.moe_profile_read.argtypes = [vp, vp, vp]
+        L.moe_route_noalloc.restype = ctypes.c_int
+        L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -136,6 +138,13 @@ def moe_profile_read(h):
     cnt = (ctypes.c_int32 * n)()
     st = lib().moe_profile_read(h, ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p))
     return st, {KERNEL_NAMES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def moe_route_noalloc(x: int, T: int, d: int, num_experts: int, top_k: int, act_dtype: int, router_w: int,
+                      router_b: int, idx: int, gate: int, counts: int = 0, stream: int = 0) -> int:
+    """Routing with no device allocation (scratch in a fixed static array; see include/moe.h)."""
+    return lib().moe_route_noalloc(x, T, d, num_experts, top_k, act_dtype, router_w, router_b or None, idx, gate,
+                                   counts or None, stream)
 
 
 def _ok(st: int, what: str):
