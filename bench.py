@@ -207,7 +207,8 @@ def run_ours(args, rank, world, local_rank):
     handles = []
     with torch.cuda.stream(stream):
         for w in wts:
-            handles.append(B.layer_from_spec(spec, w, max_tokens=max(T, 64), stream=stream))
+            handles.append(B.layer_from_spec(spec, w, max_tokens=max(T, 64), stream=stream,
+                                             path={"auto": 0, "gemv": 1, "tc": 2}[args.path]))
     g = torch.Generator(device=device)
     g.manual_seed(args.seed + 77 + rank)
     x = (torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x).to(torch.bfloat16)
@@ -220,7 +221,7 @@ def run_ours(args, rank, world, local_rank):
         _, _, cnt = h.route(x, stream=stream)
         stream.synchronize()
         U.append(int((cnt > 0).sum().item()))
-    tc_path = T > 64 and kind == "bf16"
+    tc_path = kind == "bf16" and args.path != "gemv"
     kernels_per_fwd = 5 if tc_path else 3
 
     def step():
@@ -367,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
                           "experts": spec.num_experts, "shared_experts": 1, "top_k": spec.top_k,
                           "expert_ffn": spec.ffn, "weights": kind, "layers_per_step": n_layers,
                           "l2": f"inputs larger than L2: {n_layers} distinct layers' weights per step",
-                          "parallelism": f"replicas{world}"},
+                          "parallelism": f"replicas{world}", "path": args.path},
                "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": args.steps * n_layers * kernels_per_fwd, "clocks": clocks}
         if sweep:
@@ -455,6 +456,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -58,7 +58,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
 
 /* Which expert-FFN kernels moe_forward uses. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* weight-streaming GEMV for small T, tcgen05 grouped GEMM above it */
+  MOE_PATH_AUTO = 0,   /* tcgen05 grouped GEMM when the weights allow it (bf16), else the GEMV kernels */
   MOE_PATH_GEMV = 1,   /* always the weight-streaming GEMV kernels */
   MOE_PATH_TC = 2      /* always the tcgen05 grouped GEMM (bf16 weights and activations only) */
 } moe_path;
@@ -74,7 +74,7 @@ typedef struct {
   int32_t weight_dtype;  /* MOE_F32 (with F32 activations), MOE_BF16 or MOE_NVFP4 (with BF16 activations) */
   int32_t add_residual;  /* nonzero: y = x + moe(x) */
   int32_t path;          /* moe_path */
-  int32_t gemv_max_tokens; /* MOE_PATH_AUTO: T <= this uses the GEMV kernels; 0 = library default (64) */
+  int32_t gemv_max_tokens; /* MOE_PATH_AUTO: T <= this uses the GEMV kernels even when tcgen05 could; 0 = never */
   int32_t wait_timeout_ms; /* limit of every device-side spin wait; 0 = default (2000 ms) */
 } moe_config;
 

@@ -2,23 +2,29 @@
 //
 // Per generated token the selected experts' weights are read once, so decode
 // is bound by memory bandwidth (kongchang.com, section "125+ tokens/s: The
-// Practical Threshold for Local Inference").  These kernels therefore stream
-// each touched expert's rows exactly once per call and apply them to every
-// token routed to that expert (the grouping made by the router kernels).
+// Practical Threshold for Local Inference").  These kernels stream every
+// touched expert's weights exactly once per call and apply them to all the
+// tokens routed to that expert (the grouping made by the router kernels).
 //
-//  * gemv_gateup: one warp per (expert, FFN row f): the gate row and the up
-//    row are read with 16-byte loads, dotted with every routed token, and
-//    h[slot][f] = silu(g) * u is written in fp32.  The shared expert's rows
-//    come first and need no routing, so with programmatic dependent launch
-//    they are streamed while the router is still running.
-//  * gemv_down: one warp per (expert, 4 rows of Wd): partial outputs
-//    ypart[slot][row] = Wd[row] . h[slot] in fp32.  The last warp to finish a
+// Each SM runs one persistent CTA: warp 0 streams 8 KB units of weight rows
+// into a 16-stage shared-memory ring with 1-D bulk copies (cp.async.bulk,
+// completion counted on an mbarrier per stage), and eight consumer warps take
+// the units in turn, so up to 128 KB per SM are in flight whatever the
+// compute latency.  Units are handed out in contiguous ranges per CTA.
+//
+//  * gemv_gateup: a unit is RG row pairs (gate row f, up row f) of one
+//    expert.  For each routed token the consumer dots both rows with x and
+//    writes h[slot][f] = silu(g) * u (fp32).  The shared expert's units need
+//    no routing and come first, so with programmatic dependent launch they
+//    stream while the router is still running.
+//  * gemv_down: a unit is RD rows of Wd.  Partial outputs
+//    ypart[slot][row] = Wd[row] . h[slot] (fp32); the last unit to finish a
 //    block of 32 rows (atomic counter) combines them for every token:
-//    y[t][row] = sum_j gate[t][j] * ypart[slot(t, j)][row] + ypart[shared(t)][row]
-//    (+ x[t][row]), always in the same order, so the result is deterministic.
+//    y[t][row] = sum_j gate[t][j] ypart[slot(t, j)][row] + ypart[shared(t)][row]
+//    (+ x[t][row]), always in that order, so the result is deterministic.
 //
-// Weight formats: fp32 (with fp32 activations), bf16, NVFP4 (e2m1 values with
-// one e4m3 scale per 16 values and an fp32 scale per matrix, decoded in
+// Weight formats: fp32 (with fp32 activations), bf16, and NVFP4 (e2m1 codes,
+// an e4m3 scale per 16 values, an fp32 scale per matrix; decoded in
 // registers; the format is named on the evermx.com review, section
 // "Quantization").
 #include "moe_internal.cuh"
@@ -27,13 +33,22 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumers = 8;
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kStages = 16;
+constexpr int kUnitBytes = 8192;                  // weight bytes per unit
+constexpr int kStageBytes = kUnitBytes + 1024;    // + NVFP4 block scales
+constexpr uint32_t FULLMASK = 0xFFFFFFFFu;
+// Round-robin rings (unit i to consumer i % kConsumers, stage i % kStages) are
+// only safe when each stage has a single consumer: its parity waits can then
+// never be two phases stale.
+static_assert(kStages % kConsumers == 0, "a ring stage must belong to exactly one consumer warp");
 
 template <int WF> struct Fmt;
-template <> struct Fmt<MOE_F32>   { static constexpr int EPC = 4;  };   // elements per 16-byte chunk
-template <> struct Fmt<MOE_BF16>  { static constexpr int EPC = 8;  };
-template <> struct Fmt<MOE_NVFP4> { static constexpr int EPC = 32; };
+template <> struct Fmt<MOE_F32>   { static constexpr int EPC = 4;  static constexpr int XB = 16; };
+template <> struct Fmt<MOE_BF16>  { static constexpr int EPC = 8;  static constexpr int XB = 16; };
+template <> struct Fmt<MOE_NVFP4> { static constexpr int EPC = 32; static constexpr int XB = 64; };
+// EPC: elements per 16-byte weight chunk; XB: bytes of activations matching one chunk.
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
@@ -53,45 +68,35 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
   return __half22float2(h);
 }
 
-// Dot of one 16-byte weight chunk with the matching activations.
-// x points at the first activation of the chunk.  For NVFP4, sc holds the
-// two block scales of the chunk (already decoded) and the result excludes the
-// per-matrix scale.
-template <int WF>
-__device__ __forceinline__ float chunk_dot_x(const uint4& w, const void* x, float2 sc);
+// Activations matching one weight chunk, held in registers.
+template <int WF> struct XChunk { uint4 v[Fmt<WF>::XB / 16]; };
 
-template <>
-__device__ __forceinline__ float chunk_dot_x<MOE_F32>(const uint4& w, const void* x, float2) {
-  const float4 xv = __ldg(reinterpret_cast<const float4*>(x));
-  return __uint_as_float(w.x) * xv.x + __uint_as_float(w.y) * xv.y + __uint_as_float(w.z) * xv.z +
-         __uint_as_float(w.w) * xv.w;
+template <int WF>
+__device__ __forceinline__ void load_x(XChunk<WF>& c, const uint8_t* p) {
+#pragma unroll
+  for (int i = 0; i < Fmt<WF>::XB / 16; ++i) c.v[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
 }
-template <>
-__device__ __forceinline__ float chunk_dot_x<MOE_BF16>(const uint4& w, const void* x, float2) {
-  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x));
-  float s = bf_lo(w.x) * bf_lo(xv.x);
-  s = fmaf(bf_hi(w.x), bf_hi(xv.x), s);
-  s = fmaf(bf_lo(w.y), bf_lo(xv.y), s);
-  s = fmaf(bf_hi(w.y), bf_hi(xv.y), s);
-  s = fmaf(bf_lo(w.z), bf_lo(xv.z), s);
-  s = fmaf(bf_hi(w.z), bf_hi(xv.z), s);
-  s = fmaf(bf_lo(w.w), bf_lo(xv.w), s);
-  s = fmaf(bf_hi(w.w), bf_hi(xv.w), s);
-  return s;
+
+// Dot of a 16-byte weight chunk with its activations.  NVFP4: sc = the two
+// decoded block scales; the per-matrix scale is applied by the caller.
+__device__ __forceinline__ float cdot(const uint4& w, const XChunk<MOE_F32>& x, float2) {
+  const uint4 a = x.v[0];
+  float s = __uint_as_float(w.x) * __uint_as_float(a.x);
+  s = fmaf(__uint_as_float(w.y), __uint_as_float(a.y), s);
+  s = fmaf(__uint_as_float(w.z), __uint_as_float(a.z), s);
+  return fmaf(__uint_as_float(w.w), __uint_as_float(a.w), s);
 }
-template <>
-__device__ __forceinline__ float chunk_dot_x<MOE_NVFP4>(const uint4& w, const void* x, float2 sc) {
-  const uint4* xp = reinterpret_cast<const uint4*>(x);
+__device__ __forceinline__ float cdot(const uint4& w, const XChunk<MOE_NVFP4>& x, float2 sc) {
   const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
   float blk[2];
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {          // two 16-value blocks per chunk
+  for (int b = 0; b < 2; ++b) {
     float s = 0.f;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {        // 8 values = 4 bytes of codes, 16 bytes of activations
-      const uint4 xv = __ldg(xp + b * 2 + q);
-      const uint32_t cw = wv[b * 2 + q];
+    for (int q = 0; q < 2; ++q) {
+      const uint4 xv = x.v[b * 2 + q];
       const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t cw = wv[b * 2 + q];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 wf = e2m1x2_to_f2((cw >> (8 * i)) & 0xFFu);
@@ -101,35 +106,25 @@ __device__ __forceinline__ float chunk_dot_x<MOE_NVFP4>(const uint4& w, const vo
     }
     blk[b] = s;
   }
-  return blk[0] * sc.x + blk[1] * sc.y;
+  return fmaf(blk[0], sc.x, blk[1] * sc.y);
 }
 
-// Same, activations in fp32 registers-from-global (the intermediate h).
+// Activations of a chunk taken from the fp32 intermediate h.
+template <int WF> struct HChunk { float4 v[Fmt<WF>::EPC / 4]; };
+
 template <int WF>
-__device__ __forceinline__ float chunk_dot_h(const uint4& w, const float* h, float2 sc);
-
-template <>
-__device__ __forceinline__ float chunk_dot_h<MOE_F32>(const uint4& w, const float* h, float2) {
-  const float4 hv = *reinterpret_cast<const float4*>(h);
-  return __uint_as_float(w.x) * hv.x + __uint_as_float(w.y) * hv.y + __uint_as_float(w.z) * hv.z +
-         __uint_as_float(w.w) * hv.w;
+__device__ __forceinline__ void load_h(HChunk<WF>& c, const float* p) {
+#pragma unroll
+  for (int i = 0; i < Fmt<WF>::EPC / 4; ++i) c.v[i] = __ldg(reinterpret_cast<const float4*>(p) + i);
 }
-template <>
-__device__ __forceinline__ float chunk_dot_h<MOE_BF16>(const uint4& w, const float* h, float2) {
-  const float4 a = *reinterpret_cast<const float4*>(h);
-  const float4 b = *reinterpret_cast<const float4*>(h + 4);
-  float s = bf_lo(w.x) * a.x;
-  s = fmaf(bf_hi(w.x), a.y, s);
-  s = fmaf(bf_lo(w.y), a.z, s);
-  s = fmaf(bf_hi(w.y), a.w, s);
-  s = fmaf(bf_lo(w.z), b.x, s);
-  s = fmaf(bf_hi(w.z), b.y, s);
-  s = fmaf(bf_lo(w.w), b.z, s);
-  s = fmaf(bf_hi(w.w), b.w, s);
-  return s;
+__device__ __forceinline__ float hdot(const uint4& w, const HChunk<MOE_F32>& h, float2) {
+  const float4 a = h.v[0];
+  float s = __uint_as_float(w.x) * a.x;
+  s = fmaf(__uint_as_float(w.y), a.y, s);
+  s = fmaf(__uint_as_float(w.z), a.z, s);
+  return fmaf(__uint_as_float(w.w), a.w, s);
 }
-template <>
-__device__ __forceinline__ float chunk_dot_h<MOE_NVFP4>(const uint4& w, const float* h, float2 sc) {
+__device__ __forceinline__ float hdot(const uint4& w, const HChunk<MOE_NVFP4>& h, float2 sc) {
   const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
   float blk[2];
 #pragma unroll
@@ -137,10 +132,9 @@ __device__ __forceinline__ float chunk_dot_h<MOE_NVFP4>(const uint4& w, const fl
     float s = 0.f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint32_t cw = wv[b * 2 + q];
-      const float4 h0 = *reinterpret_cast<const float4*>(h + b * 16 + q * 8);
-      const float4 h1 = *reinterpret_cast<const float4*>(h + b * 16 + q * 8 + 4);
+      const float4 h0 = h.v[b * 4 + q * 2], h1 = h.v[b * 4 + q * 2 + 1];
       const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      const uint32_t cw = wv[b * 2 + q];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 wf = e2m1x2_to_f2((cw >> (8 * i)) & 0xFFu);
@@ -150,257 +144,786 @@ __device__ __forceinline__ float chunk_dot_h<MOE_NVFP4>(const uint4& w, const fl
     }
     blk[b] = s;
   }
-  return blk[0] * sc.x + blk[1] * sc.y;
+  return fmaf(blk[0], sc.x, blk[1] * sc.y);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
-// Row of a weight matrix in format WF: byte offset of element `col` of row `row`.
 template <int WF>
-__device__ __forceinline__ size_t row_bytes(int cols) {
-  return WF == MOE_F32 ? (size_t)cols * 4 : WF == MOE_BF16 ? (size_t)cols * 2 : (size_t)cols / 2;
+__host__ __device__ __forceinline__ int row_bytes(int cols) {
+  return WF == MOE_F32 ? cols * 4 : WF == MOE_BF16 ? cols * 2 : cols / 2;
+}
+
+// Contiguous share [lo, hi) of n items for CTA b of g.
+__device__ __forceinline__ void share(int n, int b, int g, int& lo, int& hi) {
+  lo = (int)(((long long)n * b) / g);
+  hi = (int)(((long long)n * (b + 1)) / g);
+}
+
+// Ring bookkeeping common to both kernels.
+struct Ring {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  int* abort_flag;
+};
+
+__device__ __forceinline__ Ring ring_setup(uint8_t* dsm) {
+  Ring r;
+  r.stages = dsm;
+  r.full = reinterpret_cast<uint64_t*>(dsm + kStages * kStageBytes);
+  r.empty = r.full + kStages;
+  r.abort_flag = reinterpret_cast<int*>(r.empty + kStages);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&r.full[i], 1);
+      mbar_init(&r.empty[i], 1);
+    }
+    *r.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  return r;
+}
+
+// Consumer-side warp-uniform bounded wait on a full stage.
+__device__ __forceinline__ bool warp_wait_full(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+  ok = __shfl_sync(FULLMASK, ok, 0);
+  if (ok)
+    while (!mbar_try_wait(bar, parity)) {
+    }
+  return ok != 0;
+}
+
+// Down-projection completion.  After a warp has written ypart for rows of the
+// 32-row block fb for the tokens of one expert, it counts those (token, block)
+// pairs; the warp that brings a pair to `target` (all of the token's experts
+// done for that block) combines the block for that token, always in the
+// order j = 0..k-1 then the shared expert:
+//   y[t][row] = sum_j gate[t][j] ypart[slot(t, j)][row] + ypart[shared(t)][row] (+ x[t][row])
+__device__ void complete_block(const GemvArgs& a, bool shared, int off, int n, int fb, int target) {
+  const int lane = threadIdx.x & 31;
+  const int nfb = a.d / kFinRows, T = a.T, k = a.k, d = a.d;
+  __threadfence();
+  __syncwarp();
+  for (int q0 = 0; q0 < n; q0 += 32) {
+    const int q = q0 + lane;
+    int t = -1;
+    bool last = false;
+    if (q < n) {
+      t = shared ? q : a.ws.tok_of_slot[off + q];
+      last = atomicAdd(&a.ws.fin[t * nfb + fb], 1u) == (unsigned)target - 1;
+    }
+    unsigned m = __ballot_sync(0xFFFFFFFFu, last);
+    if (m) __threadfence();
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      const int tt = __shfl_sync(0xFFFFFFFFu, t, src);
+      const int row = fb * kFinRows + lane;
+      float y = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int sl = __ldcg(a.ws.slot_of + tt * k + j);
+        y = fmaf(__ldcg(a.gate + tt * k + j), __ldcg(a.ws.ypart + (size_t)sl * d + row), y);
+      }
+      if (a.Fs > 0) y += __ldcg(a.ws.ypart + (size_t)(T * k + tt) * d + row);
+      if (a.act_bf16) {
+        if (a.add_residual) y += __bfloat162float(static_cast<const __nv_bfloat16*>(a.x)[(size_t)tt * d + row]);
+        static_cast<__nv_bfloat16*>(a.y)[(size_t)tt * d + row] = __float2bfloat16_rn(y);
+      } else {
+        if (a.add_residual) y += static_cast<const float*>(a.x)[(size_t)tt * d + row];
+        static_cast<float*>(a.y)[(size_t)tt * d + row] = y;
+      }
+      if (lane == 0) a.ws.fin[tt * nfb + fb] = 0;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ gate/up
-template <int WF, int NCH>
-__device__ void gateup_item(const GemvArgs& a, bool shared, int e, int f) {
-  constexpr int EPC = Fmt<WF>::EPC;
-  const int lane = threadIdx.x & 31;
-  const int d = a.d, rowsF = shared ? a.Fs : a.F;
-  const size_t rb = row_bytes<WF>(d);
-  const size_t ridx = shared ? (size_t)f : (size_t)e * rowsF + f;
-  const uint8_t* wg = static_cast<const uint8_t*>(shared ? a.sg : a.wg) + ridx * rb;
-  const uint8_t* wu = static_cast<const uint8_t*>(shared ? a.su : a.wu) + ridx * rb;
-  uint4 g[NCH], u[NCH];
-  float2 sg[NCH], su[NCH];
-#pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    const int col = (c * 32 + lane) * EPC;
-    g[c] = make_uint4(0, 0, 0, 0);
-    u[c] = make_uint4(0, 0, 0, 0);
-    sg[c] = su[c] = make_float2(0.f, 0.f);
-    if (col < d) {
-      g[c] = __ldcs(reinterpret_cast<const uint4*>(wg) + c * 32 + lane);
-      u[c] = __ldcs(reinterpret_cast<const uint4*>(wu) + c * 32 + lane);
-      if (WF == MOE_NVFP4) {
-        const uint8_t* scg = (shared ? a.ssc_g : a.sc_g) + ridx * (d / 16) + col / 16;
-        const uint8_t* scu = (shared ? a.ssc_u : a.sc_u) + ridx * (d / 16) + col / 16;
-        sg[c] = e4m3x2_to_f2(__ldcs(reinterpret_cast<const unsigned short*>(scg)));
-        su[c] = e4m3x2_to_f2(__ldcs(reinterpret_cast<const unsigned short*>(scu)));
-      }
-    }
-  }
-  float tg = 1.f, tu = 1.f;
-  if (WF == MOE_NVFP4) {
-    tg = shared ? a.tss_g[0] : a.ts_g[e];
-    tu = shared ? a.tss_u[0] : a.ts_u[e];
-  }
-  const int n = shared ? a.T : a.ws.counts[e];
-  const int off = shared ? 0 : a.ws.offsets[e];
-  const int Fmax = max(a.F, a.Fs);
-  const size_t xes = WF == MOE_F32 ? 4 : 2;
-  for (int i = 0; i < n; ++i) {
-    const int t = shared ? i : a.ws.tok_of_slot[off + i];
-    const int slot = shared ? a.T * a.k + i : off + i;
-    const uint8_t* xt = static_cast<const uint8_t*>(a.x) + (size_t)t * d * xes;
-    float ag = 0.f, au = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int col = (c * 32 + lane) * EPC;
-      if (col < d) {
-        ag += chunk_dot_x<WF>(g[c], xt + (size_t)col * xes, sg[c]);
-        au += chunk_dot_x<WF>(u[c], xt + (size_t)col * xes, su[c]);
-      }
-    }
-    // two-value reduction: lanes 0-15 end with sum(ag), 16-31 with sum(au)
-    const bool hi = lane & 16;
-    float v = (hi ? au : ag) + __shfl_xor_sync(0xFFFFFFFFu, hi ? ag : au, 16);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    const float su_ = __shfl_sync(0xFFFFFFFFu, v, 16);
-    if (lane == 0) a.ws.h32[(size_t)slot * Fmax + f] = silu(v * tg) * (su_ * tu);
-  }
-}
-
-template <int WF, int NCH>
-__global__ void __launch_bounds__(kThreads) gemv_gateup_kernel(GemvArgs a) {
+// J = 16-byte chunks per lane per row (row = d values), RG = row pairs per unit.
+template <int WF, int J>
+__global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, uint64_t wait_ns) {
+  constexpr int RG = 8 / J;
+  extern __shared__ __align__(128) uint8_t dsm[];
   pdl_launch_dependents();
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), nw = gridDim.x * kWarps;
-  const int n_sh = a.Fs;
-  int g = gw;
-  for (; g < n_sh; g += nw) gateup_item<WF, NCH>(a, true, 0, g);
-  pdl_wait();
-  const int n_act = a.ws.active[a.E];
-  const int total = n_sh + n_act * a.F;
-  for (; g < total; g += nw) {
-    const int r = g - n_sh;
-    gateup_item<WF, NCH>(a, false, a.ws.active[r / a.F], r % a.F);
+  const Ring ring = ring_setup(dsm);
+  const WaitCtl wc{wait_ns, a.ws.err, ring.abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, G = gridDim.x, b = blockIdx.x;
+  const int rb = row_bytes<WF>(d);                  // bytes of one row
+  const int sb = WF == MOE_NVFP4 ? d / 16 : 0;      // scale bytes of one row
+  const int n_sh = a.Fs / RG;                       // shared-expert units
+  const int upe = a.F / RG;                         // units per routed expert
+  const int n_sh_local = b < n_sh ? (n_sh - b + G - 1) / G : 0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    int i = 0;
+    bool ok = true;
+    int r_lo = 0, r_hi = 0;
+    for (;; ++i) {
+      bool shared;
+      int e = 0, f0;
+      if (i < n_sh_local) {
+        shared = true;
+        f0 = (b + i * G) * RG;
+      } else {
+        if (i == n_sh_local) {
+          pdl_wait();
+          share(a.ws.active[a.E] * upe, b, G, r_lo, r_hi);
+        }
+        const int u = r_lo + (i - n_sh_local);
+        if (u >= r_hi) break;
+        shared = false;
+        e = a.ws.active[u / upe];
+        f0 = (u % upe) * RG;
+      }
+      const int s = i % kStages;
+      if (!mbar_wait(&ring.empty[s], ((i / kStages) & 1) ^ 1, wc)) { ok = false; break; }
+      uint8_t* st = ring.stages + s * kStageBytes;
+      const size_t row0 = shared ? (size_t)f0 : (size_t)e * a.F + f0;
+      const uint8_t* g = static_cast<const uint8_t*>(shared ? a.sg : a.wg) + row0 * rb;
+      const uint8_t* u = static_cast<const uint8_t*>(shared ? a.su : a.wu) + row0 * rb;
+      mbar_arrive_expect_tx(&ring.full[s], 2 * RG * (rb + sb));
+      bulk_g2s_hint(st, g, RG * rb, &ring.full[s], pol);
+      bulk_g2s_hint(st + RG * rb, u, RG * rb, &ring.full[s], pol);
+      if (WF == MOE_NVFP4) {
+        bulk_g2s_hint(st + 2 * RG * rb, (shared ? a.ssc_g : a.sc_g) + row0 * sb, RG * sb, &ring.full[s], pol);
+        bulk_g2s_hint(st + 2 * RG * rb + RG * sb, (shared ? a.ssc_u : a.sc_u) + row0 * sb, RG * sb,
+                      &ring.full[s], pol);
+      }
+    }
+    if (!ok) {   // let the copies already issued land before the CTA leaves
+      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&ring.full[j % kStages], (j / kStages) & 1))
+          if (global_ns() - t0 > wait_ns) break;
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int Fmax = max(a.F, a.Fs);
+  int r_lo = 0, r_hi = 0;
+  bool have_range = false;
+  for (int i = cw;; i += kConsumers) {
+    bool shared;
+    int e = 0, f0;
+    if (i < n_sh_local) {
+      shared = true;
+      f0 = (b + i * G) * RG;
+    } else {
+      if (!have_range) {
+        pdl_wait();
+        share(a.ws.active[a.E] * upe, b, G, r_lo, r_hi);
+        have_range = true;
+      }
+      const int u = r_lo + (i - n_sh_local);
+      if (u >= r_hi) break;
+      shared = false;
+      e = a.ws.active[u / upe];
+      f0 = (u % upe) * RG;
+    }
+    const int s = i % kStages;
+    if (!warp_wait_full(&ring.full[s], (i / kStages) & 1, wc)) break;
+    const uint8_t* st = ring.stages + s * kStageBytes;
+    // bf16 / fp32: the unit's weights move to registers and the stage is freed
+    // at once.  NVFP4: they are read from the stage at each use (the decoded
+    // form would not fit in registers) and the stage is freed after the tokens.
+    constexpr bool HOLD = WF != MOE_NVFP4;
+    uint4 wg[HOLD ? RG : 1][J], wu[HOLD ? RG : 1][J];
+    if constexpr (HOLD) {
+#pragma unroll
+      for (int p = 0; p < RG; ++p)
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          wg[p][j] = reinterpret_cast<const uint4*>(st + p * rb)[j * 32 + lane];
+          wu[p][j] = reinterpret_cast<const uint4*>(st + (RG + p) * rb)[j * 32 + lane];
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+    }
+    float tg = 1.f, tu = 1.f;
+    if (WF == MOE_NVFP4) {
+      tg = shared ? a.tss_g[0] : a.ts_g[e];
+      tu = shared ? a.tss_u[0] : a.ts_u[e];
+    }
+    const int n = shared ? a.T : a.ws.counts[e];
+    const int off = shared ? 0 : a.ws.offsets[e];
+    for (int q = 0; q < n; ++q) {
+      const int t = shared ? q : a.ws.tok_of_slot[off + q];
+      const int slot = shared ? a.T * a.k + q : off + q;
+      const uint8_t* xt = static_cast<const uint8_t*>(a.x) + (size_t)t * d * (WF == MOE_F32 ? 4 : 2);
+      XChunk<WF> xc[J];
+#pragma unroll
+      for (int j = 0; j < J; ++j) load_x<WF>(xc[j], xt + (size_t)(j * 32 + lane) * Fmt<WF>::XB);
+      float v[2 * RG];
+#pragma unroll
+      for (int p = 0; p < RG; ++p) {
+        float ag = 0.f, au = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          if constexpr (HOLD) {
+            ag += cdot(wg[p][j], xc[j], make_float2(0.f, 0.f));
+            au += cdot(wu[p][j], xc[j], make_float2(0.f, 0.f));
+          } else {
+            const int c = j * 32 + lane;
+            const float2 sg = e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + p * sb + c * 2));
+            const float2 su =
+                e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + (RG + p) * sb + c * 2));
+            ag += cdot(reinterpret_cast<const uint4*>(st + p * rb)[c], xc[j], sg);
+            au += cdot(reinterpret_cast<const uint4*>(st + (RG + p) * rb)[c], xc[j], su);
+          }
+        }
+        v[2 * p] = ag * tg;
+        v[2 * p + 1] = au * tu;
+      }
+      const float r = transpose_reduce<2 * RG, 32>(v, lane);
+      // lane l holds value (l >> SH): gate of pair p at 2p, up at 2p + 1
+      constexpr int SH = (2 * RG == 2) ? 4 : (2 * RG == 4) ? 3 : (2 * RG == 8) ? 2 : 1;
+      const float up = __shfl_down_sync(FULLMASK, r, 1 << SH);
+      const int idx = lane >> SH;
+      if ((lane & ((1 << SH) - 1)) == 0 && (idx & 1) == 0)
+        a.ws.h32[(size_t)slot * Fmax + f0 + (idx >> 1)] = silu(r) * up;
+    }
+    if constexpr (!HOLD) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+    }
   }
 }
 
 // ------------------------------------------------------------------ down + combine
-template <int WF, int NCHD>
-__device__ void down_item(const GemvArgs& a, bool shared, int e, int rg, int n_items_per_fin) {
+// CPR = 16-byte chunks per Wd row (row = F values); a unit is 512 chunks:
+// RD = 512 / CPR rows.  CPR >= 32: each lane holds JD = CPR / 32 chunk columns
+// of all RD rows.  CPR == 16: half-warps split the rows.
+template <int WF, int CPR>
+__global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint64_t wait_ns) {
+  constexpr int RD = 512 / CPR;
+  constexpr int SPLIT = CPR < 32;                    // half-warps on different rows
+  constexpr int JD = SPLIT ? 1 : CPR / 32;            // chunk columns per lane
+  constexpr int NR = SPLIT ? 16 : RD;                // rows per lane
+  constexpr int LW = SPLIT ? 16 : 32;                // lanes sharing one row
   constexpr int EPC = Fmt<WF>::EPC;
-  const int lane = threadIdx.x & 31;
-  const int d = a.d, K = shared ? a.Fs : a.F;     // row length of Wd
-  const size_t rb = row_bytes<WF>(K);
-  const int cpr = K / EPC;                         // 16-byte chunks per row
-  const int r0 = rg * kDownRPW;
-  const size_t row0 = shared ? (size_t)r0 : (size_t)e * d + r0;
-  const uint8_t* wd = static_cast<const uint8_t*>(shared ? a.sd : a.wd) + row0 * rb;
-  uint4 w[NCHD];
-  float2 sc[NCHD];
-  int rl[NCHD], col[NCHD];
-#pragma unroll
-  for (int i = 0; i < NCHD; ++i) {
-    const int q = i * 32 + lane;
-    rl[i] = q / cpr;
-    col[i] = (q % cpr) * EPC;
-    w[i] = make_uint4(0, 0, 0, 0);
-    sc[i] = make_float2(0.f, 0.f);
-    if (rl[i] < kDownRPW) {
-      w[i] = __ldcs(reinterpret_cast<const uint4*>(wd + (size_t)rl[i] * rb) + (q % cpr));
-      if (WF == MOE_NVFP4) {
-        const uint8_t* s = (shared ? a.ssc_d : a.sc_d) + (row0 + rl[i]) * (K / 16) + col[i] / 16;
-        sc[i] = e4m3x2_to_f2(__ldcs(reinterpret_cast<const unsigned short*>(s)));
+  extern __shared__ __align__(128) uint8_t dsm[];
+  pdl_launch_dependents();
+  const Ring ring = ring_setup(dsm);
+  const WaitCtl wc{wait_ns, a.ws.err, ring.abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, F = a.F, G = gridDim.x, b = blockIdx.x;
+  const int rb = row_bytes<WF>(F);
+  const int sb = WF == MOE_NVFP4 ? F / 16 : 0;
+  const int upe = d / RD;                            // units per expert
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  pdl_wait();
+  const int n_exp = a.ws.active[a.E] + has_sh;       // shared expert first
+  int u_lo, u_hi;
+  share(n_exp * upe, b, G, u_lo, u_hi);
+
+  if (warp == 0) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    int i = 0;
+    bool ok = true;
+    for (int u = u_lo; u < u_hi; ++u, ++i) {
+      const int ai = u / upe, r0 = (u % upe) * RD;
+      const bool shared = has_sh && ai == 0;
+      const int e = shared ? 0 : a.ws.active[ai - has_sh];
+      const size_t row0 = shared ? (size_t)r0 : (size_t)e * d + r0;
+      const int s = i % kStages;
+      if (!mbar_wait(&ring.empty[s], ((i / kStages) & 1) ^ 1, wc)) { ok = false; break; }
+      uint8_t* st = ring.stages + s * kStageBytes;
+      mbar_arrive_expect_tx(&ring.full[s], RD * (rb + sb));
+      bulk_g2s_hint(st, static_cast<const uint8_t*>(shared ? a.sd : a.wd) + row0 * rb, RD * rb, &ring.full[s],
+                    pol);
+      if (WF == MOE_NVFP4)
+        bulk_g2s_hint(st + RD * rb, (shared ? a.ssc_d : a.sc_d) + row0 * sb, RD * sb, &ring.full[s], pol);
+    }
+    if (!ok) {
+      for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(&ring.full[j % kStages], (j / kStages) & 1))
+          if (global_ns() - t0 > wait_ns) break;
       }
     }
+    return;
   }
-  const float ts = WF == MOE_NVFP4 ? (shared ? a.tss_d[0] : a.ts_d[e]) : 1.f;
-  const int n = shared ? a.T : a.ws.counts[e];
-  const int off = shared ? 0 : a.ws.offsets[e];
+
+  const int cw = warp - 1;
   const int Fmax = max(a.F, a.Fs);
-  const bool hi = lane & 16, b3 = lane & 8;
-  for (int i = 0; i < n; ++i) {
-    const int slot = shared ? a.T * a.k + i : off + i;
-    const float* h = a.ws.h32 + (size_t)slot * Fmax;
-    float acc[kDownRPW] = {0.f, 0.f, 0.f, 0.f};
+  const int col_lane = SPLIT ? (lane & 15) : lane;   // chunk column of this lane (plus 32 j)
+  const int row_lane = SPLIT ? (lane >> 4) : 0;      // first row of this lane (SPLIT: every other row)
+  for (int i = cw; u_lo + i < u_hi; i += kConsumers) {
+    const int u = u_lo + i;
+    const int ai = u / upe, r0 = (u % upe) * RD;
+    const bool shared = has_sh && ai == 0;
+    const int e = shared ? 0 : a.ws.active[ai - has_sh];
+    const int s = i % kStages;
+    if (!warp_wait_full(&ring.full[s], (i / kStages) & 1, wc)) break;
+    const uint8_t* st = ring.stages + s * kStageBytes;
+    constexpr bool HOLD = WF != MOE_NVFP4;     // as in gemv_gateup
+    uint4 w[HOLD ? NR : 1][JD];
+    if constexpr (HOLD) {
 #pragma unroll
-    for (int c = 0; c < NCHD; ++c) {
-      if (rl[c] < kDownRPW) {
-        const float s = chunk_dot_h<WF>(w[c], h + col[c], sc[c]);
-        acc[0] += rl[c] == 0 ? s : 0.f;
-        acc[1] += rl[c] == 1 ? s : 0.f;
-        acc[2] += rl[c] == 2 ? s : 0.f;
-        acc[3] += rl[c] == 3 ? s : 0.f;
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int j = 0; j < JD; ++j)
+          w[r][j] = reinterpret_cast<const uint4*>(st + (SPLIT ? row_lane + 2 * r : r) * rb)[j * 32 + col_lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+    }
+    const float ts = WF == MOE_NVFP4 ? (shared ? a.tss_d[0] : a.ts_d[e]) : 1.f;
+    const int n = shared ? a.T : a.ws.counts[e];
+    const int off = shared ? 0 : a.ws.offsets[e];
+    for (int q = 0; q < n; ++q) {
+      const int slot = shared ? a.T * a.k + q : off + q;
+      const float* h = a.ws.h32 + (size_t)slot * Fmax;
+      HChunk<WF> hc[JD];
+#pragma unroll
+      for (int j = 0; j < JD; ++j) load_h<WF>(hc[j], h + (j * 32 + col_lane) * EPC);
+      float v[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float acc = 0.f;
+        const int row = SPLIT ? row_lane + 2 * r : r;
+#pragma unroll
+        for (int j = 0; j < JD; ++j) {
+          const int c = j * 32 + col_lane;
+          if constexpr (HOLD) {
+            acc += hdot(w[r][j], hc[j], make_float2(0.f, 0.f));
+          } else {
+            const float2 sc = e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + RD * rb + row * sb + c * 2));
+            acc += hdot(reinterpret_cast<const uint4*>(st + row * rb)[c], hc[j], sc);
+          }
+        }
+        v[r] = acc * ts;
+      }
+      const float tot = transpose_reduce<NR, LW>(v, lane);
+      constexpr int SH = (LW == 32) ? (NR == 4 ? 3 : NR == 8 ? 2 : NR == 16 ? 1 : 0) : (NR == 16 ? 0 : 1);
+      const int li = (lane & (LW - 1)) >> SH;         // value index held by this lane
+      if ((lane & ((1 << SH) - 1)) == 0) {
+        const int row = SPLIT ? row_lane + 2 * li : li;
+        a.ws.ypart[(size_t)slot * d + r0 + row] = tot;
       }
     }
-    // four-value reduction: lane (16 h + 8 b) ends with row 2 h + b
-    const float r0v = __shfl_xor_sync(0xFFFFFFFFu, hi ? acc[0] : acc[2], 16);
-    const float r1v = __shfl_xor_sync(0xFFFFFFFFu, hi ? acc[1] : acc[3], 16);
-    const float p0 = (hi ? acc[2] : acc[0]) + r0v;
-    const float p1 = (hi ? acc[3] : acc[1]) + r1v;
-    float v = (b3 ? p1 : p0) + __shfl_xor_sync(0xFFFFFFFFu, b3 ? p0 : p1, 8);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    if ((lane & 7) == 0) a.ws.ypart[(size_t)slot * d + r0 + (hi ? 2 : 0) + (b3 ? 1 : 0)] = v * ts;
-  }
-  // Count this item towards its 32-row block; the last one combines the block.
-  __threadfence();
-  __syncwarp();
-  const int fb = r0 / kFinRows;
-  unsigned prev = 0;
-  if (lane == 0) prev = atomicAdd(&a.ws.counters[1 + fb], 1u);
-  prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-  if (prev != (unsigned)n_items_per_fin - 1) return;
-  __threadfence();
-  const int row = fb * kFinRows + lane;
-  const int T = a.T, k = a.k;
-  for (int t = 0; t < T; ++t) {
-    float y = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int s = a.ws.slot_of[t * k + j];
-      y = fmaf(a.gate[t * k + j], __ldcg(a.ws.ypart + (size_t)s * d + row), y);
+    if constexpr (!HOLD) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
     }
-    if (a.Fs > 0) y += __ldcg(a.ws.ypart + (size_t)(T * k + t) * d + row);
-    if (a.act_bf16) {
-      const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(a.x);
-      if (a.add_residual) y += __bfloat162float(xb[(size_t)t * d + row]);
-      static_cast<__nv_bfloat16*>(a.y)[(size_t)t * d + row] = __float2bfloat16_rn(y);
-    } else {
-      const float* xf = static_cast<const float*>(a.x);
-      if (a.add_residual) y += xf[(size_t)t * d + row];
-      static_cast<float*>(a.y)[(size_t)t * d + row] = y;
-    }
+    // Units never straddle a 32-row block: each of a token's experts
+    // contributes 32 / RD units to it.
+    complete_block(a, shared, off, n, r0 / kFinRows, (a.k + has_sh) * (kFinRows / RD));
   }
-  if (lane == 0) a.ws.counters[1 + fb] = 0;
 }
 
-template <int WF, int NCHD>
-__global__ void __launch_bounds__(kThreads) gemv_down_kernel(GemvArgs a) {
+// ------------------------------------------------------------------ bf16: tensor-core GEMV
+// For bf16 weights the dot products run on the tensor pipe (mma.sync
+// m16n8k16, fp32 accumulate): 16 weight rows x 16 values of A from the stage
+// via ldmatrix, 8 tokens x 16 values of B from the activations, so a unit
+// costs a few dozen instructions instead of several per weight.  A unit is
+// 16 row segments of 256 values (512 bytes each, one bulk copy per segment,
+// rows padded to 528 bytes in the stage so ldmatrix rows hit distinct banks).
+// A row group (16 rows) takes K / 256 consecutive units, handed to the same
+// consumer warp; the eight consumers work on eight row groups at a time with
+// their units interleaved in the ring.
+constexpr int kRowPad = 528;
+constexpr int kKc = 256;            // values per row segment
+constexpr int kMaxNT = kGemvChunkT / 8;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Row groups of one CTA: the shared expert's (round-robin over CTAs, need no
+// routing) then a contiguous share of the routed ones, in batches of up to 8
+// (one per consumer warp).  Units of a batch are ordered (segment, group).
+struct RgSeq {
+  int n_sh_local, G, b, per_exp, r_lo, r_hi;
+};
+
+// Runs the unit sequence: the producer (consumer == -1) issues each unit, a
+// consumer warp c processes the row groups handed to it.  `issue(c, shared, e,
+// g, kc)` issues segment kc of row group g for consumer c; `group(shared, e,
+// g)` processes a whole row group.  Each consumer owns two ring stages (see
+// kStagesPerConsumer), so a stage is only ever used by one consumer, in order.
+template <typename Issue, typename Group>
+__device__ bool rg_walk(RgSeq& q, int consumer, int KC, const GemvArgs& a, Issue&& issue, Group&& group) {
+  for (int phase = 0; phase < 2; ++phase) {
+    int lo, hi;
+    if (phase == 0) {
+      lo = 0;
+      hi = q.n_sh_local;
+    } else {
+      pdl_wait();
+      share(a.ws.active[a.E] * q.per_exp, q.b, q.G, q.r_lo, q.r_hi);
+      lo = q.r_lo;
+      hi = q.r_hi;
+    }
+    for (int bs = lo; bs < hi; bs += kConsumers) {
+      const int nb = min(kConsumers, hi - bs);
+      if (consumer < 0) {
+        for (int kc = 0; kc < KC; ++kc)
+          for (int r = 0; r < nb; ++r) {
+            const int u = bs + r;
+            const bool sh = phase == 0;
+            const int e = sh ? 0 : a.ws.active[u / q.per_exp];
+            const int g = sh ? q.b + u * q.G : u % q.per_exp;
+            if (!issue(r, sh, e, g, kc)) return false;
+          }
+      } else if (consumer < nb) {
+        const int u = bs + consumer;
+        const bool sh = phase == 0;
+        const int e = sh ? 0 : a.ws.active[u / q.per_exp];
+        const int g = sh ? q.b + u * q.G : u % q.per_exp;
+        if (!group(sh, e, g)) return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Per-consumer stage ownership: consumer c uses stages 2c and 2c + 1 for its
+// m-th unit alternately (stage 2c + (m & 1), phase parity (m >> 1) & 1).
+constexpr int kStagesPerConsumer = kStages / kConsumers;
+static_assert(kStagesPerConsumer == 2, "the ring gives each consumer warp two stages");
+struct StageOwner {
+  int m[kConsumers];
+  uint32_t last_par[kStages];
+  uint32_t used;
+};
+__device__ __forceinline__ void owner_init(StageOwner& o) {
+  for (int c = 0; c < kConsumers; ++c) o.m[c] = 0;
+  o.used = 0;
+}
+// Producer: wait for consumer c's next stage to be free; returns its index or -1.
+__device__ __forceinline__ int owner_next(StageOwner& o, int c, uint64_t* empty, const WaitCtl& wc) {
+  const int m = o.m[c]++;
+  const int s = c * kStagesPerConsumer + (m & 1);
+  if (!mbar_wait(&empty[s], ((m >> 1) & 1) ^ 1, wc)) return -1;
+  o.last_par[s] = (m >> 1) & 1;
+  o.used |= 1u << s;
+  return s;
+}
+// Producer after an abort: let the copies already issued land.
+__device__ __forceinline__ void owner_drain(const StageOwner& o, uint64_t* full, uint64_t wait_ns) {
+  for (int s = 0; s < kStages; ++s)
+    if (o.used & (1u << s)) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&full[s], o.last_par[s]))
+        if (global_ns() - t0 > wait_ns) break;
+    }
+}
+
+// gate/up: row group g = gate rows 8g..8g+7 (A rows 0-7) and up rows 8g..8g+7
+// (A rows 8-15); D rows 0-7 / 8-15 of the same thread are gate / up of the
+// same row and token, so SwiGLU happens in registers.
+__global__ void __launch_bounds__(kThreads, 1) gemv_mma_gateup_kernel(GemvArgs a, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t dsm[];
   pdl_launch_dependents();
-  pdl_wait();
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), nw = gridDim.x * kWarps;
-  const int n_rg = a.d / kDownRPW;
+  const Ring ring = ring_setup(dsm);
+  const WaitCtl wc{wait_ns, a.ws.err, ring.abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, KC = d / kKc, G = gridDim.x, b = blockIdx.x;
+  const int n_sh = a.Fs / 8;
+  RgSeq q{b < n_sh ? (n_sh - b + G - 1) / G : 0, G, b, a.F / 8, 0, 0};
+  if (warp == 0) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    StageOwner own;
+    owner_init(own);
+    auto issue = [&](int c, bool sh, int e, int g, int kc) -> bool {
+      const int s = owner_next(own, c, ring.empty, wc);
+      if (s < 0) return false;
+      uint8_t* st = ring.stages + s * kStageBytes;
+      const size_t row0 = sh ? (size_t)g * 8 : (size_t)e * a.F + (size_t)g * 8;
+      const __nv_bfloat16* gw = static_cast<const __nv_bfloat16*>(sh ? a.sg : a.wg) + row0 * d + kc * kKc;
+      const __nv_bfloat16* uw = static_cast<const __nv_bfloat16*>(sh ? a.su : a.wu) + row0 * d + kc * kKc;
+      mbar_arrive_expect_tx(&ring.full[s], 16 * kKc * 2);
+      for (int r = 0; r < 8; ++r) {
+        bulk_g2s_hint(st + r * kRowPad, gw + (size_t)r * d, kKc * 2, &ring.full[s], pol);
+        bulk_g2s_hint(st + (8 + r) * kRowPad, uw + (size_t)r * d, kKc * 2, &ring.full[s], pol);
+      }
+      return true;
+    };
+    auto none = [](bool, int, int) { return true; };
+    if (!rg_walk(q, -1, KC, a, issue, none)) owner_drain(own, ring.full, wait_ns);
+    return;
+  }
+  const int cw = warp - 1;
+  const int Fmax = max(a.F, a.Fs);
+  const uint32_t lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;   // ldmatrix row / column
+  auto none = [](int, bool, int, int, int) { return true; };
+  int m = 0;                                   // units this consumer has taken
+  auto group = [&](bool sh, int e, int g) -> bool {
+    const int n = sh ? a.T : a.ws.counts[e];
+    const int off = sh ? 0 : a.ws.offsets[e];
+    const int ntiles = (n + 7) >> 3;
+    const __nv_bfloat16* xrow[kMaxNT];
+#pragma unroll
+    for (int nt = 0; nt < kMaxNT; ++nt) {
+      int tok = nt * 8 + (lane >> 2);
+      tok = tok < n ? tok : 0;
+      const int t = sh ? tok : a.ws.tok_of_slot[off + tok];
+      xrow[nt] = static_cast<const __nv_bfloat16*>(a.x) + (size_t)t * d + (lane & 3) * 2;
+    }
+    float acc[kMaxNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int kc = 0; kc < KC; ++kc, ++m) {
+      const int s = cw * kStagesPerConsumer + (m & 1);
+      if (!warp_wait_full(&ring.full[s], (m >> 1) & 1, wc)) return false;
+      const uint32_t st = smem_u32(ring.stages + s * kStageBytes) + lrow * kRowPad + lcol * 2;
+#pragma unroll 4
+      for (int kk = 0; kk < kKc / 16; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(st + kk * 32, af);
+        const int k = kc * kKc + kk * 16;
+#pragma unroll
+        for (int nt = 0; nt < kMaxNT; ++nt)
+          if (nt < ntiles) {
+            const uint32_t b0 = __ldg(reinterpret_cast<const uint32_t*>(xrow[nt] + k));
+            const uint32_t b1 = __ldg(reinterpret_cast<const uint32_t*>(xrow[nt] + k + 8));
+            mma_bf16(acc[nt], af, b0, b1);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[s]);
+    }
+    const int f = g * 8 + (lane >> 2);
+#pragma unroll
+    for (int nt = 0; nt < kMaxNT; ++nt)
+      if (nt < ntiles) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tok = nt * 8 + (lane & 3) * 2 + c;
+          if (tok < n) {
+            const int slot = sh ? a.T * a.k + tok : off + tok;
+            a.ws.h16[(size_t)slot * Fmax + f] = __float2bfloat16_rn(silu(acc[nt][c]) * acc[nt][2 + c]);
+          }
+        }
+      }
+    return true;
+  };
+  rg_walk(q, cw, KC, a, none, group);
+}
+
+// down: row group g = Wd rows 16g..16g+15 of one expert; K = F (then F / 256
+// segments); B = h (bf16) of the expert's slots.
+__global__ void __launch_bounds__(kThreads, 1) gemv_mma_down_kernel(GemvArgs a, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  pdl_launch_dependents();
+  const Ring ring = ring_setup(dsm);
+  const WaitCtl wc{wait_ns, a.ws.err, ring.abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, F = a.F, G = gridDim.x, b = blockIdx.x;
+  const int kd = F < kKc ? F : kKc, KC = F / kd, pad = kd * 2 + 16;   // segment values, segments, row pitch
   const int has_sh = a.Fs > 0 ? 1 : 0;
+  pdl_wait();
+  // All row groups need h, so there is no early phase: the shared expert's
+  // groups join the contiguous split (routed index offset by one expert).
   const int n_exp = a.ws.active[a.E] + has_sh;
-  const int per_fin = n_exp * (kFinRows / kDownRPW);
-  for (int g = gw; g < n_exp * n_rg; g += nw) {
-    const int ai = g / n_rg, rg = g % n_rg;
-    if (has_sh && ai == 0)
-      down_item<WF, NCHD>(a, true, 0, rg, per_fin);
-    else
-      down_item<WF, NCHD>(a, false, a.ws.active[ai - has_sh], rg, per_fin);
+  const int total = n_exp * (d / 16);
+  int lo, hi;
+  share(total, b, G, lo, hi);
+  auto expert_of = [&](int u, bool& sh, int& e, int& g) {
+    const int ai = u / (d / 16);
+    sh = has_sh && ai == 0;
+    e = sh ? 0 : a.ws.active[ai - has_sh];
+    g = u % (d / 16);
+  };
+  if (warp == 0) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    StageOwner own;
+    owner_init(own);
+    bool ok = true;
+    for (int bs = lo; bs < hi && ok; bs += kConsumers) {
+      const int nb = min(kConsumers, hi - bs);
+      for (int kc = 0; kc < KC && ok; ++kc)
+        for (int r = 0; r < nb; ++r) {
+          bool sh;
+          int e, g;
+          expert_of(bs + r, sh, e, g);
+          const int s = owner_next(own, r, ring.empty, wc);
+          if (s < 0) { ok = false; break; }
+          uint8_t* st = ring.stages + s * kStageBytes;
+          const size_t row0 = sh ? (size_t)g * 16 : (size_t)e * d + (size_t)g * 16;
+          const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(sh ? a.sd : a.wd) + row0 * F + kc * kd;
+          mbar_arrive_expect_tx(&ring.full[s], 16 * kd * 2);
+          for (int rr = 0; rr < 16; ++rr) bulk_g2s_hint(st + rr * pad, w + (size_t)rr * F, kd * 2, &ring.full[s], pol);
+        }
+    }
+    if (!ok) owner_drain(own, ring.full, wait_ns);
+    return;
+  }
+  const int cw = warp - 1;
+  const int Fmax = max(a.F, a.Fs);
+  const uint32_t lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
+  int m = 0;                                   // units this consumer has taken
+  for (int bs = lo; bs < hi; bs += kConsumers) {
+    const int nb = min(kConsumers, hi - bs);
+    if (cw < nb) {
+      bool sh;
+      int e, g;
+      expert_of(bs + cw, sh, e, g);
+      const int n = sh ? a.T : a.ws.counts[e];
+      const int off = sh ? 0 : a.ws.offsets[e];
+      const int ntiles = (n + 7) >> 3;
+      const __nv_bfloat16* hrow[kMaxNT];
+#pragma unroll
+      for (int nt = 0; nt < kMaxNT; ++nt) {
+        int tok = nt * 8 + (lane >> 2);
+        tok = tok < n ? tok : 0;
+        const int slot = sh ? a.T * a.k + tok : off + tok;
+        hrow[nt] = a.ws.h16 + (size_t)slot * Fmax + (lane & 3) * 2;
+      }
+      float acc[kMaxNT][4];
+#pragma unroll
+      for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      bool ok = true;
+      for (int kc = 0; kc < KC; ++kc, ++m) {
+        const int s = cw * kStagesPerConsumer + (m & 1);
+        if (!warp_wait_full(&ring.full[s], (m >> 1) & 1, wc)) { ok = false; break; }
+        const uint32_t st = smem_u32(ring.stages + s * kStageBytes) + lrow * pad + lcol * 2;
+#pragma unroll 4
+        for (int kk = 0; kk < kd / 16; ++kk) {
+          uint32_t af[4];
+          ldsm_x4(st + kk * 32, af);
+          const int k = kc * kd + kk * 16;
+#pragma unroll
+          for (int nt = 0; nt < kMaxNT; ++nt)
+            if (nt < ntiles) {
+              const uint32_t b0 = __ldg(reinterpret_cast<const uint32_t*>(hrow[nt] + k));
+              const uint32_t b1 = __ldg(reinterpret_cast<const uint32_t*>(hrow[nt] + k + 8));
+              mma_bf16(acc[nt], af, b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[s]);
+      }
+      if (!ok) return;
+      const int r = g * 16 + (lane >> 2);
+#pragma unroll
+      for (int nt = 0; nt < kMaxNT; ++nt)
+        if (nt < ntiles) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tok = nt * 8 + (lane & 3) * 2 + c;
+            if (tok < n) {
+              const int slot = sh ? a.T * a.k + tok : off + tok;
+              a.ws.ypart[(size_t)slot * d + r] = acc[nt][c];
+              a.ws.ypart[(size_t)slot * d + r + 8] = acc[nt][2 + c];
+            }
+          }
+        }
+      // each of a token's experts brings two 16-row groups to a 32-row block
+      complete_block(a, sh, off, n, (g * 16) / kFinRows, (a.k + has_sh) * (kFinRows / 16));
+    }
   }
 }
+
+constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kStages * 8 + 16;
 
 template <typename K>
-cudaError_t launch_pdl(K kernel, int grid, cudaStream_t s, const GemvArgs& a) {
+cudaError_t launch_pdl(K kernel, int grid, cudaStream_t s, const GemvArgs& a, uint64_t wait_ns) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a, wait_ns);
 }
 
-template <int WF, int NCH, int NCHD>
-cudaError_t launch_fmt(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
-  static int occ_gu = 0, occ_dn = 0;
-  if (!occ_gu) {
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_gu, gemv_gateup_kernel<WF, NCH>, kThreads, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_dn, gemv_down_kernel<WF, NCHD>, kThreads, 0);
-    occ_gu = occ_gu < 1 ? 1 : occ_gu;
-    occ_dn = occ_dn < 1 ? 1 : occ_dn;
+cudaError_t launch_mma(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
+  static bool attr_set = false;   // set once, before any stream capture
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_mma_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
   if (prof) prof->begin(MOE_K_GEMV_GATEUP, s);
-  cudaError_t e = launch_pdl(gemv_gateup_kernel<WF, NCH>, num_sms * occ_gu, s, a);
+  cudaError_t e = launch_pdl(gemv_mma_gateup_kernel, num_sms, s, a, wait_ns);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   if (prof) prof->begin(MOE_K_GEMV_DOWN, s);
-  e = launch_pdl(gemv_down_kernel<WF, NCHD>, num_sms * occ_dn, s, a);
+  e = launch_pdl(gemv_mma_down_kernel, num_sms, s, a, wait_ns);
+  if (prof) prof->end(s);
+  return e;
+}
+
+template <int WF, int J, int CPR>
+cudaError_t launch_fmt(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
+  static bool attr_set = false;   // set once, before any stream capture
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_gateup_kernel<WF, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_down_kernel<WF, CPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (prof) prof->begin(MOE_K_GEMV_GATEUP, s);
+  cudaError_t e = launch_pdl(gemv_gateup_kernel<WF, J>, num_sms, s, a, wait_ns);
+  if (prof) prof->end(s);
+  if (e != cudaSuccess) return e;
+  if (prof) prof->begin(MOE_K_GEMV_DOWN, s);
+  e = launch_pdl(gemv_down_kernel<WF, CPR>, num_sms, s, a, wait_ns);
   if (prof) prof->end(s);
   return e;
 }
 
 }  // namespace
 
-// Chunks of 16 bytes per lane: gate/up rows hold d values, down rows hold F
-// values, four rows per warp item.
-cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int num_sms, cudaStream_t s, Prof* prof) {
-  const int row_b = wfmt == MOE_F32 ? a.d * 4 : wfmt == MOE_BF16 ? a.d * 2 : a.d / 2;
-  const int nch = (row_b + 511) / 512;
-  const int kmax = a.F > a.Fs ? a.F : a.Fs;
-  const int drow_b = wfmt == MOE_F32 ? kmax * 4 : wfmt == MOE_BF16 ? kmax * 2 : kmax / 2;
-  const int nchd = (kDownRPW * drow_b + 511) / 512;
-#define MOE_G(WF, A, B) \
-  if (nch <= A && nchd <= B) return launch_fmt<WF, A, B>(a, num_sms, s, prof);
+bool gemv_supported(int wfmt, int d, int F, int Fs) {
+  if (Fs != 0 && Fs != F) return false;
+  if (wfmt == MOE_BF16) return d % kKc == 0 && (F % kKc == 0 || F == 128) && d % kFinRows == 0;
+  const int rb = wfmt == MOE_F32 ? d * 4 : wfmt == MOE_BF16 ? d * 2 : d / 2;
+  const int fb = wfmt == MOE_F32 ? F * 4 : wfmt == MOE_BF16 ? F * 2 : F / 2;
+  if (rb % 512 != 0) return false;
+  const int J = rb / 512;
+  if (J != 1 && J != 2 && J != 4 && J != 8) return false;
+  const int cpr = fb / 16;
+  if (fb % 16 != 0 || (cpr != 16 && cpr != 32 && cpr != 64 && cpr != 128)) return false;
+  const int rg = 8 / J;
+  if (F % rg != 0 || Fs % rg != 0 || d % (512 / cpr) != 0) return false;
+  return true;
+}
+
+cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
+  const int rb = wfmt == MOE_F32 ? a.d * 4 : wfmt == MOE_BF16 ? a.d * 2 : a.d / 2;
+  const int J = rb / 512;
+  const int cpr = (wfmt == MOE_F32 ? a.F * 4 : wfmt == MOE_BF16 ? a.F * 2 : a.F / 2) / 16;
+#define MOE_G(WF, JJ, CC) \
+  if (J == JJ && cpr == CC) return launch_fmt<WF, JJ, CC>(a, num_sms, s, prof, wait_ns);
+#define MOE_GF(WF, JJ) MOE_G(WF, JJ, 16) MOE_G(WF, JJ, 32) MOE_G(WF, JJ, 64) MOE_G(WF, JJ, 128)
   if (wfmt == MOE_BF16) {
-    MOE_G(MOE_BF16, 4, 4) MOE_G(MOE_BF16, 8, 8) MOE_G(MOE_BF16, 16, 16)
+    return launch_mma(a, num_sms, s, prof, wait_ns);
   } else if (wfmt == MOE_F32) {
-    MOE_G(MOE_F32, 4, 4) MOE_G(MOE_F32, 8, 8) MOE_G(MOE_F32, 16, 16)
+    MOE_GF(MOE_F32, 1) MOE_GF(MOE_F32, 2) MOE_GF(MOE_F32, 4) MOE_GF(MOE_F32, 8)
   } else {
-    MOE_G(MOE_NVFP4, 2, 2) MOE_G(MOE_NVFP4, 4, 4) MOE_G(MOE_NVFP4, 8, 8)
+    MOE_GF(MOE_NVFP4, 1) MOE_GF(MOE_NVFP4, 2) MOE_GF(MOE_NVFP4, 4) MOE_GF(MOE_NVFP4, 8)
   }
+#undef MOE_GF
 #undef MOE_G
   return cudaErrorInvalidValue;
 }

@@ -15,6 +15,7 @@ struct moe_layer {
   int device = 0;
   int num_sms = 0;
   bool tc_capable = false;
+  bool gemv_capable = false;
   uint64_t wait_ns = 0;
   int max_units_gu = 0, max_units_dn = 0;
   CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp;
@@ -28,14 +29,7 @@ inline size_t act_bytes(const moe_config& c) { return c.act_dtype == MOE_F32 ? 4
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Largest 16-byte chunk counts the GEMV kernels are built for (see gemv.cu).
-bool gemv_shape_ok(const moe_config& c) {
-  const int kmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
-  const int es2 = c.weight_dtype == MOE_F32 ? 8 : c.weight_dtype == MOE_BF16 ? 4 : 1;  // 2 x bytes/elem
-  const int row_b = c.d * es2 / 2, drow_b = kDownRPW * kmax * es2 / 2;
-  const int cap = c.weight_dtype == MOE_NVFP4 ? 8 : 16;
-  return (row_b + 511) / 512 <= cap && (drow_b + 511) / 512 <= cap;
-}
+bool gemv_shape_ok(const moe_config& c) { return gemv_supported(c.weight_dtype, c.d, c.ffn, c.shared_ffn); }
 
 bool tc_shape_ok(const moe_config& c) {
   return c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.d % kTcBM == 0 && c.ffn % kTcBM == 0 &&
@@ -53,8 +47,10 @@ moe_status validate_config(const moe_config* c) {
   const bool combo = (c->act_dtype == MOE_F32 && c->weight_dtype == MOE_F32) ||
                      (c->act_dtype == MOE_BF16 && (c->weight_dtype == MOE_BF16 || c->weight_dtype == MOE_NVFP4));
   if (!combo) return MOE_ERR_UNSUPPORTED;
-  if (!gemv_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
-  if (c->path == MOE_PATH_TC && !tc_shape_ok(*c)) return MOE_ERR_UNSUPPORTED;
+  const bool gemv = gemv_shape_ok(*c), tc = tc_shape_ok(*c);
+  if (!gemv && !tc) return MOE_ERR_UNSUPPORTED;
+  if (c->path == MOE_PATH_TC && !tc) return MOE_ERR_UNSUPPORTED;
+  if (c->path == MOE_PATH_GEMV && !gemv) return MOE_ERR_UNSUPPORTED;
   if ((long long)c->max_tokens * c->top_k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -72,11 +68,11 @@ moe_status validate_weights(const moe_config& c, const moe_weights* w) {
   if (c.weight_dtype == MOE_NVFP4) {
     const void* s[] = {w->s_gate, w->s_up, w->s_down, w->t_gate, w->t_up, w->t_down};
     for (const void* p : s)
-      if (!p || (reinterpret_cast<uintptr_t>(p) & 1u)) return MOE_ERR_INVALID_ARG;
+      if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
     if (c.shared_ffn > 0) {
       const void* ss[] = {w->ss_gate, w->ss_up, w->ss_down, w->ts_gate, w->ts_up, w->ts_down};
       for (const void* p : ss)
-        if (!p || (reinterpret_cast<uintptr_t>(p) & 1u)) return MOE_ERR_INVALID_ARG;
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
     }
   }
   return MOE_OK;
@@ -179,8 +175,11 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
   const moe_config& c = h->cfg;
   int32_t* idx = idx_out ? idx_out : h->ws.idx;
   float* gate = gate_out ? gate_out : h->ws.gate;
-  const int gemv_max = c.gemv_max_tokens > 0 ? c.gemv_max_tokens : kSmallT;
-  const bool tc = c.path == MOE_PATH_TC || (c.path == MOE_PATH_AUTO && h->tc_capable && T > gemv_max);
+  // AUTO: the tensor-core path whenever the weights allow it (it streams the
+  // weights faster than the GEMV kernels at every batch size measured), unless
+  // the caller asked for GEMV up to gemv_max_tokens.
+  const bool tc = c.path == MOE_PATH_TC ||
+                  (c.path == MOE_PATH_AUTO && h->tc_capable && (T > c.gemv_max_tokens || !h->gemv_capable));
   if (tc) {
     moe_status st = cuda_status(launch_route(route_args(h, x, T, idx, gate, nullptr, true), h->num_sms, s, &h->prof));
     if (st != MOE_OK) return st;
@@ -211,7 +210,7 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
     float* gc = gate + (size_t)t0 * c.top_k;
     moe_status st = cuda_status(launch_route(route_args(h, xc, tc_, ic, gc, nullptr, false), h->num_sms, s, &h->prof));
     if (st != MOE_OK) return st;
-    st = cuda_status(launch_gemv(gemv_args(h, xc, yc, gc, tc_), c.weight_dtype, h->num_sms, s, &h->prof));
+    st = cuda_status(launch_gemv(gemv_args(h, xc, yc, gc, tc_), c.weight_dtype, h->num_sms, s, &h->prof, h->wait_ns));
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
@@ -256,7 +255,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
   h->tc_capable = tc_shape_ok(c) && cc_major == 10;
-  if (c.path == MOE_PATH_TC && !h->tc_capable) {
+  h->gemv_capable = gemv_shape_ok(c);
+  if ((c.path == MOE_PATH_TC && !h->tc_capable) || (!h->tc_capable && !h->gemv_capable)) {
     delete h;
     return MOE_ERR_UNSUPPORTED;
   }
@@ -287,11 +287,12 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.units_dn, (size_t)(h->max_units_dn > 0 ? h->max_units_dn : 1) * sizeof(TcUnit)},
       {(void**)&ws.n_units, 2 * 4},
       {(void**)&ws.h32, Tg * (k + 1) * Fmax * 4},
-      {(void**)&ws.h16, h->tc_capable ? Tm * (k + 1) * Fmax * 2 : 16},
+      {(void**)&ws.h16, (h->tc_capable ? Tm : Tg) * (k + 1) * Fmax * 2},
       {(void**)&ws.xp, h->tc_capable ? Tm * k * d * 2 : 16},
       {(void**)&ws.ypart, Tg * (k + 1) * d * 4},
       {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
-      {(void**)&ws.counters, (1 + d / kFinRows + 64) * 4},
+      {(void**)&ws.counters, 64 * 4},
+      {(void**)&ws.fin, Tg * (d / kFinRows) * 4},
       {(void**)&ws.err, 16},
       {&ws.x_stage, Tm * d * act_bytes(c)},
       {&ws.y_stage, Tm * d * act_bytes(c)},
@@ -310,7 +311,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
     off += up256(p.bytes);
   }
   // Counters and the error word start at zero; the rest is written before it is read.
-  cudaError_t e = cudaMemsetAsync(ws.counters, 0, (1 + d / kFinRows + 64) * 4, stream);
+  cudaError_t e = cudaMemsetAsync(ws.counters, 0, 64 * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.fin, 0, Tg * (d / kFinRows) * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.err, 0, 16, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {

@@ -14,9 +14,8 @@ namespace moe {
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 8;
 constexpr int kSmallT = 64;          // largest T the single-kernel small-batch router handles
-constexpr int kGemvChunkT = 256;     // GEMV path: tokens per pass (longer batches run in passes)
+constexpr int kGemvChunkT = 64;      // GEMV path: tokens per pass (longer batches run in passes)
 constexpr int kFinRows = 32;         // GEMV down: rows finalised together by the last contributor
-constexpr int kDownRPW = 4;          // GEMV down: rows per warp item
 constexpr int kTcBN = 128;           // tcgen05 path: largest token tile (MMA N)
 constexpr int kTcBM = 128;           // tcgen05 path: weight rows per tile (MMA M)
 constexpr int kTcBK = 64;            // tcgen05 path: reduction step per stage (128 bytes of bf16)
@@ -44,11 +43,12 @@ struct Workspace {
   TcUnit* units_dn;       // tcgen05 down units
   int32_t* n_units;       // [2] unit counts (gate/up, down)
   float* h32;             // [min(max_T, kGemvChunkT) * (k + 1)][F_max] GEMV intermediate
-  __nv_bfloat16* h16;     // [max_T * (k + 1)][F_max] tcgen05 intermediate
+  __nv_bfloat16* h16;     // [max(max_T, ...) * (k + 1)][F_max] bf16 intermediate (tcgen05 and bf16 GEMV)
   __nv_bfloat16* xp;      // [max_T * k][d] tcgen05 slot-ordered copy of the routed activations
   float* ypart;           // [min(max_T, kGemvChunkT) * (k + 1)][d] GEMV down partials
   float* yacc;            // [max_T][d] tcgen05 fp32 accumulator
-  uint32_t* counters;     // router ticket + GEMV finalisation counters
+  uint32_t* counters;     // router ticket
+  uint32_t* fin;          // [kGemvChunkT][d / 32] GEMV down completion counts (kept at zero between calls)
   unsigned int* err;      // device error word
   void* x_stage;          // [max_T][d] moe_forward_host staging
   void* y_stage;
@@ -110,7 +110,11 @@ struct GemvArgs {
 
 // Launchers (return the launch status).
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof);
-cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int num_sms, cudaStream_t s, Prof* prof);
+cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns);
+// Shapes the GEMV kernels are built for: rows of d values span 1, 2, 4 or 8
+// x 512 bytes; rows of F values span 16, 32, 64 or 128 chunks of 16 bytes;
+// the shared expert, if any, has the routed width.
+bool gemv_supported(int wfmt, int d, int F, int Fs);
 cudaError_t launch_debug_wait(unsigned int* err, uint64_t limit_ns, cudaStream_t s);
 
 struct TcArgs {

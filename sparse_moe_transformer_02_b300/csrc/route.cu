@@ -38,12 +38,6 @@ __device__ __forceinline__ void load_x4(const void* x, int act_bf16, size_t off,
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
 // (value, index) order of the selection: larger value first, lower index on ties.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -182,37 +176,87 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
 }
 
 // ------------------------------------------------------------------ small T
+// grid (ceil(E / 8), ceil(T / 8)): warp w of CTA (bx, by) scores expert 8 bx + w
+// against tokens 8 by .. 8 by + 7, whose activations are staged in shared memory.
+constexpr int kSmallTok = 8;
+
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
   pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t xs[];     // [8][d] activations (f32 or bf16)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, d = a.d, T = a.T, k = a.k;
+  const int t0 = blockIdx.y * kSmallTok;
+  const int nt = min(kSmallTok, T - t0);
+  const int es = a.act_bf16 ? 2 : 4;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.x) + (size_t)t0 * d * es);
+    const int n16 = nt * d * es / 16;
+    for (int i = threadIdx.x; i < n16; i += kRouteThreads) reinterpret_cast<uint4*>(xs)[i] = __ldg(src + i);
+  }
+  __syncthreads();
   const int e = blockIdx.x * (kRouteThreads / 32) + warp;
   if (e < E) {
     const float* w = a.Wr + (size_t)e * d;
-    const float be = a.b ? a.b[e] : 0.f;
-    for (int t = 0; t < T; ++t) {
-      float acc = 0.f;
-#pragma unroll 8
-      for (int c = lane * 4; c < d; c += 128) {
-        const float4 wv = __ldg(reinterpret_cast<const float4*>(w + c));
-        float xv[4];
-        load_x4(a.x, a.act_bf16, (size_t)t * d + c, xv);
-        acc = fmaf(wv.x, xv[0], acc);
-        acc = fmaf(wv.y, xv[1], acc);
-        acc = fmaf(wv.z, xv[2], acc);
-        acc = fmaf(wv.w, xv[3], acc);
+    float acc[kSmallTok];
+#pragma unroll
+    for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
+#pragma unroll 4
+    for (int c = lane * 4; c < d; c += 128) {
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(w + c));
+#pragma unroll
+      for (int t = 0; t < kSmallTok; ++t) {
+        if (t < nt) {
+          float xv[4];
+          if (a.act_bf16) {
+            const uint2 r = *reinterpret_cast<const uint2*>(xs + ((size_t)t * d + c) * 2);
+            xv[0] = __uint_as_float(r.x << 16);
+            xv[1] = __uint_as_float(r.x & 0xFFFF0000u);
+            xv[2] = __uint_as_float(r.y << 16);
+            xv[3] = __uint_as_float(r.y & 0xFFFF0000u);
+          } else {
+            const float4 r = *reinterpret_cast<const float4*>(xs + ((size_t)t * d + c) * 4);
+            xv[0] = r.x; xv[1] = r.y; xv[2] = r.z; xv[3] = r.w;
+          }
+          acc[t] = fmaf(wv.x, xv[0], acc[t]);
+          acc[t] = fmaf(wv.y, xv[1], acc[t]);
+          acc[t] = fmaf(wv.z, xv[2], acc[t]);
+          acc[t] = fmaf(wv.w, xv[3], acc[t]);
+        }
       }
-      acc = warp_sum(acc);
-      if (lane == 0) a.ws.logits[(size_t)t * E + e] = acc + be;
     }
+    const float tot = transpose_reduce<kSmallTok, 32>(acc, lane);    // lane l: token l >> 2
+    const int tt = lane >> 2;
+    if ((lane & 3) == 0 && tt < nt) a.ws.logits[(size_t)(t0 + tt) * E + e] = tot + (a.b ? a.b[e] : 0.f);
   }
-  // Last CTA to finish does the selection and grouping.
+  // Two-level tail.  The last of the expert-chunk CTAs of this token chunk
+  // selects the chunk's tokens (one warp per token); the last of those does
+  // the grouping for all tokens.
   __shared__ int s_last;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
+    const unsigned ticket = atomicAdd(&a.ws.counters[1 + blockIdx.y], 1u);
     s_last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < nt) {
+    const int t = t0 + warp;
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int ee = lane + 32 * i;
+      v[i] = ee < E ? __ldcg(a.ws.logits + (size_t)t * E + ee) : -INFINITY;
+    }
+    warp_topk<kMaxExperts / 32>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, nullptr);
+  }
+  if (threadIdx.x == 0) a.ws.counters[1 + blockIdx.y] = 0;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
+    s_last = ticket == gridDim.y - 1;
   }
   __syncthreads();
   if (!s_last) return;
@@ -221,16 +265,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
   __shared__ int32_t s_idx[kSmallT * kMaxTopK];
   __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
   __shared__ uint32_t bm[kMaxExperts][2];
-  for (int t = warp; t < T; t += kRouteThreads / 32) {
-    float v[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int ee = lane + 32 * i;
-      v[i] = ee < E ? __ldcg(a.ws.logits + (size_t)t * E + ee) : -INFINITY;
-    }
-    warp_topk<kMaxExperts / 32>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + t * k);
-  }
   for (int i = threadIdx.x; i < E; i += blockDim.x) { cnt[i] = 0; bm[i][0] = 0; bm[i][1] = 0; }
+  for (int s = threadIdx.x; s < T * k; s += blockDim.x) s_idx[s] = __ldcg(a.idx + s);
   __syncthreads();
   for (int s = threadIdx.x; s < T * k; s += blockDim.x) {
     const int ee = s_idx[s], t = s / k;
@@ -387,8 +423,16 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
   (void)num_sms;
   if (prof) prof->begin(MOE_K_ROUTE, s);
   if (a.T <= kSmallT) {
-    const int grid = (a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
-    route_small_kernel<<<grid, kRouteThreads, 0, s>>>(a);
+    const size_t smem = (size_t)kSmallTok * a.d * (a.act_bf16 ? 2 : 4);
+    static bool attr_set = false;  // once, before any stream capture
+    if (!attr_set) {
+      if (cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+          cudaSuccess)
+        return cudaGetLastError();
+      attr_set = true;
+    }
+    const dim3 grid((a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32), (a.T + kSmallTok - 1) / kSmallTok);
+    route_small_kernel<<<grid, kRouteThreads, smem, s>>>(a);
     if (prof) prof->end(s);
     return cudaGetLastError();
   }

@@ -10,8 +10,8 @@
 // fixed-size array that lives in the library's own device image.
 //
 // The scratch array is shared by every call on a device and keeps the
-// previous call's contents; the one word that must start at zero (the grid
-// ticket of the routing kernel) is cleared by each call.  Calls that overlap
+// previous call's contents; the words that must start at zero (the routing
+// kernel's tickets) are cleared by each call.  Calls that overlap
 // on the GPU (different streams, or several host threads) race on it and must
 // be serialised by the caller.
 //
@@ -114,8 +114,9 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int
   w.src_of_slot = reinterpret_cast<int32_t*>(s + kOffSrc);
   w.slot_of = reinterpret_cast<int32_t*>(s + kOffSlot);
   w.counters = reinterpret_cast<uint32_t*>(s + kOffTicket);
-  // The previous call's ticket may be anything if it was interrupted: clear it.
-  if (cudaMemsetAsync(w.counters, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+  // The previous call's tickets may be anything if it was interrupted: clear
+  // them (the grid ticket and one per 8-token chunk).
+  if (cudaMemsetAsync(w.counters, 0, kAlign, stream) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }

@@ -65,7 +65,11 @@ def fake_weights():
     (dict(act_dtype=B.MOE_F32, weight_dtype=B.MOE_BF16), B.MOE_ERR_UNSUPPORTED),
     (dict(act_dtype=B.MOE_F32, weight_dtype=B.MOE_NVFP4), B.MOE_ERR_UNSUPPORTED),
     (dict(act_dtype=B.MOE_F32, weight_dtype=B.MOE_F32, path=B.MOE_PATH_TC), B.MOE_ERR_UNSUPPORTED),
-    (dict(d=8192, act_dtype=B.MOE_BF16, weight_dtype=B.MOE_BF16), B.MOE_ERR_UNSUPPORTED),
+    (dict(d=192, act_dtype=B.MOE_BF16, weight_dtype=B.MOE_BF16), B.MOE_ERR_UNSUPPORTED),
+    (dict(ffn=192, act_dtype=B.MOE_BF16, weight_dtype=B.MOE_BF16), B.MOE_ERR_UNSUPPORTED),
+    (dict(act_dtype=B.MOE_BF16, weight_dtype=B.MOE_NVFP4), B.MOE_ERR_UNSUPPORTED),
+    (dict(act_dtype=B.MOE_F32, weight_dtype=B.MOE_F32, path=B.MOE_PATH_GEMV, shared_ffn=256),
+     B.MOE_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config(lib, kw, want):
     st, h = B.moe_create(good_cfg(**kw), fake_weights(), 0)
@@ -85,7 +89,7 @@ def test_create_rejects_bad_weight_pointers(lib):
     assert B.moe_create(good_cfg(), w, 0)[0] == B.MOE_ERR_INVALID_ARG
     w = fake_weights()
     w.s_gate = None                               # NVFP4 scales missing
-    cfg = good_cfg(act_dtype=B.MOE_BF16, weight_dtype=B.MOE_NVFP4)
+    cfg = good_cfg(d=1024, ffn=512, shared_ffn=512, act_dtype=B.MOE_BF16, weight_dtype=B.MOE_NVFP4)
     assert B.moe_create(cfg, w, 0)[0] == B.MOE_ERR_INVALID_ARG
 
 

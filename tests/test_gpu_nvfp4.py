@@ -9,7 +9,7 @@ from sparse_moe_transformer_02_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-SMALL = I.LayerSpec(d=1024, ffn=256, shared_ffn=256, num_experts=16, top_k=4, weight="nvfp4")
+SMALL = I.LayerSpec(d=1024, ffn=512, shared_ffn=512, num_experts=16, top_k=4, weight="nvfp4")
 
 
 def run(spec, dev, x_np, max_tokens, **kw):
