@@ -296,21 +296,18 @@ def run_ours(args, rank, world, local_rank):
     }
     layer_bytes = (Umean + 1) * b_exp + 4 * d * E + 4 * E + T * d * 2 * 2
     layer_flops = 2 * T * (spec.top_k + 1) * 3 * d * F + 2 * T * d * E
-    if tc_path:
-        bound, unit = "tensor", "TFLOP/s"
-        flops_dom = {"tc_gateup": 2 * T * (spec.top_k + 1) * 2 * d * F,
-                     "tc_down": 2 * T * (spec.top_k + 1) * d * F}.get(dom)
-        if flops_dom is None:
-            bound, unit = "hbm", "GB/s"
-            achieved = per_kernel_bytes.get(dom, 0) / (dom_ms * 1e-3) / 1e9
-            peak = pk["hbm_gbs"]
-        else:
-            achieved = flops_dom / (dom_ms * 1e-3) / 1e12
-            peak = pk["bf16_tflops"]
+    # the dominant kernel's binding roof: whichever of HBM bytes / measured
+    # bandwidth and tensor flops / measured bf16 peak takes longer
+    per_kernel_flops = {"tc_gateup": 2 * T * (spec.top_k + 1) * 2 * d * F,
+                        "tc_down": 2 * T * (spec.top_k + 1) * d * F}
+    dom_bytes = per_kernel_bytes.get(dom, 0)
+    dom_flops = per_kernel_flops.get(dom, 0)
+    if dom_flops / (pk["bf16_tflops"] * 1e12) > dom_bytes / (pk["hbm_gbs"] * 1e9):
+        bound, unit, peak = "tensor", "TFLOP/s", pk["bf16_tflops"]
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     else:
-        bound, unit = "hbm", "GB/s"
-        achieved = per_kernel_bytes[dom] / (dom_ms * 1e-3) / 1e9
-        peak = pk["hbm_gbs"]
+        bound, unit, peak = "hbm", "GB/s", pk["hbm_gbs"]
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = dram_traffic(dom, args.workload)
     roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": pk["source"],

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   uint64_t* tempty = bars + 2 * S + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* col_tok = abort_flag + 3;                               // [4 warps][kTcBN] token of each column (pass 2)
+  float* col_gate = reinterpret_cast<float*>(col_tok + 4 * kTcBN);   // [4 warps][kTcBN] its gate
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    const uint64_t pol = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
     uint32_t last_par[S];
@@ -178,8 +181,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         uint8_t* st = stages + stage * C::STAGE_BYTES;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, ma0, k0, arow, &full[stage]);
-          if (MODE == 0) tma_load_2d(st + kTcBM * 128, ma1, k0, arow, &full[stage]);
+          // weights are streamed once: evict them first so that the activations,
+          // h and the fp32 accumulator stay in L2
+          tma_load_2d_hint(st, ma0, k0, arow, &full[stage], pol);
+          if (MODE == 0) tma_load_2d_hint(st + kTcBM * 128, ma1, k0, arow, &full[stage], pol);
           tma_load_2d(st + (MODE == 0 ? 2 : 1) * kTcBM * 128, mb, k0, brow, &full[stage]);
         }
         __syncwarp();
@@ -276,6 +281,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       const TcUnit un = get_unit(p, u);
       const bool sh = un.expert == p.E;
       const int n_pad = (un.n + 15) & ~15;
+      if (MODE == 1) {
+        // token and gate of every column of this tile, loaded once per warp into
+        // its own shared-memory table (no cross-warp barrier to get stuck on)
+        __syncwarp();
+        for (int c = lane; c < un.n; c += 32) {
+          int t;
+          float g;
+          if (sh) {
+            t = un.slot0 + c;
+            g = 1.f;
+          } else {
+            const int src = __ldcg(p.src_of_slot + un.slot0 + c);
+            t = src / p.k;
+            g = __ldcg(p.gate + src);
+          }
+          col_tok[q * kTcBN + c] = t;
+          col_gate[q * kTcBN + c] = g;
+        }
+        __syncwarp();
+      }
       if (!warp_wait(&tfull[buf], tph[buf], wc)) break;
       tc_fence_after();
       const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
@@ -300,22 +325,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           uint32_t v[16];
           tmem_ld16(acc + c0, v);
           tmem_ld_wait();
+          const int* ct = col_tok + q * kTcBN;
+          const float* cg = col_gate + q * kTcBN;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
-            if (col < un.n) {
-              int t;
-              float g;
-              if (sh) {
-                t = un.slot0 + col;
-                g = 1.f;
-              } else {
-                const int src = __ldcg(p.src_of_slot + un.slot0 + col);
-                t = src / p.k;
-                g = __ldcg(p.gate + src);
-              }
-              red_add_f32(p.yacc + (size_t)t * p.d + row, g * __uint_as_float(v[i]));
-            }
+            if (col < un.n) red_add_f32(p.yacc + (size_t)ct[col] * p.d + row, cg[col] * __uint_as_float(v[i]));
           }
         }
       }
@@ -333,18 +348,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   }
 }
 
-// Slot-ordered copy of the routed tokens' activations: xp[slot] = x[tok_of_slot[slot]].
+// Slot-ordered copy of the routed tokens' activations, xp[slot] = x[token of
+// slot], one warp per slot.  After a large-batch router (wpb > 0) the warp
+// also places the slot: it computes the grouped position of slot s = (t, j)
+// from the selection bitmap and writes tok_of_slot, src_of_slot and slot_of.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const __nv_bfloat16* __restrict__ x,
-                                                        const int32_t* __restrict__ tok_of_slot,
-                                                        __nv_bfloat16* __restrict__ xp, int slots, int d) {
+                                                        const int32_t* __restrict__ idx, Workspace ws, int T,
+                                                        int E, int k, int d, int wpb) {
   pdl_launch_dependents();
   pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
   const int per_row = d / 8;                       // 16-byte pieces per row
-  const size_t n = (size_t)slots * per_row;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const int s = (int)(i / per_row), c = (int)(i % per_row);
-    const int t = __ldg(tok_of_slot + s);
-    reinterpret_cast<uint4*>(xp)[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + c);
+  for (int s = gw; s < T * k; s += nw) {
+    int pos, t;
+    if (wpb > 0) {
+      t = s / k;
+      pos = slot_position(ws, E, t, __ldg(idx + s), wpb);
+      if (lane == 0) {
+        ws.tok_of_slot[pos] = t;
+        ws.src_of_slot[pos] = s;
+        ws.slot_of[s] = pos;
+      }
+    } else {
+      pos = s;
+      t = __ldg(ws.tok_of_slot + s);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)pos * d);
+    for (int c = lane; c < per_row; c += 32) dst[c] = __ldg(src + c);
   }
 }
 
@@ -381,7 +413,7 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restric
 template <int MODE>
 size_t tc_smem_bytes() {
   using C = TcCfg<MODE>;
-  return 1024 + C::STAGES * C::STAGE_BYTES + (2 * C::STAGES + 4) * 8 + 16;
+  return 1024 + C::STAGES * C::STAGE_BYTES + (2 * C::STAGES + 4) * 8 + 16 + 8 * kTcBN * 4;
 }
 
 template <typename... KArgs, typename... Args>
@@ -437,12 +469,11 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.wait_ns = a.wait_ns;
   p.n_units = a.ws.n_units;
   // slot-ordered copy of the routed activations
-  const size_t gpieces = (size_t)a.T * a.k * (a.d / 8);
-  const int gg = (int)((gpieces + 255) / 256 < (size_t)num_sms * 8 ? (gpieces + 255) / 256 : (size_t)num_sms * 8);
+  const int slots = a.T * a.k;
+  const int gg = (slots + 7) / 8 < num_sms * 8 ? (slots + 7) / 8 : num_sms * 8;   // 8 warps per block
   if (prof) prof->begin(MOE_K_TC_GATHER, s);
-  cudaError_t e = launch_ex(tc_gather_kernel, gg > 0 ? gg : 1, 256, 0, s,
-                            static_cast<const __nv_bfloat16*>(a.x), (const int32_t*)a.ws.tok_of_slot,
-                            a.ws.xp, a.T * a.k, a.d);
+  cudaError_t e = launch_ex(tc_gather_kernel, gg > 0 ? gg : 1, 256, 0, s, static_cast<const __nv_bfloat16*>(a.x),
+                            a.idx, a.ws, a.T, a.E, a.k, a.d, a.wpb);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // pass 1: gate/up

@@ -422,19 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint
   const int upe = d / RD;                            // units per expert
   const int has_sh = a.Fs > 0 ? 1 : 0;
   pdl_wait();
-  const int n_exp = a.ws.active[a.E] + has_sh;       // shared expert first
-  int u_lo, u_hi;
-  share(n_exp * upe, b, G, u_lo, u_hi);
+  // The shared expert's units (every token) are the heaviest: deal them
+  // round-robin over the CTAs; the routed ones follow in contiguous shares.
+  const int n_act = a.ws.active[a.E];
+  const int n_sh = has_sh ? upe : 0;
+  const int n_sh_local = b < n_sh ? (n_sh - b + G - 1) / G : 0;
+  int r_lo, r_hi;
+  share(n_act * upe, b, G, r_lo, r_hi);
+  const int n_local = n_sh_local + (r_hi - r_lo);
+  // local unit i -> (shared?, expert, first row)
+  auto unit_of = [&](int i, bool& shared, int& e, int& r0) {
+    if (i < n_sh_local) {
+      shared = true;
+      e = 0;
+      r0 = (b + i * G) * RD;
+    } else {
+      const int u = r_lo + (i - n_sh_local);
+      shared = false;
+      e = a.ws.active[u / upe];
+      r0 = (u % upe) * RD;
+    }
+  };
 
   if (warp == 0) {
     if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
     int i = 0;
     bool ok = true;
-    for (int u = u_lo; u < u_hi; ++u, ++i) {
-      const int ai = u / upe, r0 = (u % upe) * RD;
-      const bool shared = has_sh && ai == 0;
-      const int e = shared ? 0 : a.ws.active[ai - has_sh];
+    for (; i < n_local; ++i) {
+      bool shared;
+      int e, r0;
+      unit_of(i, shared, e, r0);
       const size_t row0 = shared ? (size_t)r0 : (size_t)e * d + r0;
       const int s = i % kStages;
       if (!mbar_wait(&ring.empty[s], ((i / kStages) & 1) ^ 1, wc)) { ok = false; break; }
@@ -459,11 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint
   const int Fmax = max(a.F, a.Fs);
   const int col_lane = SPLIT ? (lane & 15) : lane;   // chunk column of this lane (plus 32 j)
   const int row_lane = SPLIT ? (lane >> 4) : 0;      // first row of this lane (SPLIT: every other row)
-  for (int i = cw; u_lo + i < u_hi; i += kConsumers) {
-    const int u = u_lo + i;
-    const int ai = u / upe, r0 = (u % upe) * RD;
-    const bool shared = has_sh && ai == 0;
-    const int e = shared ? 0 : a.ws.active[ai - has_sh];
+  for (int i = cw; i < n_local; i += kConsumers) {
+    bool shared;
+    int e, r0;
+    unit_of(i, shared, e, r0);
     const int s = i % kStages;
     if (!warp_wait_full(&ring.full[s], (i / kStages) & 1, wc)) break;
     const uint8_t* st = ring.stages + s * kStageBytes;

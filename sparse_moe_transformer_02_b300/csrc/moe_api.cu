@@ -16,9 +16,11 @@ struct moe_layer {
   int num_sms = 0;
   bool tc_capable = false;
   bool gemv_capable = false;
+  bool rtc_capable = false;    // tensor-core router for T > 64
+  int n_counters = 64;
   uint64_t wait_ns = 0;
   int max_units_gu = 0, max_units_dn = 0;
-  CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp;
+  CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp, tm_wr;
   void* block = nullptr;
   Prof prof;
 };
@@ -170,6 +172,21 @@ moe_status check_call(const moe_layer* h, const void* x, int32_t T) {
   return MOE_OK;
 }
 
+// Routing: the tensor-core router for large bf16 batches, else the fp32 SIMT
+// kernels.  tm_x (box 64 x 128 over x) is built here when needed and returned.
+moe_status do_route(moe_layer* h, const void* x, int32_t T, int32_t* idx, float* gate, int32_t* counts,
+                    bool tc_units, CUtensorMap* tm_x, bool* have_tm_x, cudaStream_t s) {
+  const RouteArgs ra = route_args(h, x, T, idx, gate, counts, tc_units);
+  if (T > kSmallT && h->rtc_capable) {
+    if (!*have_tm_x) {
+      if (!make_map_bf16(tm_x, x, (uint64_t)T, (uint64_t)h->cfg.d, kTcBN, kTcBK)) return MOE_ERR_CUDA;
+      *have_tm_x = true;
+    }
+    return cuda_status(launch_route_tc(ra, tm_x, &h->tm_wr, h->ws.cand, h->wait_ns, s, &h->prof));
+  }
+  return cuda_status(launch_route(ra, h->num_sms, s, &h->prof));
+}
+
 moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
                        cudaStream_t s) {
   const moe_config& c = h->cfg;
@@ -181,10 +198,11 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
   const bool tc = c.path == MOE_PATH_TC ||
                   (c.path == MOE_PATH_AUTO && h->tc_capable && (T > c.gemv_max_tokens || !h->gemv_capable));
   if (tc) {
-    moe_status st = cuda_status(launch_route(route_args(h, x, T, idx, gate, nullptr, true), h->num_sms, s, &h->prof));
-    if (st != MOE_OK) return st;
     CUtensorMap tm_x;
-    if (!make_map_bf16(&tm_x, x, (uint64_t)T, (uint64_t)c.d, kTcBN, kTcBK)) return MOE_ERR_CUDA;
+    bool have_tm_x = false;
+    moe_status st = do_route(h, x, T, idx, gate, nullptr, true, &tm_x, &have_tm_x, s);
+    if (st != MOE_OK) return st;
+    if (!have_tm_x && !make_map_bf16(&tm_x, x, (uint64_t)T, (uint64_t)c.d, kTcBN, kTcBK)) return MOE_ERR_CUDA;
     TcArgs a;
     a.tm_x = &tm_x;
     a.tm_xp = &h->tm_xp;
@@ -193,6 +211,8 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
     a.x = x;
     a.y = y;
     a.gate = gate;
+    a.idx = idx;
+    a.wpb = T > kSmallT ? (h->rtc_capable ? 4 : 1) : 0;
     a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
     a.add_residual = c.add_residual != 0;
     a.ws = h->ws;
@@ -208,7 +228,9 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
     uint8_t* yc = static_cast<uint8_t*>(y) + (size_t)t0 * c.d * es;
     int32_t* ic = idx + (size_t)t0 * c.top_k;
     float* gc = gate + (size_t)t0 * c.top_k;
-    moe_status st = cuda_status(launch_route(route_args(h, xc, tc_, ic, gc, nullptr, false), h->num_sms, s, &h->prof));
+    CUtensorMap tm_x;
+    bool have_tm_x = false;
+    moe_status st = do_route(h, xc, tc_, ic, gc, nullptr, false, &tm_x, &have_tm_x, s);
     if (st != MOE_OK) return st;
     st = cuda_status(launch_gemv(gemv_args(h, xc, yc, gc, tc_), c.weight_dtype, h->num_sms, s, &h->prof, h->wait_ns));
     if (st != MOE_OK) return st;
@@ -256,6 +278,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
   h->tc_capable = tc_shape_ok(c) && cc_major == 10;
   h->gemv_capable = gemv_shape_ok(c);
+  h->rtc_capable = cc_major == 10 && c.act_dtype == MOE_BF16 && c.num_experts % 64 == 0 && c.d % 64 == 0;
   if ((c.path == MOE_PATH_TC && !h->tc_capable) || (!h->tc_capable && !h->gemv_capable)) {
     delete h;
     return MOE_ERR_UNSUPPORTED;
@@ -276,7 +299,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.idx, Tm * k * 4},
       {(void**)&ws.gate, Tm * k * 4},
       {(void**)&ws.logits, (size_t)kSmallT * E * 4},
-      {(void**)&ws.sel, 2 * nblk * E * 4},
+      {(void**)&ws.sel, nblk * E * 4},
+      {(void**)&ws.bcnt, nblk * E * 4},
+      {(void**)&ws.bpref, nblk * E * 4},
       {(void**)&ws.counts, (E + 1) * 4},
       {(void**)&ws.offsets, (E + 2) * 4},
       {(void**)&ws.tok_of_slot, Tm * k * 4},
@@ -291,7 +316,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.xp, h->tc_capable ? Tm * k * d * 2 : 16},
       {(void**)&ws.ypart, Tg * (k + 1) * d * 4},
       {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
-      {(void**)&ws.counters, 64 * 4},
+      {(void**)&ws.counters, (size_t)(64 + (Tm + 127) / 128) * 4},
+      {(void**)&ws.wr_split, h->rtc_capable ? 3 * E * d * 2 : 16},
+      {(void**)&ws.cand, h->rtc_capable ? Tm * (E / 64) * kMaxTopK * 8 : 16},
       {(void**)&ws.fin, Tg * (d / kFinRows) * 4},
       {(void**)&ws.err, 16},
       {&ws.x_stage, Tm * d * act_bytes(c)},
@@ -311,7 +338,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
     off += up256(p.bytes);
   }
   // Counters and the error word start at zero; the rest is written before it is read.
-  cudaError_t e = cudaMemsetAsync(ws.counters, 0, 64 * 4, stream);
+  h->n_counters = (int)(64 + (Tm + 127) / 128);
+  cudaError_t e = cudaMemsetAsync(ws.counters, 0, (size_t)h->n_counters * 4, stream);
+  if (e == cudaSuccess && h->rtc_capable) e = launch_router_split(w->router_w, ws.wr_split, E * d, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.fin, 0, Tg * (d / kFinRows) * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.err, 0, 16, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -321,6 +350,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
     delete h;
     return MOE_ERR_CUDA;
   }
+  if (h->rtc_capable && !make_map_bf16(&h->tm_wr, ws.wr_split, 3 * E, d, 64, kTcBK)) h->rtc_capable = false;
   if (h->tc_capable) {
     const uint64_t F = c.ffn, Fs = c.shared_ffn;
     bool ok = make_map_bf16(&h->tm_wg, w->w_gate, E * F, d, kTcBM, kTcBK) &&
@@ -363,7 +393,12 @@ moe_status moe_route(moe_handle h, const void* x, int32_t T, int32_t* idx, float
   if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(gate) & 3u) ||
       (reinterpret_cast<uintptr_t>(counts) & 3u))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_route(route_args(h, x, T, idx, gate, counts, false), h->num_sms, stream, &h->prof));
+  CUtensorMap tm_x;
+  bool have_tm_x = false;
+  moe_status st2 = do_route(h, x, T, idx, gate, counts, false, &tm_x, &have_tm_x, stream);
+  if (st2 != MOE_OK || T <= kSmallT) return st2;
+  // large-batch routers leave the per-slot placement to a separate pass
+  return cuda_status(launch_place(idx, h->ws, T, h->cfg.num_experts, h->cfg.top_k, h->rtc_capable ? 4 : 1, stream));
 }
 
 moe_status moe_forward(moe_handle h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,

@@ -32,7 +32,9 @@ struct Workspace {
   int32_t* idx;           // [max_T][k]   routing when the caller passes no buffer
   float* gate;            // [max_T][k]
   float* logits;          // [kSmallT][E] small-batch router scratch
-  uint32_t* sel;          // [ceil(max_T/32)][E] token-selection bitmap words (large-batch router)
+  uint32_t* sel;          // [ceil(max_T/32)][E] token-selection bitmap words (large-batch routers)
+  int32_t* bcnt;          // [ceil(max_T/32)][E] per-block expert counts (large-batch routers)
+  int32_t* bpref;         // [ceil(max_T/32)][E] exclusive prefix of bcnt over blocks
   int32_t* counts;        // [E + 1]
   int32_t* offsets;       // [E + 2]
   int32_t* tok_of_slot;   // [max_T * k]  token of each grouped slot
@@ -47,7 +49,9 @@ struct Workspace {
   __nv_bfloat16* xp;      // [max_T * k][d] tcgen05 slot-ordered copy of the routed activations
   float* ypart;           // [min(max_T, kGemvChunkT) * (k + 1)][d] GEMV down partials
   float* yacc;            // [max_T][d] tcgen05 fp32 accumulator
-  uint32_t* counters;     // router ticket
+  uint32_t* counters;     // router tickets: [0] grid, [1 + b] per token chunk / block
+  __nv_bfloat16* wr_split;  // [3][E][d] router weights as bf16 hi, mid, lo (tensor-core router)
+  uint64_t* cand;         // [max_T][E / 64][kMaxTopK] tensor-core router: per-slice selection keys
   uint32_t* fin;          // [kGemvChunkT][d / 32] GEMV down completion counts (kept at zero between calls)
   unsigned int* err;      // device error word
   void* x_stage;          // [max_T][d] moe_forward_host staging
@@ -110,6 +114,24 @@ struct GemvArgs {
 
 // Launchers (return the launch status).
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof);
+// Tensor-core router for T > 64 with bf16 activations (E a multiple of 64).
+cudaError_t launch_route_tc(const RouteArgs& a, const CUtensorMap* tm_x, const CUtensorMap* tm_wr, uint64_t* cand,
+                            uint64_t wait_ns, cudaStream_t s, Prof* prof);
+// Grouped slot positions after a large-batch router (wpb bitmap words per block).
+cudaError_t launch_place(const int32_t* idx, const Workspace& ws, int T, int E, int k, int wpb, cudaStream_t s);
+
+// Grouped position of slot (t, expert e) after a large-batch router: the
+// expert's offset, the counts of earlier token blocks, and the earlier tokens
+// of this block (from the selection bitmap; blocks of 32 * wpb tokens).
+__device__ __forceinline__ int slot_position(const Workspace& ws, int E, int t, int e, int wpb) {
+  const int w = t >> 5, b = w / wpb;
+  int pos = __ldcg(ws.offsets + e) + __ldcg(ws.bpref + (size_t)b * E + e);
+  for (int ww = b * wpb; ww < w; ++ww) pos += __popc(__ldcg(ws.sel + (size_t)ww * E + e));
+  return pos + __popc(__ldcg(ws.sel + (size_t)w * E + e) & ((1u << (t & 31)) - 1u));
+}
+
+// Splits fp32 router weights w[n] into bf16 hi, mid, lo (out[3][n]).
+cudaError_t launch_router_split(const float* w, __nv_bfloat16* out, size_t n, cudaStream_t s);
 cudaError_t launch_gemv(const GemvArgs& a, int wfmt, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns);
 // Shapes the GEMV kernels are built for: rows of d values span 1, 2, 4 or 8
 // x 512 bytes; rows of F values span 16, 32, 64 or 128 chunks of 16 bytes;
@@ -130,6 +152,8 @@ struct TcArgs {
   const void* x;
   void* y;
   const float* gate;            // [T][k]
+  const int32_t* idx;           // [T][k]
+  int wpb;                      // > 0: the gather kernel places slots (bitmap words per router block)
   int T, d, F, Fs, E, k, add_residual;
   Workspace ws;
   uint64_t wait_ns;

@@ -38,6 +38,21 @@ __device__ __forceinline__ void load_x4(const void* x, int act_bf16, size_t off,
   }
 }
 
+// Grid ticket: every CTA calls this once after writing its results; *last is
+// set in the CTA that arrives n-th.  One fence by the ticket thread publishes
+// the whole CTA's writes (fences are cumulative over writes ordered before
+// them by the barrier) and, in the last CTA, orders the reads that follow.
+__device__ __forceinline__ void ticket_last(unsigned int* counter, unsigned n, int* last) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const bool l = atomicAdd(counter, 1u) == n - 1;
+    if (l) __threadfence();
+    *last = l;
+  }
+  __syncthreads();
+}
+
 // (value, index) order of the selection: larger value first, lower index on ties.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -54,7 +69,9 @@ __device__ void warp_topk(float (&vals)[NPL], int E, int k, int32_t* idx_t, floa
 #pragma unroll
   for (int i = 0; i < NPL; ++i)
     if (isnan(vals[i])) vals[i] = -INFINITY;
-  for (int j = 0; j < k; ++j) {
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
 #pragma unroll
@@ -74,13 +91,17 @@ __device__ void warp_topk(float (&vals)[NPL], int E, int k, int32_t* idx_t, floa
   }
   if (lane == 0) {
     float z = 0.f;
-    for (int j = 0; j < k; ++j) z += expf(selv[j] - selv[0]);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) z += expf(selv[j] - selv[0]);
     const float inv = 1.f / z;
-    for (int j = 0; j < k; ++j) {
-      idx_t[j] = seli[j];
-      gate_t[j] = expf(selv[j] - selv[0]) * inv;
-      if (sidx_t) sidx_t[j] = seli[j];
-    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        idx_t[j] = seli[j];
+        gate_t[j] = expf(selv[j] - selv[0]) * inv;
+        if (sidx_t) sidx_t[j] = seli[j];
+      }
   }
 }
 
@@ -175,6 +196,35 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
   }
 }
 
+// Grouping from per-block counts.  Tokens come in blocks of 32 * wpb tokens
+// (wpb selection-bitmap words per expert and block; sel[w][e] bit t % 32 is
+// set when token 32 w + t % 32 chose expert e) and bcnt[b][e] is block b's
+// count for expert e.  One CTA turns the counts into offsets, the active list
+// and the unit lists, and stores the exclusive prefix of the block counts in
+// bpref[b][e]; the per-slot placement (slot_position) runs afterwards, in
+// parallel, in whichever kernel needs it.
+__device__ void group_from_counts(const RouteArgs& a, int nblk) {
+  __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
+  const int E = a.E, tid = threadIdx.x, nth = blockDim.x;
+  for (int ee = tid; ee < E; ee += nth) {
+    int run = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {
+      int c[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) c[i] = b0 + i < nblk ? __ldcg(a.ws.bcnt + (size_t)(b0 + i) * E + ee) : 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (b0 + i < nblk) a.ws.bpref[(size_t)(b0 + i) * E + ee] = run;
+        run += c[i];
+      }
+    }
+    cnt[ee] = run;
+  }
+  __syncthreads();
+  finish_grouping(a, cnt, offs, scratch);
+  if (tid == 0) a.ws.counters[0] = 0;
+}
+
 // ------------------------------------------------------------------ small T
 // grid (ceil(E / 8), ceil(T / 8)): warp w of CTA (bx, by) scores expert 8 bx + w
 // against tokens 8 by .. 8 by + 7, whose activations are staged in shared memory.
@@ -232,15 +282,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
   // selects the chunk's tokens (one warp per token); the last of those does
   // the grouping for all tokens.
   __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned ticket = atomicAdd(&a.ws.counters[1 + blockIdx.y], 1u);
-    s_last = ticket == gridDim.x - 1;
-  }
-  __syncthreads();
+  ticket_last(&a.ws.counters[1 + blockIdx.y], gridDim.x, &s_last);
   if (!s_last) return;
-  __threadfence();
   if (warp < nt) {
     const int t = t0 + warp;
     float v[kMaxExperts / 32];
@@ -252,15 +295,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
     warp_topk<kMaxExperts / 32>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, nullptr);
   }
   if (threadIdx.x == 0) a.ws.counters[1 + blockIdx.y] = 0;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
-    s_last = ticket == gridDim.y - 1;
-  }
-  __syncthreads();
+  ticket_last(&a.ws.counters[0], gridDim.y, &s_last);
   if (!s_last) return;
-  __threadfence();
 
   __shared__ int32_t s_idx[kSmallT * kMaxTopK];
   __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
@@ -378,46 +414,323 @@ __global__ void __launch_bounds__(kRouteThreads) route_large_kernel(RouteArgs a)
     if (t0 + tt < T) atomicOr(&word[s_idx[s]], 1u << tt);
   }
   __syncthreads();
-  for (int i = tid; i < E; i += kRouteThreads) a.ws.sel[(size_t)blockIdx.x * E + i] = word[i];
+  for (int i = tid; i < E; i += kRouteThreads) {
+    a.ws.sel[(size_t)blockIdx.x * E + i] = word[i];
+    a.ws.bcnt[(size_t)blockIdx.x * E + i] = __popc(word[i]);
+  }
 
   // Last CTA: counts, word prefixes, offsets, slots.
   __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned ticket = atomicAdd(&a.ws.counters[0], 1u);
-    s_last = ticket == gridDim.x - 1;
-  }
-  __syncthreads();
+  ticket_last(&a.ws.counters[0], gridDim.x, &s_last);
   if (!s_last) return;
-  __threadfence();
-  __shared__ int cnt[kMaxExperts], offs[kMaxExperts + 1], scratch[kMaxExperts];
-  const int nblk = gridDim.x;
-  int32_t* wpref = reinterpret_cast<int32_t*>(a.ws.sel) + (size_t)nblk * E;   // [nblk][E] prefixes
-  for (int ee = tid; ee < E; ee += kRouteThreads) {
-    int run = 0;
-    for (int bk = 0; bk < nblk; ++bk) {
-      wpref[(size_t)bk * E + ee] = run;
-      run += __popc(__ldcg(a.ws.sel + (size_t)bk * E + ee));
+  group_from_counts(a, gridDim.x);
+}
+
+// ------------------------------------------------------------------ large T, tensor cores
+// With bf16 activations (exact in bf16) and the fp32 router weights split once
+// into three bf16 parts w = hi + mid + lo (to within 2^-24 of w), three bf16
+// MMAs accumulating in fp32 give the logits to within fp32 rounding, on the
+// tensor pipe.  CTA (es, tb): 128 tokens x 64 experts, K = d.  Each CTA keeps
+// the top 8 of its 64 experts per token (ordered by logit, then lower index);
+// the last CTA of a token block merges the slices (the global top k lies in
+// the union of the slices' top k) and writes the token block's bitmap words;
+// the last token block groups all tokens.
+constexpr int kRtStages = 4;
+constexpr int kRtA = 128 * 128;                // x tile: 128 tokens x 64 values
+constexpr int kRtB = 64 * 128;                 // router tile: 64 experts x 64 values (one split)
+constexpr int kRtStageBytes = kRtA + 3 * kRtB;
+
+struct RouteTcParams {
+  CUtensorMap tm_x;        // x [T][d] bf16, box {64, 128}
+  CUtensorMap tm_wr;       // split router weights [3 E][d] bf16, box {64, 64}
+  RouteArgs a;
+  uint64_t* cand;          // [T][E / 64][kMaxTopK] per-slice selection keys
+  uint64_t wait_ns;
+};
+
+// Selection keys: (logit, expert) packed into 64 bits so that unsigned order
+// is the selection order (larger logit first, lower index on equal logits).
+// NaN counts as -inf and -0 as +0, as in the float comparison.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+  v = isnan(v) ? -INFINITY : v + 0.0f;
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint32_t)(0x7FFFFFFF - e);
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+  uint32_t u = (uint32_t)(k >> 32);
+  u = (u & 0x80000000u) ? (u ^ 0x80000000u) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_index(uint64_t k) { return 0x7FFFFFFF - (int)(uint32_t)k; }
+__device__ __forceinline__ void cswap(uint64_t& a, uint64_t& b) {   // a >= b afterwards
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+// Sorts 8 keys in descending order (19-comparator network, depth 6).
+__device__ __forceinline__ void sort8(uint64_t (&a)[8]) {
+  cswap(a[0], a[1]); cswap(a[2], a[3]); cswap(a[4], a[5]); cswap(a[6], a[7]);
+  cswap(a[0], a[2]); cswap(a[1], a[3]); cswap(a[4], a[6]); cswap(a[5], a[7]);
+  cswap(a[1], a[2]); cswap(a[5], a[6]); cswap(a[0], a[4]); cswap(a[3], a[7]);
+  cswap(a[1], a[5]); cswap(a[2], a[6]);
+  cswap(a[1], a[4]); cswap(a[3], a[6]);
+  cswap(a[2], a[4]); cswap(a[3], a[5]);
+  cswap(a[3], a[4]);
+}
+// r = top 8 of the descending lists r and b, descending (bitonic merge).
+__device__ __forceinline__ void merge_top8(uint64_t (&r)[8], const uint64_t (&b)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = r[i] > b[7 - i] ? r[i] : b[7 - i];
+#pragma unroll
+  for (int dd = 4; dd >= 1; dd >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & dd) == 0) cswap(r[i], r[i + dd]);
+}
+
+__global__ void __launch_bounds__(192, 1) route_tc_kernel(const __grid_constant__ RouteTcParams p) {
+  const RouteArgs& a = p.a;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + kRtStages * kRtStageBytes);
+  uint64_t* empty = full + kRtStages;
+  uint64_t* tfull = empty + kRtStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int E = a.E, T = a.T, k = a.k, d = a.d;
+  const int es = blockIdx.x, nsl = gridDim.x, tb = blockIdx.y, t0 = tb * 128;
+  if (tid == 0) {
+    for (int i = 0; i < kRtStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    cnt[ee] = run;
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  const WaitCtl wc{p.wait_ns, a.ws.err, abort_flag};
+  const int nkb = d / 64;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_x);
+    tma_prefetch_desc(&p.tm_wr);
+    int issued = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kRtStages;
+      if (!mbar_wait(&empty[s], ((kb / kRtStages) & 1) ^ 1, wc)) { ok = false; break; }
+      uint8_t* st = dsm + s * kRtStageBytes;
+      mbar_arrive_expect_tx(&full[s], kRtStageBytes);
+      tma_load_2d(st, &p.tm_x, kb * 64, t0, &full[s]);
+#pragma unroll
+      for (int sp = 0; sp < 3; ++sp) tma_load_2d(st + kRtA + sp * kRtB, &p.tm_wr, kb * 64, sp * E + es * 64, &full[s]);
+      issued = kb + 1;
+    }
+    if (!ok)
+      for (int j = issued - kRtStages < 0 ? 0 : issued - kRtStages; j < issued; ++j) {
+        const uint64_t ts = global_ns();
+        while (!mbar_try_wait(&full[j % kRtStages], (j / kRtStages) & 1))
+          if (global_ns() - ts > p.wait_ns) break;
+      }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, 64);
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kRtStages;
+      if (!mbar_wait(&full[s], (kb / kRtStages) & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t st = smem_u32(dsm + s * kRtStageBytes);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+          tc_mma_f16(tmem, sdesc_sw128(st + kk * 32), sdesc_sw128(st + kRtA + sp * kRtB + kk * 32), idesc,
+                     (kb > 0 || kk > 0 || sp > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
+    }
+    if (ok) tc_commit(tfull);
+    else if (nkb > 0) {
+      const uint64_t ts = global_ns();
+      while (!mbar_try_wait(&empty[(nkb - 1) % kRtStages], ((nkb - 1) / kRtStages) & 1))
+        if (global_ns() - ts > p.wait_ns) break;
+    }
+  } else if (warp >= 2) {
+    // epilogue: TMEM lane quarter q holds tokens 32 q .. 32 q + 31
+    const int q = warp & 3, r = q * 32 + lane, t = t0 + r;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(tfull, 0, wc) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (ok) {
+      while (!mbar_try_wait(tfull, 0)) {
+      }
+      tc_fence_after();
+      uint64_t best[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) best[j] = 0;          // below every real key
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint64_t g[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = es * 64 + c0 + 8 * h + i;
+            g[i] = sel_key(__uint_as_float(v[8 * h + i]) + (a.b ? __ldg(a.b + e) : 0.f), e);
+          }
+          sort8(g);
+          merge_top8(best, g);
+        }
+      }
+      // static indices only: a runtime index would put the list in local memory
+      if (t < T) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (j < k) p.cand[((size_t)t * nsl + es) * kMaxTopK + j] = best[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (*abort_flag) return;
+
+  // ---- merge the slices of this token block (last slice CTA to finish)
+  __shared__ int s_last;
+  ticket_last(&a.ws.counters[1 + tb], nsl, &s_last);
+  if (!s_last) return;
+  __shared__ uint32_t words[4][kMaxExperts];
+  for (int i = tid; i < 4 * kMaxExperts; i += blockDim.x) (&words[0][0])[i] = 0;
+  __syncthreads();
+  for (int r = tid; r < 128; r += blockDim.x) {
+    const int t = t0 + r;
+    if (t >= T) continue;
+    // every slice's list is already sorted: merge them pairwise
+    uint64_t best[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) best[j] = 0;
+#pragma unroll
+    for (int sl = 0; sl < kMaxExperts / 64; ++sl) {
+      if (sl >= nsl) break;
+      uint64_t c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = j < k ? __ldcg(p.cand + ((size_t)t * nsl + sl) * kMaxTopK + j) : 0;
+      merge_top8(best, c);
+    }
+    float lv[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) lv[j] = key_value(best[j]);
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) z += expf(lv[j] - lv[0]);
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        const int e = key_index(best[j]);
+        a.idx[(size_t)t * k + j] = e;
+        a.gate[(size_t)t * k + j] = expf(lv[j] - lv[0]) * inv;
+        atomicOr(&words[r >> 5][e], 1u << (r & 31));
+      }
   }
   __syncthreads();
-  finish_grouping(a, cnt, offs, scratch);
-  __threadfence_block();
-  for (int s = tid; s < T * k; s += kRouteThreads) {
-    const int t = s / k, bk = t >> 5;
-    const int ee = __ldcg(a.idx + s);
-    const uint32_t w = __ldcg(a.ws.sel + (size_t)bk * E + ee);
-    const int slot = offs[ee] + wpref[(size_t)bk * E + ee] + __popc(w & ((1u << (t & 31)) - 1u));
-    a.ws.tok_of_slot[slot] = t;
-    a.ws.src_of_slot[slot] = s;
-    a.ws.slot_of[s] = slot;
+  const int nw = (T + 31) / 32;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < 4; ++w) {
+      if (tb * 4 + w < nw) a.ws.sel[(size_t)(tb * 4 + w) * E + e] = words[w][e];
+      c += __popc(words[w][e]);
+    }
+    a.ws.bcnt[(size_t)tb * E + e] = c;
   }
-  if (tid == 0) a.ws.counters[0] = 0;
+  if (tid == 0) a.ws.counters[1 + tb] = 0;
+
+  // ---- the last token block groups everything
+  ticket_last(&a.ws.counters[0], gridDim.y, &s_last);
+  if (!s_last) return;
+  group_from_counts(a, gridDim.y);
+}
+
+__global__ void router_split_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ out, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = __float2bfloat16_rn(r2);
+  }
 }
 
 }  // namespace
+
+// Grouped position of every slot (t, j): tok_of_slot, src_of_slot, slot_of.
+__global__ void __launch_bounds__(256) place_kernel(const int32_t* __restrict__ idx, Workspace ws, int T, int E, int k,
+                                                    int wpb) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < T * k; s += gridDim.x * blockDim.x) {
+    const int t = s / k, e = __ldg(idx + s);
+    const int pos = slot_position(ws, E, t, e, wpb);
+    ws.tok_of_slot[pos] = t;
+    ws.src_of_slot[pos] = s;
+    ws.slot_of[s] = pos;
+  }
+}
+
+cudaError_t launch_place(const int32_t* idx, const Workspace& ws, int T, int E, int k, int wpb, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((T * k + 255) / 256 < 1024 ? (T * k + 255) / 256 : 1024);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, place_kernel, idx, ws, T, E, k, wpb);
+}
+
+cudaError_t launch_router_split(const float* w, __nv_bfloat16* out, size_t n, cudaStream_t s) {
+  router_split_kernel<<<256, 256, 0, s>>>(w, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_tc(const RouteArgs& a, const CUtensorMap* tm_x, const CUtensorMap* tm_wr, uint64_t* cand,
+                            uint64_t wait_ns, cudaStream_t s, Prof* prof) {
+  const size_t smem = 1024 + (size_t)kRtStages * kRtStageBytes + (2 * kRtStages + 1) * 8 + 16;
+  static bool attr_set = false;   // once, before any stream capture
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return cudaGetLastError();
+    attr_set = true;
+  }
+  RouteTcParams p;
+  p.tm_x = *tm_x;
+  p.tm_wr = *tm_wr;
+  p.a = a;
+  p.cand = cand;
+  p.wait_ns = wait_ns;
+  if (prof) prof->begin(MOE_K_ROUTE, s);
+  route_tc_kernel<<<dim3(a.E / 64, (a.T + 127) / 128), 192, smem, s>>>(p);
+  if (prof) prof->end(s);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
   (void)num_sms;

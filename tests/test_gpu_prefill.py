@@ -90,3 +90,28 @@ def test_flint_prefill_ragged_with_residual(flint_bf16):
     x = I.make_tokens(spec, seed=1000, T=T)
     _, y, idx, gate = run(spec, dev, x, T, add_residual=True)
     check_layer(L, x, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=np.arange(0, T, 31))
+
+
+@pytest.mark.parametrize("which", ["tensor_core_router", "simt_router"])
+def test_route_and_grouping_large_batch(flint_bf16, small, which):
+    if which == "tensor_core_router":
+        spec, L, dev = flint_bf16                # E = 256: tensor-core router
+        T = 777
+    else:
+        spec, (L, dev) = SMALL, small            # E = 16: fp32 SIMT router
+        T = 300
+    x_np = I.make_tokens(spec, seed=55, T=T)
+    layer = B.layer_from_spec(spec, dev, T)
+    idx, gate, cnt = layer.route(to_torch_x(x_np))
+    offs, tos, so = layer.grouping(T, "cuda")
+    torch.cuda.synchronize()
+    W = LayerWeights(L)
+    xf = (x_np.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    l = router_logits(xf, W.Wr, W.b)
+    ig = idx.cpu().numpy().astype(np.int64)
+    check_routing(l, ig, gate.cpu().numpy().astype(np.float64), spec.top_k)
+    counts, offsets, tok_of_slot, slot_of = group_slots(ig, spec.num_experts)
+    assert np.array_equal(cnt.cpu().numpy(), counts)
+    assert np.array_equal(offs.cpu().numpy(), offsets)
+    assert np.array_equal(tos.cpu().numpy(), tok_of_slot)
+    assert np.array_equal(so.cpu().numpy(), slot_of)
