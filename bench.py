@@ -36,6 +36,7 @@ WORKLOADS = {
     "decode1": ("bf16", 1, 16),
     "prefill4096": ("bf16", 4096, 8),
     "nvfp4_32": ("nvfp4", 32, 32),
+    "stack47": ("stack", 2048, 47),      # 47 chained layers, residual adds, Zipf(1.1) load
 }
 DEFAULT = "decode64"
 SWEEP = ["decode1", "decode8", "decode32"]
@@ -133,7 +134,7 @@ def make_device_layers(kind, n_layers, device, seed):
     import torch
     from sparse_moe_transformer_02_b300 import binding as B
     from sparse_moe_transformer_02_b300 import inputs as I
-    spec = I.FLINT_BF16 if kind == "bf16" else I.FLINT_NVFP4
+    spec = {"bf16": I.FLINT_BF16, "nvfp4": I.FLINT_NVFP4, "stack": I.FLINT_STACK_ZIPF}[kind]
     E, d, F, Fs = spec.num_experts, spec.d, spec.ffn, spec.shared_ffn
     g = torch.Generator(device=device)
     layers = []
@@ -144,7 +145,9 @@ def make_device_layers(kind, n_layers, device, seed):
         g.manual_seed(seed * 1000 + li)
         w = {"router_w": torch.randn(E, d, generator=g, device=device) * spec.sigma_router,
              "router_b": torch.zeros(E, device=device)}
-        if kind == "bf16":
+        if spec.bias == "zipf":
+            w["router_b"] = torch.from_numpy(I.zipf_bias(seed, li, E)).to(device)
+        if kind in ("bf16", "stack"):
             for name, shape in (("w_gate", (E, F, d)), ("w_up", (E, F, d)), ("w_down", (E, d, F)),
                                 ("ws_gate", (Fs, d)), ("ws_up", (Fs, d)), ("ws_down", (d, Fs))):
                 w[name] = (torch.randn(*shape, generator=g, device=device) * spec.sigma_w).to(torch.bfloat16)
@@ -162,6 +165,7 @@ def oracle_tokens_per_s(kind, T, seed, budget_s=20.0):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", kind, str(T), str(seed), str(budget_s)]
+    # (the stack's oracle sample is one layer of the stack)
     res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
     if res.returncode != 0:
         raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
@@ -173,7 +177,7 @@ def oracle_sample_main(kind, T, seed, budget_s):
     """Child side of oracle_tokens_per_s: prints {"tokens_per_s", "sample"}."""
     import oracle
     from sparse_moe_transformer_02_b300 import inputs as I
-    spec = I.FLINT_BF16 if kind == "bf16" else I.FLINT_NVFP4
+    spec = {"bf16": I.FLINT_BF16, "nvfp4": I.FLINT_NVFP4, "stack": I.FLINT_STACK_ZIPF}[kind]
     L = I.make_layer(spec, seed=seed)
     W = oracle.LayerWeights(L)
     x = I.make_tokens(spec, seed=seed, T=max(T, 1))
@@ -181,7 +185,7 @@ def oracle_sample_main(kind, T, seed, budget_s):
     n = min(T, 8)
     while t_used < budget_s and done < T:
         t0 = time.perf_counter()
-        oracle.moe_forward(x[done:done + n], W, spec.top_k)
+        oracle.moe_forward(x[done:done + n], W, spec.top_k, residual=spec.add_residual)
         t_used += time.perf_counter() - t0
         done += n
     print(json.dumps({"tokens_per_s": done / t_used,
@@ -213,20 +217,24 @@ def run_ours(args, rank, world, local_rank):
     g.manual_seed(args.seed + 77 + rank)
     x = (torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x).to(torch.bfloat16)
     ys = [torch.empty_like(x) for _ in handles]
+    chain = kind == "stack"          # layer l + 1 reads layer l's output
+    ins = [x] + ys[:-1] if chain else [x] * len(handles)
     torch.cuda.synchronize()
 
-    # realised routing: distinct experts per layer
+    def step():
+        for h, xi, y in zip(handles, ins, ys):
+            h.forward(xi, y, stream=stream)
+
+    # realised routing: distinct experts per layer (on each layer's actual input)
+    step()
+    stream.synchronize()
     U = []
-    for h in handles:
-        _, _, cnt = h.route(x, stream=stream)
+    for h, xi in zip(handles, ins):
+        _, _, cnt = h.route(xi, stream=stream)
         stream.synchronize()
         U.append(int((cnt > 0).sum().item()))
-    tc_path = kind == "bf16" and args.path != "gemv"
+    tc_path = kind in ("bf16", "stack") and args.path != "gemv"
     kernels_per_fwd = 5 if tc_path else 3
-
-    def step():
-        for h, y in zip(handles, ys):
-            h.forward(x, y, stream=stream)
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -283,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
     dom_ms = tot[dom][0] / max(tot[dom][1], 1)
     pk = peaks()
     Umean = sum(U) / len(U)
-    b_exp = B_EXP_BF16 if kind == "bf16" else B_EXP_NVFP4
+    b_exp = B_EXP_NVFP4 if kind == "nvfp4" else B_EXP_BF16
     d, E, F = spec.d, spec.num_experts, spec.ffn
     per_kernel_bytes = {
         "route": 4 * d * E + 4 * E + T * d * 2,
@@ -320,7 +328,9 @@ def run_ours(args, rank, world, local_rank):
              "hbm_frac_of_8tbs": round(layer_bytes / layer_time_s / 1e9 / 8000.0, 4),
              "tflops": round(layer_flops / layer_time_s / 1e12, 2)}
 
-    # end to end through the C ABI with host buffers: H2D x, forward, D2H y, every layer
+    # end to end with host buffers, host<->device copies inside the timed region:
+    # independent layers go through moe_forward_host (copy in, forward, copy out);
+    # the chained stack copies its input in and its output out around the chain
     xh = x.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
     for h in handles[:2]:
@@ -331,18 +341,26 @@ def run_ours(args, rank, world, local_rank):
     e_steps = max(1, min(args.steps, 10))
     t0 = time.perf_counter()
     for _ in range(e_steps):
-        for h in handles:
-            h.forward_host(xh, yh, stream=stream)
+        if chain:
+            with torch.cuda.stream(stream):
+                x.copy_(xh, non_blocking=True)
+                step()
+                yh.copy_(ys[-1], non_blocking=True)
+            stream.synchronize()
+        else:
+            for h in handles:
+                h.forward_host(xh, yh, stream=stream)
     e_s = time.perf_counter() - t0
     if world > 1:
         tt = torch.tensor([e_s], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e_s = float(tt.item())
+    io_layers = 1 if chain else n_layers
     e2e = {"value": round(world * T * n_layers * e_steps / e_s, 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": T * spec.d * 2 * n_layers, "d2h_bytes_per_step": T * spec.d * 2 * n_layers}
+           "h2d_bytes_per_step": T * spec.d * 2 * io_layers, "d2h_bytes_per_step": T * spec.d * 2 * io_layers}
 
     sweep = {}
-    if args.sweep and rank == 0 and world == 1:
+    if args.sweep and rank == 0 and world == 1 and args.workload.startswith("decode"):
         for wname in SWEEP:
             sweep[wname] = sweep_point(args, wname, handles, spec, device, stream)
 
@@ -359,12 +377,14 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         out = {"metric": "MoE-layer tokens/s", "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": kind,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "nvfp4" if kind == "nvfp4" else "bf16",
                "data": "synthetic (seeded N(0,0.02) weights drawn on the device, N(0,1) activations)",
                "config": {"workload": f"flint_moe_layer_{args.workload}", "tokens": T, "d": spec.d,
                           "experts": spec.num_experts, "shared_experts": 1, "top_k": spec.top_k,
                           "expert_ffn": spec.ffn, "weights": kind, "layers_per_step": n_layers,
                           "l2": f"inputs larger than L2: {n_layers} distinct layers' weights per step",
+                          "chained": chain, "router_bias": spec.bias,
                           "parallelism": f"replicas{world}", "path": args.path},
                "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": args.steps * n_layers * kernels_per_fwd, "clocks": clocks}

@@ -31,9 +31,10 @@ TID_SGATE, TID_SUP, TID_SDOWN, TID_ZIPF_PERM = 6, 7, 8, 9
 
 # Router-bias scale for the Zipf(1.1) skewed-load workload.  Fitted once by
 # oracle/fit_zipf_alpha.py on a calibration seed (seed 1000) so that the
-# realised per-expert load, ranked, falls with a log-log slope of -1.1.
+# realised per-expert load of N(0, 1) tokens, ranked, falls with a log-log
+# slope of -1.1 over the 64 most loaded experts.
 ZIPF_S = 1.1
-ZIPF_ALPHA = 0.62
+ZIPF_ALPHA = 0.5324
 
 
 @dataclasses.dataclass(frozen=True)

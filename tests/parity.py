@@ -9,6 +9,11 @@ Tolerances (the layer's acceptance bounds):
     (fp32 logits and an fp32 exp/divide: a few units of fp32 rounding);
   - output max-abs <= 2e-2 and rel-L2 <= 1e-2 for bf16 weights, rel-L2 <=
     5e-2 for NVFP4 weights; rel-L2 = ||y_gpu - y_ref||_2 / ||y_ref||_2.
+    When the output carries the residual x (values of several units) and is
+    stored in bf16, the max-abs bound is 2e-2 plus one bf16 unit in the last
+    place of the reference value: the output format's resolution there
+    exceeds 2e-2 (2^-5 for |y| in [4, 8)), and a sum computed to fp32
+    accuracy may round to either bf16 neighbour of the exact one.
 """
 import numpy as np
 import torch
@@ -20,6 +25,12 @@ GAP = 1e-4
 GATE_ATOL = 2e-5
 MAX_ABS = 2e-2
 REL_L2 = {"f32": 1e-2, "bf16": 1e-2, "nvfp4": 5e-2}
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (normal range)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    return np.exp2(e - 7)
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -81,6 +92,7 @@ def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tens
     max_abs = float(np.max(np.abs(err)))
     rel = float(np.linalg.norm(err) / max(np.linalg.norm(y_ref), 1e-30))
     assert np.all(np.isfinite(yg))
-    assert max_abs <= MAX_ABS, (max_abs, rel)
+    bound = MAX_ABS + (bf16_ulp(y_ref) if residual and y_gpu.dtype == torch.bfloat16 else 0.0)
+    assert np.all(np.abs(err) <= bound), (max_abs, rel)
     assert rel <= REL_L2[fmt], (max_abs, rel)
     return {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near}
