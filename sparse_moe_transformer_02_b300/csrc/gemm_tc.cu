@@ -18,6 +18,10 @@
 //    slot's gate and adds into an fp32 accumulator y_acc[t][row] with
 //    red.global.add (order of the adds is not fixed: the fp32 sum is
 //    deterministic up to rounding order).
+//  * pass 2 for large batches (token-major): A = h of 128 slots, B = 256 rows
+//    of Wd, D[slot][row]; each epilogue thread owns one slot, so it looks up
+//    one (token, gate) pair per tile and adds 16 consecutive outputs with four
+//    red.global.add.v4.f32 (a quarter of the atomic requests of pass 2).
 //  * finalise: y = bf16(y_acc (+ x)).
 //
 // One persistent CTA per SM, 6 warps: warp 0 issues TMA into a ring of
@@ -41,10 +45,16 @@ template <> struct TcCfg<0> {     // gate/up: A_g + A_u + B per stage
   static constexpr int ACC_COLS = 2 * kTcBN;          // per buffer: gate then up
   static constexpr int TMEM_COLS = 2 * ACC_COLS;      // two buffers
 };
-template <> struct TcCfg<1> {     // down: A + B per stage
+template <> struct TcCfg<1> {     // down, weight-major: A (128 Wd rows) + B (h of <= 128 slots)
   static constexpr int STAGES = 6;
   static constexpr int STAGE_BYTES = kTcBM * 128 + kTcBN * 128;
   static constexpr int ACC_COLS = kTcBN;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+};
+template <> struct TcCfg<2> {     // down, token-major: A (h of 128 slots) + B (256 Wd rows)
+  static constexpr int STAGES = 4;
+  static constexpr int STAGE_BYTES = kTcBM * 128 + 2 * kTcBN * 128;
+  static constexpr int ACC_COLS = 2 * kTcBN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
 };
 
@@ -144,7 +154,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   pdl_launch_dependents();
   const WaitCtl wc{p.wait_ns, p.err, abort_flag};
 
-  if (MODE == 1) pdl_wait();
+  constexpr int LIST = MODE == 0 ? 0 : 1;       // unit list: gate/up or down
+  if (MODE >= 1) pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -155,27 +166,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     bool issued[S];
     for (int i = 0; i < S; ++i) issued[i] = false;
     int n_total = p.n_pre;
-    bool waited = MODE == 1;
-    if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+    bool waited = MODE >= 1;
+    if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
     bool ok = true;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
         pdl_wait();
         waited = true;
-        n_total = __ldcg(p.n_units + MODE);
+        n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
       }
       const TcUnit un = get_unit(p, u);
       const bool sh = un.expert == p.E;
-      const int n_pad = (un.n + 15) & ~15;
       const int K = sh ? p.Ks : p.K;
-      const int arow = sh ? un.m_tile * kTcBM : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * kTcBM;
+      const int wrows = MODE == 2 ? 2 * kTcBN : kTcBM;          // weight rows per tile
+      const int arow = sh ? un.m_tile * wrows : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * wrows;
       const CUtensorMap* ma0 = sh ? &p.tm_sa0 : &p.tm_a0;
       const CUtensorMap* ma1 = sh ? &p.tm_sa1 : &p.tm_a1;
-      const uint32_t bytes = (MODE == 0 ? 2 : 1) * kTcBM * 128 + kTcBN * 128;
+      const uint32_t bytes = MODE == 0 ? 2 * kTcBM * 128 + kTcBN * 128 : (uint32_t)C::STAGE_BYTES;
       const CUtensorMap* mb = sh ? &p.tm_sb : &p.tm_b;
-      const int brow = (MODE == 1 && sh) ? p.T * p.k + un.slot0 : un.slot0;
+      const int brow = (MODE >= 1 && sh) ? p.T * p.k + un.slot0 : un.slot0;
       for (int k0 = 0; k0 < K; k0 += kTcBK) {
         if (!warp_wait(&empty[stage], phase ^ 1, wc)) { ok = false; break; }
         uint8_t* st = stages + stage * C::STAGE_BYTES;
@@ -183,9 +194,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           mbar_arrive_expect_tx(&full[stage], bytes);
           // weights are streamed once: evict them first so that the activations,
           // h and the fp32 accumulator stay in L2
-          tma_load_2d_hint(st, ma0, k0, arow, &full[stage], pol);
-          if (MODE == 0) tma_load_2d_hint(st + kTcBM * 128, ma1, k0, arow, &full[stage], pol);
-          tma_load_2d(st + (MODE == 0 ? 2 : 1) * kTcBM * 128, mb, k0, brow, &full[stage]);
+          if (MODE == 2) {
+            tma_load_2d(st, mb, k0, brow, &full[stage]);                          // h: 128 slots
+            tma_load_2d_hint(st + kTcBM * 128, ma0, k0, arow, &full[stage], pol);  // Wd: 256 rows
+          } else {
+            tma_load_2d_hint(st, ma0, k0, arow, &full[stage], pol);
+            if (MODE == 0) tma_load_2d_hint(st + kTcBM * 128, ma1, k0, arow, &full[stage], pol);
+            tma_load_2d(st + (MODE == 0 ? 2 : 1) * kTcBM * 128, mb, k0, brow, &full[stage]);
+          }
         }
         __syncwarp();
         issued[stage] = true;
@@ -205,8 +221,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       uint32_t tph[2] = {0, 0};
       int buf = 0;
       int n_total = p.n_pre;
-      bool waited = MODE == 1;
-      if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+      bool waited = MODE >= 1;
+      if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
       bool ok = true;
       uint64_t* last_commit = nullptr;
       uint32_t last_commit_par = 0;
@@ -215,14 +231,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           if (waited) break;
           pdl_wait();
           waited = true;
-          n_total = __ldcg(p.n_units + MODE);
+          n_total = __ldcg(p.n_units + LIST);
           if (u >= n_total) break;
         }
         const TcUnit un = get_unit(p, u);
         const bool sh = un.expert == p.E;
         const int n_pad = (un.n + 15) & ~15;
         const int K = sh ? p.Ks : p.K;
-        const uint32_t idesc = idesc_bf16_f32(kTcBM, n_pad);
+        const uint32_t idesc = MODE == 2 ? idesc_bf16_f32(kTcBM, 2 * kTcBN) : idesc_bf16_f32(kTcBM, n_pad);
         if (!mbar_wait(&tempty[buf], tph[buf] ^ 1, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::ACC_COLS;
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
               const uint64_t bd = sdesc_sw128(st + 2 * kTcBM * 128 + kk * 32);
               tc_mma_f16(acc, sdesc_sw128(st + kk * 32), bd, idesc, accum);
               tc_mma_f16(acc + kTcBN, sdesc_sw128(st + kTcBM * 128 + kk * 32), bd, idesc, accum);
-            } else {
+            } else {   // MODE 1: A = Wd rows, B = h; MODE 2: A = h, B = Wd rows
               tc_mma_f16(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + kTcBM * 128 + kk * 32), idesc, accum);
             }
           }
@@ -268,14 +284,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     uint32_t tph[2] = {0, 0};
     int buf = 0;
     int n_total = p.n_pre;
-    bool waited = MODE == 1;
-    if (MODE == 1) n_total = __ldcg(p.n_units + 1);
+    bool waited = MODE >= 1;
+    if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
     for (int u = blockIdx.x;; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
         pdl_wait();
         waited = true;
-        n_total = __ldcg(p.n_units + MODE);
+        n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
       }
       const TcUnit un = get_unit(p, u);
@@ -300,6 +316,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           col_gate[q * kTcBN + c] = g;
         }
         __syncwarp();
+      }
+      if (MODE == 2) {
+        // this thread's slot (row of the tile): token and gate, once per tile
+        const int r = q * 32 + lane;
+        int t = 0;
+        float g = 0.f;
+        if (r < un.n) {
+          if (sh) {
+            t = un.slot0 + r;
+            g = 1.f;
+          } else {
+            const int src = __ldcg(p.src_of_slot + un.slot0 + r);
+            t = src / p.k;
+            g = __ldcg(p.gate + src);
+          }
+        }
+        if (!warp_wait(&tfull[buf], tph[buf], wc)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
+        float* yrow = p.yacc + (size_t)t * p.d + un.m_tile * (2 * kTcBN);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 2 * kTcBN; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(acc + c0, v);
+          tmem_ld_wait();
+          if (r < un.n) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              red_add_v4_f32(yrow + c0 + i, g * __uint_as_float(v[i]), g * __uint_as_float(v[i + 1]),
+                             g * __uint_as_float(v[i + 2]), g * __uint_as_float(v[i + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+        tph[buf] ^= 1;
+        buf ^= 1;
+        continue;
       }
       if (!warp_wait(&tfull[buf], tph[buf], wc)) break;
       tc_fence_after();
@@ -454,6 +507,8 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
                                          (int)tc_smem_bytes<0>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<1>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<2>());
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -492,18 +547,24 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // pass 2: down
-  p.tm_a0 = *a.tm_wd; p.tm_a1 = *a.tm_wd;
-  p.tm_sa0 = a.Fs > 0 ? *a.tm_sd : *a.tm_wd; p.tm_sa1 = p.tm_sa0;
+  const bool tok_major = a.dn_rows == 2 * kTcBN;
+  const CUtensorMap* wd = tok_major ? a.tm_wd256 : a.tm_wd;
+  const CUtensorMap* sd = tok_major ? a.tm_sd256 : a.tm_sd;
+  p.tm_a0 = *wd; p.tm_a1 = *wd;
+  p.tm_sa0 = a.Fs > 0 ? *sd : *wd; p.tm_sa1 = p.tm_sa0;
   p.tm_b = *a.tm_h;
   p.tm_sb = *a.tm_h;
   p.K = a.F; p.Ks = a.Fs > 0 ? a.Fs : a.F;
-  p.mt = a.d / kTcBM;
-  p.mt_s = a.d / kTcBM;
+  p.mt = a.d / a.dn_rows;
+  p.mt_s = a.d / a.dn_rows;
   p.n_pre = 0;
   p.units = a.ws.units_dn;
   const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
   if (prof) prof->begin(MOE_K_TC_DOWN, s);
-  e = launch_ex(tc_kernel<1>, grid2, kThreadsTc, tc_smem_bytes<1>(), s, p);
+  if (tok_major)
+    e = launch_ex(tc_kernel<2>, grid2, kThreadsTc, tc_smem_bytes<2>(), s, p);
+  else
+    e = launch_ex(tc_kernel<1>, grid2, kThreadsTc, tc_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise

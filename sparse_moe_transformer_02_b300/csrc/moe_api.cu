@@ -20,7 +20,8 @@ struct moe_layer {
   int n_counters = 64;
   uint64_t wait_ns = 0;
   int max_units_gu = 0, max_units_dn = 0;
-  CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp, tm_wr;
+  CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp, tm_wr, tm_wd256, tm_sd256;
+  bool tok_major_ok = false;   // 256-row down maps exist
   void* block = nullptr;
   Prof prof;
 };
@@ -134,6 +135,7 @@ RouteArgs route_args(const moe_layer* h, const void* x, int T, int32_t* idx, flo
   a.counts_out = counts;
   a.ws = h->ws;
   a.build_tc_units = tc_units ? 1 : 0;
+  a.dn_rows = (tc_units && T >= kTokMajorT && h->tok_major_ok) ? 2 * kTcBN : kTcBM;
   a.F = h->cfg.ffn;
   a.Fs = h->cfg.shared_ffn;
   a.has_shared = h->cfg.shared_ffn > 0;
@@ -208,6 +210,8 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
     a.tm_xp = &h->tm_xp;
     a.tm_wg = &h->tm_wg; a.tm_wu = &h->tm_wu; a.tm_sg = &h->tm_sg; a.tm_su = &h->tm_su;
     a.tm_wd = &h->tm_wd; a.tm_sd = &h->tm_sd; a.tm_h = &h->tm_h;
+    a.tm_wd256 = &h->tm_wd256; a.tm_sd256 = &h->tm_sd256;
+    a.dn_rows = (T >= kTokMajorT && h->tok_major_ok) ? 2 * kTcBN : kTcBM;
     a.x = x;
     a.y = y;
     a.gate = gate;
@@ -362,6 +366,11 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       ok = make_map_bf16(&h->tm_sg, w->ws_gate, Fs, d, kTcBM, kTcBK) &&
            make_map_bf16(&h->tm_su, w->ws_up, Fs, d, kTcBM, kTcBK) &&
            make_map_bf16(&h->tm_sd, w->ws_down, d, Fs, kTcBM, kTcBK);
+    if (ok && d % (2 * kTcBN) == 0) {
+      h->tok_major_ok = make_map_bf16(&h->tm_wd256, w->w_down, E * d, F, 2 * kTcBN, kTcBK) &&
+                        (Fs == 0 || make_map_bf16(&h->tm_sd256, w->ws_down, d, Fs, 2 * kTcBN, kTcBK));
+      if (Fs == 0) h->tm_sd256 = h->tm_wd256;
+    }
     if (!ok) {
       if (c.path == MOE_PATH_TC) {
         cudaFree(h->block);

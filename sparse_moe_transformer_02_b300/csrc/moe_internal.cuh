@@ -19,6 +19,7 @@ constexpr int kFinRows = 32;         // GEMV down: rows finalised together by th
 constexpr int kTcBN = 128;           // tcgen05 path: largest token tile (MMA N)
 constexpr int kTcBM = 128;           // tcgen05 path: weight rows per tile (MMA M)
 constexpr int kTcBK = 64;            // tcgen05 path: reduction step per stage (128 bytes of bf16)
+constexpr int kTokMajorT = 512;      // tcgen05 path: T at which the down pass turns token-major
 constexpr unsigned kErrTimeout = 1u << 5;
 
 // One unit of tcgen05 work: expert (E = the shared expert), weight-row tile,
@@ -91,6 +92,7 @@ struct RouteArgs {
   int32_t* counts_out;    // [E] or nullptr
   Workspace ws;
   int build_tc_units;     // also build tcgen05 unit lists
+  int dn_rows;            // Wd rows per down tile (128 weight-major, 256 token-major)
   int F, Fs;              // widths (for unit lists)
   int has_shared;
 };
@@ -148,6 +150,9 @@ struct TcArgs {
   const CUtensorMap* tm_su;
   const CUtensorMap* tm_wd;     // [E*d][F]
   const CUtensorMap* tm_sd;     // [d][Fs]
+  const CUtensorMap* tm_wd256;  // [E*d][F], box 64 x 256 (token-major down pass)
+  const CUtensorMap* tm_sd256;  // [d][Fs], box 64 x 256
+  int dn_rows;                  // Wd rows per down tile: 128 (weight-major) or 256 (token-major)
   const CUtensorMap* tm_h;      // [slots][F_max] (box 64 x kTcBN)
   const void* x;
   void* y;

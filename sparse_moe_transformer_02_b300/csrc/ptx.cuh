@@ -220,5 +220,9 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
+// Four consecutive floats (16-byte aligned address) in one request.
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 
 }  // namespace moe

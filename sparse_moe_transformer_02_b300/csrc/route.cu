@@ -170,7 +170,7 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
   __syncthreads();
   if (!a.build_tc_units) return;
   // tcgen05 units: shared expert first, then routed experts in index order.
-  const int mt_gu = a.F / kTcBM, mt_dn = a.d / kTcBM;
+  const int mt_gu = a.F / kTcBM, mt_dn = a.d / a.dn_rows;
   const int sh_tb = a.has_shared ? (a.T + kTcBN - 1) / kTcBN : 0;
   const int sh_mt_gu = a.has_shared ? a.Fs / kTcBM : 0;
   for (int pass = 0; pass < 2; ++pass) {

@@ -115,3 +115,39 @@ def test_route_and_grouping_large_batch(flint_bf16, small, which):
     assert np.array_equal(offs.cpu().numpy(), offsets)
     assert np.array_equal(tos.cpu().numpy(), tok_of_slot)
     assert np.array_equal(so.cpu().numpy(), slot_of)
+
+
+WIDE = I.LayerSpec(d=384, ffn=256, shared_ffn=128, num_experts=16, top_k=4)
+
+
+@pytest.mark.parametrize("T", [511, 512, 900])
+def test_token_major_down_pass_boundary(small, T):
+    """From 512 tokens on the down pass runs token-major (256 Wd rows per tile)."""
+    L, dev = small
+    x = I.make_tokens(SMALL, seed=T, T=T)
+    _, y, idx, gate = run(SMALL, dev, x, 900, path=B.MOE_PATH_TC)
+    check_layer(L, x, y, idx, gate, SMALL.top_k, "bf16")
+
+
+def test_down_pass_layouts_agree(small):
+    """The same 511 tokens through the weight-major (T = 511) and the token-major
+    (T = 512, one extra token) down pass: same routing, outputs equal to fp32
+    accumulation order."""
+    L, dev = small
+    x = I.make_tokens(SMALL, seed=77, T=512)
+    _, y_a, idx_a, _ = run(SMALL, dev, x[:511], 512, path=B.MOE_PATH_TC)
+    _, y_b, idx_b, _ = run(SMALL, dev, x, 512, path=B.MOE_PATH_TC)
+    assert torch.equal(idx_a, idx_b[:511])
+    a, b = y_a.double(), y_b[:511].double()
+    assert ((a - b).norm() / b.norm()).item() < 2e-3
+
+
+@pytest.mark.parametrize("spec", [NOSHARED, WIDE], ids=["no_shared", "d384"])
+def test_token_major_no_shared_and_narrow_d(spec):
+    """No shared expert (token-major pass on routed tiles only), and d = 384
+    (not a multiple of 256: the weight-major pass stays in use)."""
+    L = I.make_layer(spec, seed=3)
+    dev = B.upload_layer(L)
+    x = I.make_tokens(spec, seed=3, T=700)
+    _, y, idx, gate = run(spec, dev, x, 700, path=B.MOE_PATH_TC)
+    check_layer(L, x, y, idx, gate, spec.top_k, "bf16")
