@@ -53,54 +53,96 @@ __device__ __forceinline__ void ticket_last(unsigned int* counter, unsigned n, i
   __syncthreads();
 }
 
-// (value, index) order of the selection: larger value first, lower index on ties.
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+
+// Selection keys: (logit, expert) packed into 64 bits so that unsigned order
+// is the selection order (larger logit first, lower index on equal logits).
+// NaN counts as -inf and -0 as +0, as in the float comparison.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+  v = isnan(v) ? -INFINITY : v + 0.0f;
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint32_t)(0x7FFFFFFF - e);
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+  uint32_t u = (uint32_t)(k >> 32);
+  u = (u & 0x80000000u) ? (u ^ 0x80000000u) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_index(uint64_t k) { return 0x7FFFFFFF - (int)(uint32_t)k; }
+__device__ __forceinline__ void cswap(uint64_t& a, uint64_t& b) {   // a >= b afterwards
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+// Sorts 8 keys in descending order (19-comparator network, depth 6).
+__device__ __forceinline__ void sort8(uint64_t (&a)[8]) {
+  cswap(a[0], a[1]); cswap(a[2], a[3]); cswap(a[4], a[5]); cswap(a[6], a[7]);
+  cswap(a[0], a[2]); cswap(a[1], a[3]); cswap(a[4], a[6]); cswap(a[5], a[7]);
+  cswap(a[1], a[2]); cswap(a[5], a[6]); cswap(a[0], a[4]); cswap(a[3], a[7]);
+  cswap(a[1], a[5]); cswap(a[2], a[6]);
+  cswap(a[1], a[4]); cswap(a[3], a[6]);
+  cswap(a[2], a[4]); cswap(a[3], a[5]);
+  cswap(a[3], a[4]);
+}
+// r = top 8 of the descending lists r and b, descending (bitonic merge).
+__device__ __forceinline__ void merge_top8(uint64_t (&r)[8], const uint64_t (&b)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = r[i] > b[7 - i] ? r[i] : b[7 - i];
+#pragma unroll
+  for (int dd = 4; dd >= 1; dd >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & dd) == 0) cswap(r[i], r[i + dd]);
 }
 
-// Top-k of one token's E logits by one warp.  vals[i] holds expert lane + 32 i.
-// Writes idx/gate for the token.  NaN logits are ordered below every number.
-template <int NPL>
-__device__ void warp_topk(float (&vals)[NPL], int E, int k, int32_t* idx_t, float* gate_t, int32_t* sidx_t) {
+// Top k of one token's E logits by one warp; row(e) returns logit e.  Lane l
+// scores experts l NPL .. l NPL + NPL - 1 and keeps its best 8 as sorted keys;
+// five butterfly merges then leave the warp's best 8 in every lane.  Writes
+// idx/gate (and sidx, if given) for the token.
+template <int NPL, typename Row>
+__device__ void warp_topk(const Row& row, int E, int k, int32_t* idx_t, float* gate_t, int32_t* sidx_t) {
+  static_assert(NPL == 8 || NPL == 16, "8 or 16 experts per lane");
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;
-  float selv[kMaxTopK];
-  int seli[kMaxTopK];
+  uint64_t best[8];
 #pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (isnan(vals[i])) vals[i] = -INFINITY;
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * NPL + i;
+    best[i] = e < E ? sel_key(row(e), e) : 0;             // 0 is below every real key
+  }
+  sort8(best);
+  if (NPL == 16) {
+    uint64_t b[8];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j >= k) break;
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && better(vals[i], e, bv, bi)) { bv = vals[i]; bi = e; }
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * NPL + 8 + i;
+      b[i] = e < E ? sel_key(row(e), e) : 0;
     }
+    sort8(b);
+    merge_top8(best, b);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    selv[j] = bv;
-    seli[j] = bi;
+  for (int o = 1; o < 32; o <<= 1) {
+    uint64_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = __shfl_xor_sync(0xFFFFFFFFu, best[i], o);
+    merge_top8(best, b);
   }
   if (lane == 0) {
+    float lv[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) lv[j] = key_value(best[j]);
     float z = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) z += expf(selv[j] - selv[0]);
+      if (j < k) z += expf(lv[j] - lv[0]);
     const float inv = 1.f / z;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
       if (j < k) {
-        idx_t[j] = seli[j];
-        gate_t[j] = expf(selv[j] - selv[0]) * inv;
-        if (sidx_t) sidx_t[j] = seli[j];
+        const int e = key_index(best[j]);
+        idx_t[j] = e;
+        gate_t[j] = expf(lv[j] - lv[0]) * inv;
+        if (sidx_t) sidx_t[j] = e;
       }
   }
 }
@@ -250,27 +292,36 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
     float acc[kSmallTok];
 #pragma unroll
     for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
-#pragma unroll 4
-    for (int c = lane * 4; c < d; c += 128) {
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(w + c));
+    // 16 loads of the router row in flight per lane (one round trip for d = 2048)
+    for (int cb = lane * 4; cb < d; cb += 128 * 16) {
+      float4 wr[16];
 #pragma unroll
-      for (int t = 0; t < kSmallTok; ++t) {
-        if (t < nt) {
-          float xv[4];
-          if (a.act_bf16) {
-            const uint2 r = *reinterpret_cast<const uint2*>(xs + ((size_t)t * d + c) * 2);
-            xv[0] = __uint_as_float(r.x << 16);
-            xv[1] = __uint_as_float(r.x & 0xFFFF0000u);
-            xv[2] = __uint_as_float(r.y << 16);
-            xv[3] = __uint_as_float(r.y & 0xFFFF0000u);
-          } else {
-            const float4 r = *reinterpret_cast<const float4*>(xs + ((size_t)t * d + c) * 4);
-            xv[0] = r.x; xv[1] = r.y; xv[2] = r.z; xv[3] = r.w;
+      for (int i = 0; i < 16; ++i)
+        wr[i] = cb + 128 * i < d ? __ldg(reinterpret_cast<const float4*>(w + cb + 128 * i))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = cb + 128 * i;
+        if (c >= d) break;
+#pragma unroll
+        for (int t = 0; t < kSmallTok; ++t) {
+          if (t < nt) {
+            float xv[4];
+            if (a.act_bf16) {
+              const uint2 r = *reinterpret_cast<const uint2*>(xs + ((size_t)t * d + c) * 2);
+              xv[0] = __uint_as_float(r.x << 16);
+              xv[1] = __uint_as_float(r.x & 0xFFFF0000u);
+              xv[2] = __uint_as_float(r.y << 16);
+              xv[3] = __uint_as_float(r.y & 0xFFFF0000u);
+            } else {
+              const float4 r = *reinterpret_cast<const float4*>(xs + ((size_t)t * d + c) * 4);
+              xv[0] = r.x; xv[1] = r.y; xv[2] = r.z; xv[3] = r.w;
+            }
+            acc[t] = fmaf(wr[i].x, xv[0], acc[t]);
+            acc[t] = fmaf(wr[i].y, xv[1], acc[t]);
+            acc[t] = fmaf(wr[i].z, xv[2], acc[t]);
+            acc[t] = fmaf(wr[i].w, xv[3], acc[t]);
           }
-          acc[t] = fmaf(wv.x, xv[0], acc[t]);
-          acc[t] = fmaf(wv.y, xv[1], acc[t]);
-          acc[t] = fmaf(wv.z, xv[2], acc[t]);
-          acc[t] = fmaf(wv.w, xv[3], acc[t]);
         }
       }
     }
@@ -286,13 +337,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
   if (!s_last) return;
   if (warp < nt) {
     const int t = t0 + warp;
-    float v[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int ee = lane + 32 * i;
-      v[i] = ee < E ? __ldcg(a.ws.logits + (size_t)t * E + ee) : -INFINITY;
-    }
-    warp_topk<kMaxExperts / 32>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, nullptr);
+    const float* lrow = a.ws.logits + (size_t)t * E;
+    auto row = [lrow](int e) { return __ldcg(lrow + e); };
+    if (E <= 256)
+      warp_topk<8>(row, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, nullptr);
+    else
+      warp_topk<16>(row, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, nullptr);
   }
   if (threadIdx.x == 0) a.ws.counters[1 + blockIdx.y] = 0;
   ticket_last(&a.ws.counters[0], gridDim.y, &s_last);
@@ -400,13 +450,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_large_kernel(RouteArgs a)
   for (int tt = warp; tt < kLargeBT; tt += kRouteThreads / 32) {
     const int t = t0 + tt;
     if (t >= T) break;
-    float v[EJ * 4];
-#pragma unroll
-    for (int i = 0; i < EJ * 4; ++i) {
-      const int ee = lane + 32 * i;
-      v[i] = ee < E ? lg[tt * Ep + ee] : -INFINITY;
-    }
-    warp_topk<EJ * 4>(v, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + tt * k);
+    const float* lrow = lg + tt * Ep;
+    auto row = [lrow](int e) { return lrow[e]; };
+    if (E <= 256)
+      warp_topk<8>(row, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + tt * k);
+    else
+      warp_topk<16>(row, E, k, a.idx + (size_t)t * k, a.gate + (size_t)t * k, s_idx + tt * k);
   }
   __syncthreads();
   for (int s = tid; s < kLargeBT * k; s += kRouteThreads) {
@@ -447,47 +496,6 @@ struct RouteTcParams {
   uint64_t* cand;          // [T][E / 64][kMaxTopK] per-slice selection keys
   uint64_t wait_ns;
 };
-
-// Selection keys: (logit, expert) packed into 64 bits so that unsigned order
-// is the selection order (larger logit first, lower index on equal logits).
-// NaN counts as -inf and -0 as +0, as in the float comparison.
-__device__ __forceinline__ uint64_t sel_key(float v, int e) {
-  v = isnan(v) ? -INFINITY : v + 0.0f;
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((uint64_t)u << 32) | (uint32_t)(0x7FFFFFFF - e);
-}
-__device__ __forceinline__ float key_value(uint64_t k) {
-  uint32_t u = (uint32_t)(k >> 32);
-  u = (u & 0x80000000u) ? (u ^ 0x80000000u) : ~u;
-  return __uint_as_float(u);
-}
-__device__ __forceinline__ int key_index(uint64_t k) { return 0x7FFFFFFF - (int)(uint32_t)k; }
-__device__ __forceinline__ void cswap(uint64_t& a, uint64_t& b) {   // a >= b afterwards
-  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-  a = hi;
-  b = lo;
-}
-// Sorts 8 keys in descending order (19-comparator network, depth 6).
-__device__ __forceinline__ void sort8(uint64_t (&a)[8]) {
-  cswap(a[0], a[1]); cswap(a[2], a[3]); cswap(a[4], a[5]); cswap(a[6], a[7]);
-  cswap(a[0], a[2]); cswap(a[1], a[3]); cswap(a[4], a[6]); cswap(a[5], a[7]);
-  cswap(a[1], a[2]); cswap(a[5], a[6]); cswap(a[0], a[4]); cswap(a[3], a[7]);
-  cswap(a[1], a[5]); cswap(a[2], a[6]);
-  cswap(a[1], a[4]); cswap(a[3], a[6]);
-  cswap(a[2], a[4]); cswap(a[3], a[5]);
-  cswap(a[3], a[4]);
-}
-// r = top 8 of the descending lists r and b, descending (bitonic merge).
-__device__ __forceinline__ void merge_top8(uint64_t (&r)[8], const uint64_t (&b)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) r[i] = r[i] > b[7 - i] ? r[i] : b[7 - i];
-#pragma unroll
-  for (int dd = 4; dd >= 1; dd >>= 1)
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((i & dd) == 0) cswap(r[i], r[i + dd]);
-}
 
 __global__ void __launch_bounds__(192, 1) route_tc_kernel(const __grid_constant__ RouteTcParams p) {
   const RouteArgs& a = p.a;
