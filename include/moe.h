@@ -51,7 +51,9 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,   /* shape or dtype combination this build does not implement */
   MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch error, no device, ...) */
   MOE_ERR_OOM = 4,           /* workspace allocation failed in moe_create */
-  MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out (reported by moe_check) */
+  MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out (reported by moe_check) */
+  MOE_ERR_RANGE = 6          /* NVFP4 weights on the tensor-core path: an intermediate h / xs^2 exceeded
+                                the f16 range and was saturated (reported by moe_check) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
@@ -169,6 +171,7 @@ moe_status moe_get_grouping(moe_handle h, int32_t T, int32_t* offsets, int32_t* 
 /*
  * Synchronise `stream`, then report and clear the device error word:
  * MOE_ERR_TIMEOUT if a bounded wait ran out since the last check,
+ * MOE_ERR_RANGE if an f16 intermediate saturated since then (NVFP4 on the tensor cores),
  * MOE_ERR_CUDA if the stream reported an error, else MOE_OK.
  */
 moe_status moe_check(moe_handle h, cudaStream_t stream);

@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["moe_api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "route_noalloc.cu"]
+SOURCES = ["moe_api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "gemm_tc_fp4.cu", "route_noalloc.cu"]
 HEADERS = ["moe_internal.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

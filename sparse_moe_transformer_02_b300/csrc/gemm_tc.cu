@@ -86,26 +86,6 @@ __device__ __forceinline__ TcUnit get_unit(const TcParams& p, int u) {
   return p.units[u];
 }
 
-// Bounded wait that ignores the abort flag (used to drain copies in flight
-// before the CTA leaves after an abort).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > limit_ns) return;
-}
-
-// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and on
-// success every lane observes the completed phase itself.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  if (ok)
-    while (!mbar_try_wait(bar, parity)) {
-    }
-  return ok != 0;
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<MODE>;
@@ -487,17 +467,29 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), int grid, int block, size_t smem
 
 }  // namespace
 
-int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k) {
+int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k, int tile_n) {
   (void)d;
-  const long long routed = (long long)(F / kTcBM) * ((long long)T * k / kTcBN + E);
-  const long long shared = (long long)(Fs / kTcBM) * ((T + kTcBN - 1) / kTcBN);
+  const long long routed = (long long)(F / kTcBM) * ((long long)T * k / tile_n + E);
+  const long long shared = (long long)(Fs / kTcBM) * ((T + tile_n - 1) / tile_n);
   return (int)(routed + shared);
 }
-int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k) {
+int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n) {
   (void)F;
-  const long long routed = (long long)(d / kTcBM) * ((long long)T * k / kTcBN + E);
-  const long long shared = Fs > 0 ? (long long)(d / kTcBM) * ((T + kTcBN - 1) / kTcBN) : 0;
+  const long long routed = (long long)(d / kTcBM) * ((long long)T * k / tile_n + E);
+  const long long shared = Fs > 0 ? (long long)(d / kTcBM) * ((T + tile_n - 1) / tile_n) : 0;
   return (int)(routed + shared);
+}
+
+cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, int num_sms,
+                               cudaStream_t s, Prof* prof) {
+  const size_t n8 = n / 8;
+  const int grid = (int)((n8 + 255) / 256 < (size_t)num_sms * 4 ? (n8 + 255) / 256 : (size_t)num_sms * 4);
+  if (prof) prof->begin(MOE_K_TC_FINALIZE, s);
+  const cudaError_t e = launch_ex(tc_finalize_kernel, grid > 0 ? grid : 1, 256, 0, s, yacc,
+                                  static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), n8,
+                                  (int)residual);
+  if (prof) prof->end(s);
+  return e;
 }
 
 cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
@@ -568,14 +560,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise
-  const size_t n8 = (size_t)a.T * a.d / 8;
-  const int grid3 = (int)((n8 + 255) / 256 < (size_t)num_sms * 4 ? (n8 + 255) / 256 : (size_t)num_sms * 4);
-  if (prof) prof->begin(MOE_K_TC_FINALIZE, s);
-  e = launch_ex(tc_finalize_kernel, grid3 > 0 ? grid3 : 1, 256, 0, s, (const float*)a.ws.yacc,
-                static_cast<const __nv_bfloat16*>(a.x), static_cast<__nv_bfloat16*>(a.y), n8,
-                (int)a.add_residual);
-  if (prof) prof->end(s);
-  return e;
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, num_sms, s, prof);
 }
 
 }  // namespace moe

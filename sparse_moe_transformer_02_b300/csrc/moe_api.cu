@@ -22,6 +22,8 @@ struct moe_layer {
   int max_units_gu = 0, max_units_dn = 0;
   CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd, tm_h, tm_xp, tm_wr, tm_wd256, tm_sd256;
   bool tok_major_ok = false;   // 256-row down maps exist
+  bool fp4 = false;            // NVFP4 weights (tcgen05 path decodes them into tensor memory)
+  CUtensorMap q4[3], sc4[3], sq4[3], ssc4[3];   // NVFP4 codes / block scales: gate, up, down (routed, shared)
   void* block = nullptr;
   Prof prof;
 };
@@ -35,9 +37,13 @@ inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 bool gemv_shape_ok(const moe_config& c) { return gemv_supported(c.weight_dtype, c.d, c.ffn, c.shared_ffn); }
 
 bool tc_shape_ok(const moe_config& c) {
-  return c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.d % kTcBM == 0 && c.ffn % kTcBM == 0 &&
-         c.shared_ffn % kTcBM == 0;
+  if (c.act_dtype != MOE_BF16) return false;
+  if (c.weight_dtype == MOE_BF16)
+    return c.d % kTcBM == 0 && c.ffn % kTcBM == 0 && c.shared_ffn % kTcBM == 0;
+  // NVFP4: stages of 256 K values (16 block-scale bytes per row)
+  return c.weight_dtype == MOE_NVFP4 && c.d % kTc4KS == 0 && c.ffn % kTc4KS == 0 && c.shared_ffn % kTc4KS == 0;
 }
+inline int tile_n_of(const moe_config& c) { return c.weight_dtype == MOE_NVFP4 ? kTc4BN : kTcBN; }
 
 moe_status validate_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -112,6 +118,34 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D f16 tensor [rows][cols], box {box_cols, box_rows}, 128-byte swizzle.
+bool make_map_f16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte tensor [rows][cols], box {box_cols, box_rows}; 128-byte swizzle or none.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -135,7 +169,8 @@ RouteArgs route_args(const moe_layer* h, const void* x, int T, int32_t* idx, flo
   a.counts_out = counts;
   a.ws = h->ws;
   a.build_tc_units = tc_units ? 1 : 0;
-  a.dn_rows = (tc_units && T >= kTokMajorT && h->tok_major_ok) ? 2 * kTcBN : kTcBM;
+  a.dn_rows = (tc_units && !h->fp4 && T >= kTokMajorT && h->tok_major_ok) ? 2 * kTcBN : kTcBM;
+  a.tile_n = tile_n_of(h->cfg);
   a.F = h->cfg.ffn;
   a.Fs = h->cfg.shared_ffn;
   a.has_shared = h->cfg.shared_ffn > 0;
@@ -199,6 +234,33 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
   // the caller asked for GEMV up to gemv_max_tokens.
   const bool tc = c.path == MOE_PATH_TC ||
                   (c.path == MOE_PATH_AUTO && h->tc_capable && (T > c.gemv_max_tokens || !h->gemv_capable));
+  if (tc && h->fp4) {
+    CUtensorMap tm_x;
+    bool have_tm_x = false;
+    moe_status st = do_route(h, x, T, idx, gate, nullptr, true, &tm_x, &have_tm_x, s);
+    if (st != MOE_OK) return st;
+    const moe_weights& w = h->w;
+    Tc4Args a;
+    for (int m = 0; m < 3; ++m) {
+      a.q[m] = &h->q4[m]; a.sc[m] = &h->sc4[m]; a.sq[m] = &h->sq4[m]; a.ssc[m] = &h->ssc4[m];
+    }
+    a.ts[0] = w.t_gate; a.ts[1] = w.t_up; a.ts[2] = w.t_down;
+    a.tss[0] = w.ts_gate; a.tss[1] = w.ts_up; a.tss[2] = w.ts_down;
+    a.tm_xp = &h->tm_xp;
+    a.tm_h = &h->tm_h;
+    a.x = x;
+    a.y = y;
+    a.gate = gate;
+    a.idx = idx;
+    a.wpb = T > kSmallT ? (h->rtc_capable ? 4 : 1) : 0;
+    a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+    a.add_residual = c.add_residual != 0;
+    a.ws = h->ws;
+    a.wait_ns = h->wait_ns;
+    a.max_units_gu = tc_max_units_gu(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, kTc4BN);
+    a.max_units_dn = tc_max_units_dn(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, kTc4BN);
+    return cuda_status(launch_tc4(a, h->num_sms, s, &h->prof));
+  }
   if (tc) {
     CUtensorMap tm_x;
     bool have_tm_x = false;
@@ -221,8 +283,8 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
     a.add_residual = c.add_residual != 0;
     a.ws = h->ws;
     a.wait_ns = h->wait_ns;
-    a.max_units_gu = tc_max_units_gu(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
-    a.max_units_dn = tc_max_units_dn(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+    a.max_units_gu = tc_max_units_gu(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, kTcBN);
+    a.max_units_dn = tc_max_units_dn(T, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, kTcBN);
     return cuda_status(launch_tc(a, h->num_sms, s, &h->prof));
   }
   const size_t es = act_bytes(c);
@@ -254,6 +316,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
     case MOE_ERR_OOM: return "MOE_ERR_OOM: device allocation failed";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: device-side wait ran out";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE: an intermediate value saturated its format";
   }
   return "MOE_ERR_UNKNOWN";
 }
@@ -281,6 +344,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
   h->tc_capable = tc_shape_ok(c) && cc_major == 10;
+  h->fp4 = c.weight_dtype == MOE_NVFP4;
   h->gemv_capable = gemv_shape_ok(c);
   h->rtc_capable = cc_major == 10 && c.act_dtype == MOE_BF16 && c.num_experts % 64 == 0 && c.d % 64 == 0;
   if ((c.path == MOE_PATH_TC && !h->tc_capable) || (!h->tc_capable && !h->gemv_capable)) {
@@ -294,8 +358,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   const size_t Tg = Tm < (size_t)kGemvChunkT ? Tm : (size_t)kGemvChunkT;
   const size_t nblk = (Tm + 31) / 32;
   if (h->tc_capable) {
-    h->max_units_gu = tc_max_units_gu(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
-    h->max_units_dn = tc_max_units_dn(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k);
+    h->max_units_gu = tc_max_units_gu(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, tile_n_of(c));
+    h->max_units_dn = tc_max_units_dn(c.max_tokens, c.d, c.ffn, c.shared_ffn, c.num_experts, c.top_k, tile_n_of(c));
   }
   struct Part { void** dst; size_t bytes; };
   Workspace& ws = h->ws;
@@ -317,7 +381,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.n_units, 2 * 4},
       {(void**)&ws.h32, Tg * (k + 1) * Fmax * 4},
       {(void**)&ws.h16, (h->tc_capable ? Tm : Tg) * (k + 1) * Fmax * 2},
-      {(void**)&ws.xp, h->tc_capable ? Tm * k * d * 2 : 16},
+      {(void**)&ws.xp, h->tc_capable ? Tm * (h->fp4 ? k + 1 : k) * d * 2 : 16},
+      {(void**)&ws.xs, h->tc_capable && h->fp4 ? Tm * (k + 1) * 4 : 16},
       {(void**)&ws.ypart, Tg * (k + 1) * d * 4},
       {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
       {(void**)&ws.counters, (size_t)(64 + (Tm + 127) / 128) * 4},
@@ -355,7 +420,31 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
     return MOE_ERR_CUDA;
   }
   if (h->rtc_capable && !make_map_bf16(&h->tm_wr, ws.wr_split, 3 * E, d, 64, kTcBK)) h->rtc_capable = false;
-  if (h->tc_capable) {
+  if (h->tc_capable && h->fp4) {
+    const uint64_t F = c.ffn, Fs = c.shared_ffn;
+    const void* qs[3] = {w->w_gate, w->w_up, w->w_down};
+    const void* ss[3] = {w->s_gate, w->s_up, w->s_down};
+    const void* sq[3] = {w->ws_gate, w->ws_up, w->ws_down};
+    const void* sss[3] = {w->ss_gate, w->ss_up, w->ss_down};
+    const uint64_t rows[3] = {E * F, E * F, E * d}, srows[3] = {Fs, Fs, d}, kk[3] = {d, d, F}, skk[3] = {d, d, Fs};
+    bool ok = make_map_f16(&h->tm_xp, ws.xp, Tm * (k + 1), d, 16, 64) &&
+              make_map_f16(&h->tm_h, ws.h16, Tm * (k + 1), Fmax, 16, 64);
+    for (int m = 0; m < 3 && ok; ++m) {
+      ok = make_map_u8(&h->q4[m], qs[m], rows[m], kk[m] / 2, 128, 128, true) &&
+           make_map_u8(&h->sc4[m], ss[m], rows[m], kk[m] / 16, 128, 16, false);
+      if (ok && Fs > 0)
+        ok = make_map_u8(&h->sq4[m], sq[m], srows[m], skk[m] / 2, 128, 128, true) &&
+             make_map_u8(&h->ssc4[m], sss[m], srows[m], skk[m] / 16, 128, 16, false);
+    }
+    if (!ok) {
+      if (c.path == MOE_PATH_TC) {
+        cudaFree(h->block);
+        delete h;
+        return MOE_ERR_CUDA;
+      }
+      h->tc_capable = false;
+    }
+  } else if (h->tc_capable) {
     const uint64_t F = c.ffn, Fs = c.shared_ffn;
     bool ok = make_map_bf16(&h->tm_wg, w->w_gate, E * F, d, kTcBM, kTcBK) &&
               make_map_bf16(&h->tm_wu, w->w_up, E * F, d, kTcBM, kTcBK) &&
@@ -464,6 +553,7 @@ moe_status moe_check(moe_handle h, cudaStream_t stream) {
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kErrRange) return MOE_ERR_RANGE;
   return MOE_OK;
 }
 

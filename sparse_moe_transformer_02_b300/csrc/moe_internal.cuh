@@ -20,7 +20,10 @@ constexpr int kTcBN = 128;           // tcgen05 path: largest token tile (MMA N)
 constexpr int kTcBM = 128;           // tcgen05 path: weight rows per tile (MMA M)
 constexpr int kTcBK = 64;            // tcgen05 path: reduction step per stage (128 bytes of bf16)
 constexpr int kTokMajorT = 512;      // tcgen05 path: T at which the down pass turns token-major
+constexpr int kTc4BN = 64;           // NVFP4 tcgen05 path: largest token tile
+constexpr int kTc4KS = 256;          // NVFP4 tcgen05 path: reduction step per stage (16 scale bytes per row)
 constexpr unsigned kErrTimeout = 1u << 5;
+constexpr unsigned kErrRange = 1u << 6;     // an f16 intermediate saturated (NVFP4 tcgen05 path)
 
 // One unit of tcgen05 work: expert (E = the shared expert), weight-row tile,
 // first slot (for the shared expert: first token) and token count (<= kTcBN).
@@ -47,7 +50,9 @@ struct Workspace {
   int32_t* n_units;       // [2] unit counts (gate/up, down)
   float* h32;             // [min(max_T, kGemvChunkT) * (k + 1)][F_max] GEMV intermediate
   __nv_bfloat16* h16;     // [max(max_T, ...) * (k + 1)][F_max] bf16 intermediate (tcgen05 and bf16 GEMV)
-  __nv_bfloat16* xp;      // [max_T * k][d] tcgen05 slot-ordered copy of the routed activations
+  __nv_bfloat16* xp;      // tcgen05 slot-ordered copy of the activations: bf16 [max_T * k][d], or for
+                          // NVFP4 weights f16 [max_T * (k + 1)][d] (routed slots, then the tokens)
+  float* xs;              // [max_T * (k + 1)] power-of-two scale of each f16 row of xp
   float* ypart;           // [min(max_T, kGemvChunkT) * (k + 1)][d] GEMV down partials
   float* yacc;            // [max_T][d] tcgen05 fp32 accumulator
   uint32_t* counters;     // router tickets: [0] grid, [1 + b] per token chunk / block
@@ -93,6 +98,7 @@ struct RouteArgs {
   Workspace ws;
   int build_tc_units;     // also build tcgen05 unit lists
   int dn_rows;            // Wd rows per down tile (128 weight-major, 256 token-major)
+  int tile_n;             // token tile of the unit lists (kTcBN, or kTc4BN for NVFP4 weights)
   int F, Fs;              // widths (for unit lists)
   int has_shared;
 };
@@ -165,7 +171,36 @@ struct TcArgs {
   int max_units_gu, max_units_dn;
 };
 cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof);
-int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k);
-int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k);
+// Most unit-list entries a call can produce (token tiles of tile_n).
+int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k, int tile_n);
+int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n);
+// y = bf16(y_acc (+ x)) over T x d values.
+cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, int num_sms,
+                               cudaStream_t s, Prof* prof);
+
+// NVFP4 weights on the tensor cores.  Tensor maps over the packed codes
+// (bytes [rows][K / 2], box 128 B x 128 rows, 128-byte swizzle) and the block
+// scales (bytes [rows][K / 16], box 16 B x 128 rows); xp / h rows are f16
+// (box 64 x 16, 128-byte swizzle).
+struct Tc4Args {
+  const CUtensorMap* q[3];      // routed codes: gate, up, down
+  const CUtensorMap* sc[3];     // routed block scales
+  const CUtensorMap* sq[3];     // shared-expert codes
+  const CUtensorMap* ssc[3];    // shared-expert block scales
+  const CUtensorMap* tm_xp;     // f16 activation rows [max_T * (k + 1)][d]
+  const CUtensorMap* tm_h;      // f16 intermediate rows [max_T * (k + 1)][F_max]
+  const float* ts[3];           // routed per-matrix scales [E]
+  const float* tss[3];          // shared per-matrix scales [1]
+  const void* x;
+  void* y;
+  const float* gate;
+  const int32_t* idx;
+  int wpb;                      // > 0: the gather kernel places slots (bitmap words per router block)
+  int T, d, F, Fs, E, k, add_residual;
+  Workspace ws;
+  uint64_t wait_ns;
+  int max_units_gu, max_units_dn;
+};
+cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof);
 
 }  // namespace moe

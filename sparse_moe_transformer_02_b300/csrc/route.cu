@@ -212,26 +212,26 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
   __syncthreads();
   if (!a.build_tc_units) return;
   // tcgen05 units: shared expert first, then routed experts in index order.
-  const int mt_gu = a.F / kTcBM, mt_dn = a.d / a.dn_rows;
-  const int sh_tb = a.has_shared ? (a.T + kTcBN - 1) / kTcBN : 0;
+  const int mt_gu = a.F / kTcBM, mt_dn = a.d / a.dn_rows, tn = a.tile_n;
+  const int sh_tb = a.has_shared ? (a.T + tn - 1) / tn : 0;
   const int sh_mt_gu = a.has_shared ? a.Fs / kTcBM : 0;
   for (int pass = 0; pass < 2; ++pass) {
     const int mt = pass == 0 ? mt_gu : mt_dn;
     const int sh_mt = pass == 0 ? sh_mt_gu : mt_dn;
     TcUnit* out = pass == 0 ? a.ws.units_gu : a.ws.units_dn;
-    for (int e = tid; e < E; e += blockDim.x) scratch[e] = mt * ((cnt[e] + kTcBN - 1) / kTcBN);
+    for (int e = tid; e < E; e += blockDim.x) scratch[e] = mt * ((cnt[e] + tn - 1) / tn);
     __syncthreads();
     const int n_routed = block_exclusive_scan(scratch, E);
     const int sh_units = sh_mt * sh_tb;
     for (int u = tid; u < sh_units; u += blockDim.x) {
       const int tb = u / sh_mt, m = u % sh_mt;
-      out[u] = TcUnit{E, m, tb * kTcBN, min(kTcBN, a.T - tb * kTcBN)};
+      out[u] = TcUnit{E, m, tb * tn, min(tn, a.T - tb * tn)};
     }
     for (int e = tid; e < E; e += blockDim.x) {
       const int c = cnt[e];
       int u = sh_units + scratch[e];
-      for (int tb = 0; tb * kTcBN < c; ++tb)
-        for (int m = 0; m < mt; ++m) out[u++] = TcUnit{e, m, offs[e] + tb * kTcBN, min(kTcBN, c - tb * kTcBN)};
+      for (int tb = 0; tb * tn < c; ++tb)
+        for (int m = 0; m < mt; ++m) out[u++] = TcUnit{e, m, offs[e] + tb * tn, min(tn, c - tb * tn)};
     }
     if (tid == 0) a.ws.n_units[pass] = sh_units + n_routed;
     __syncthreads();

@@ -32,7 +32,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert B.moe_status_string(s).startswith("MOE_")
     assert "UNKNOWN" in B.moe_status_string(99)
 
