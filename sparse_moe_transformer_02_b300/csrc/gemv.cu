@@ -24,9 +24,16 @@
 //    (+ x[t][row]), always in that order, so the result is deterministic.
 //
 // Weight formats: fp32 (with fp32 activations), bf16, and NVFP4 (e2m1 codes,
-// an e4m3 scale per 16 values, an fp32 scale per matrix; decoded in
-// registers; the format is named on the evermx.com review, section
-// "Quantization").
+// an e4m3 scale per 16 values, an fp32 scale per matrix; the format is named
+// on the evermx.com review, section "Quantization").  NVFP4 runs on packed
+// f16 arithmetic: each code pair is decoded exactly by cvt.rn.f16x2.e2m1x2
+// and multiplied into f16 activations with fma.rn.f16x2, one 16-value block at
+// a time (at most 8 products per half, magnitudes below 96), and each block
+// sum is widened to fp32 and scaled by its e4m3 scale.  The activations are a
+// per-token f16 copy scaled by a power of two (largest value into [1, 2),
+// made by gemv_x16_kernel), the intermediate is stored in f16 as h / xs^2,
+// and the exact power-of-two factors are applied to the fp32 results; an h
+// beyond the f16 range saturates and sets the range bit of the error word.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -53,13 +60,6 @@ template <> struct Fmt<MOE_NVFP4> { static constexpr int EPC = 32; static conste
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
-// Two e2m1 codes (one byte, element 2i in the low nibble) -> two floats.
-__device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t byte) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
-}
 // Two e4m3 codes (low byte first) -> two floats.
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
   uint32_t h2;
@@ -86,36 +86,48 @@ __device__ __forceinline__ float cdot(const uint4& w, const XChunk<MOE_F32>& x, 
   s = fmaf(__uint_as_float(w.z), __uint_as_float(a.z), s);
   return fmaf(__uint_as_float(w.w), __uint_as_float(a.w), s);
 }
-__device__ __forceinline__ float cdot(const uint4& w, const XChunk<MOE_NVFP4>& x, float2 sc) {
+// NVFP4: 32 codes (two 16-value blocks; sc2 = their scales as f16x2) against
+// 32 f16 values (16 f16x2 words; word m holds values 2m, 2m + 1).
+__device__ __forceinline__ float cdot4(const uint4& w, const XChunk<MOE_NVFP4>& x, uint32_t sc2) {
+  const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&sc2));
   const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-  float blk[2];
+  const uint32_t xv[16] = {x.v[0].x, x.v[0].y, x.v[0].z, x.v[0].w, x.v[1].x, x.v[1].y, x.v[1].z, x.v[1].w,
+                           x.v[2].x, x.v[2].y, x.v[2].z, x.v[2].w, x.v[3].x, x.v[3].y, x.v[3].z, x.v[3].w};
+  float r = 0.f;
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
-    float s = 0.f;
+    uint32_t acc = 0u;                       // f16x2 zero
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint4 xv = x.v[b * 2 + q];
-      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-      const uint32_t cw = wv[b * 2 + q];
+      uint32_t hq[4];
+      e2m1x8_f16x2(wv[2 * b + q], hq);       // codes 8 (2b + q) + 2c, + 1
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 wf = e2m1x2_to_f2((cw >> (8 * i)) & 0xFFu);
-        s = fmaf(wf.x, bf_lo(xs[i]), s);
-        s = fmaf(wf.y, bf_hi(xs[i]), s);
-      }
+      for (int c = 0; c < 4; ++c) acc = hfma2(hq[c], xv[8 * b + 4 * q + c], acc);
     }
-    blk[b] = s;
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&acc));
+    r = fmaf(f.x + f.y, b == 0 ? sc.x : sc.y, r);
   }
-  return fmaf(blk[0], sc.x, blk[1] * sc.y);
+  return r;
 }
 
-// Activations of a chunk taken from the fp32 intermediate h.
+// Activations of a chunk taken from the fp32 intermediate h (NVFP4: f16 h / xs^2).
 template <int WF> struct HChunk { float4 v[Fmt<WF>::EPC / 4]; };
+template <> struct HChunk<MOE_NVFP4> { XChunk<MOE_NVFP4> c; };
 
 template <int WF>
 __device__ __forceinline__ void load_h(HChunk<WF>& c, const float* p) {
 #pragma unroll
-  for (int i = 0; i < Fmt<WF>::EPC / 4; ++i) c.v[i] = __ldg(reinterpret_cast<const float4*>(p) + i);
+  for (int i = 0; i < Fmt<WF>::EPC / 4; ++i) c.v[i] = __ldcg(reinterpret_cast<const float4*>(p) + i);
+}
+__device__ __forceinline__ void load_h16(HChunk<MOE_NVFP4>& h, const __half* p) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h.c.v[i] = __ldcg(reinterpret_cast<const uint4*>(p) + i);
+}
+// Two e4m3 codes (low byte first) -> f16x2.  Exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two));
+  return h2;
 }
 __device__ __forceinline__ float hdot(const uint4& w, const HChunk<MOE_F32>& h, float2) {
   const float4 a = h.v[0];
@@ -124,29 +136,6 @@ __device__ __forceinline__ float hdot(const uint4& w, const HChunk<MOE_F32>& h, 
   s = fmaf(__uint_as_float(w.z), a.z, s);
   return fmaf(__uint_as_float(w.w), a.w, s);
 }
-__device__ __forceinline__ float hdot(const uint4& w, const HChunk<MOE_NVFP4>& h, float2 sc) {
-  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-  float blk[2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float4 h0 = h.v[b * 4 + q * 2], h1 = h.v[b * 4 + q * 2 + 1];
-      const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      const uint32_t cw = wv[b * 2 + q];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 wf = e2m1x2_to_f2((cw >> (8 * i)) & 0xFFu);
-        s = fmaf(wf.x, hv[2 * i], s);
-        s = fmaf(wf.y, hv[2 * i + 1], s);
-      }
-    }
-    blk[b] = s;
-  }
-  return fmaf(blk[0], sc.x, blk[1] * sc.y);
-}
-
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
 template <int WF>
@@ -158,6 +147,64 @@ __host__ __device__ __forceinline__ int row_bytes(int cols) {
 __device__ __forceinline__ void share(int n, int b, int g, int& lo, int& hi) {
   lo = (int)(((long long)n * b) / g);
   hi = (int)(((long long)n * (b + 1)) / g);
+}
+
+// Units of the templated GEMV kernels, in one sequence: the shared expert's
+// (if any), then each active routed expert's, upe units per expert.  A unit's
+// cost is 1 + the tokens its expert serves (one weight stream, then one
+// pass per token), and each CTA takes a contiguous run of units holding an
+// equal share of the total cost, so a CTA whose run falls on a popular expert
+// gets fewer units.  Warp-collective (one warp); *lo, *hi = the CTA's run.
+__device__ void unit_range(const GemvArgs& a, int upe, int b, int G, int* lo, int* hi) {
+  const int lane = threadIdx.x & 31;
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int n_seq = has_sh + a.ws.active[a.E];
+  // this lane's experts s = lane * per .. lane * per + per - 1 (per <= 17 covers E + 1 <= 513)
+  const int per = (n_seq + 31) / 32;
+  int c[17];
+  int run = 0;
+#pragma unroll
+  for (int i = 0; i < 17; ++i) {
+    const int sq = lane * per + i;
+    int v = 0;
+    if (i < per && sq < n_seq)
+      v = 1 + (sq < has_sh ? a.T : __ldcg(a.ws.counts + __ldcg(a.ws.active + sq - has_sh)));
+    c[i] = v;
+    run += v;
+  }
+  // exclusive scan of the lane totals
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const long long total = (long long)__shfl_sync(0xFFFFFFFFu, incl, 31) * upe;
+  const long long excl = (long long)(incl - run) * upe;
+  int res[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const long long X = total * (b + w) / G;         // cost at which the run starts / ends
+    int g = n_seq * upe;                             // X == total: the end
+    long long st = excl;
+    int found = -1;
+#pragma unroll
+    for (int i = 0; i < 17; ++i) {
+      const long long len = (long long)c[i] * upe;
+      if (found < 0 && c[i] > 0 && X >= st && X < st + len) {
+        const long long j = (X - st + c[i] - 1) / c[i];     // first unit starting at or after X
+        found = (lane * per + i) * upe + (int)j;
+      }
+      st += len;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, found >= 0);
+    if (m) g = __shfl_sync(0xFFFFFFFFu, found, __ffs(m) - 1);
+    res[w] = g;
+  }
+  if (lane == 0) {
+    *lo = res[0];
+    *hi = res[1];
+  }
 }
 
 // Ring bookkeeping common to both kernels.
@@ -254,9 +301,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
   const int d = a.d, G = gridDim.x, b = blockIdx.x;
   const int rb = row_bytes<WF>(d);                  // bytes of one row
   const int sb = WF == MOE_NVFP4 ? d / 16 : 0;      // scale bytes of one row
-  const int n_sh = a.Fs / RG;                       // shared-expert units
-  const int upe = a.F / RG;                         // units per routed expert
-  const int n_sh_local = b < n_sh ? (n_sh - b + G - 1) / G : 0;
+  const int upe = a.F / RG;                         // units per expert (the shared expert has the routed width)
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  pdl_wait();
+  __shared__ int s_run[2];
+  if (warp == 0) unit_range(a, upe, b, G, &s_run[0], &s_run[1]);
+  __syncthreads();
+  const int g_lo = s_run[0], n_local = s_run[1] - s_run[0];
+  // local unit i -> (shared?, expert, first row pair)
+  auto unit_of = [&](int i, bool& shared, int& e, int& f0) {
+    const int g = g_lo + i, sq = g / upe;
+    shared = sq < has_sh;
+    e = shared ? 0 : a.ws.active[sq - has_sh];
+    f0 = (g % upe) * RG;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -264,24 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
     const uint64_t pol = policy_evict_first();
     int i = 0;
     bool ok = true;
-    int r_lo = 0, r_hi = 0;
-    for (;; ++i) {
+    for (; i < n_local; ++i) {
       bool shared;
-      int e = 0, f0;
-      if (i < n_sh_local) {
-        shared = true;
-        f0 = (b + i * G) * RG;
-      } else {
-        if (i == n_sh_local) {
-          pdl_wait();
-          share(a.ws.active[a.E] * upe, b, G, r_lo, r_hi);
-        }
-        const int u = r_lo + (i - n_sh_local);
-        if (u >= r_hi) break;
-        shared = false;
-        e = a.ws.active[u / upe];
-        f0 = (u % upe) * RG;
-      }
+      int e, f0;
+      unit_of(i, shared, e, f0);
       const int s = i % kStages;
       if (!mbar_wait(&ring.empty[s], ((i / kStages) & 1) ^ 1, wc)) { ok = false; break; }
       uint8_t* st = ring.stages + s * kStageBytes;
@@ -310,45 +354,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
   // ---------------------------------------------------------------- consumers
   const int cw = warp - 1;
   const int Fmax = max(a.F, a.Fs);
-  int r_lo = 0, r_hi = 0;
-  bool have_range = false;
-  for (int i = cw;; i += kConsumers) {
+  bool range_bad = false;
+  for (int i = cw; i < n_local; i += kConsumers) {
     bool shared;
-    int e = 0, f0;
-    if (i < n_sh_local) {
-      shared = true;
-      f0 = (b + i * G) * RG;
-    } else {
-      if (!have_range) {
-        pdl_wait();
-        share(a.ws.active[a.E] * upe, b, G, r_lo, r_hi);
-        have_range = true;
-      }
-      const int u = r_lo + (i - n_sh_local);
-      if (u >= r_hi) break;
-      shared = false;
-      e = a.ws.active[u / upe];
-      f0 = (u % upe) * RG;
-    }
+    int e, f0;
+    unit_of(i, shared, e, f0);
     const int s = i % kStages;
     if (!warp_wait_full(&ring.full[s], (i / kStages) & 1, wc)) break;
     const uint8_t* st = ring.stages + s * kStageBytes;
-    // bf16 / fp32: the unit's weights move to registers and the stage is freed
-    // at once.  NVFP4: they are read from the stage at each use (the decoded
-    // form would not fit in registers) and the stage is freed after the tokens.
-    constexpr bool HOLD = WF != MOE_NVFP4;
-    uint4 wg[HOLD ? RG : 1][J], wu[HOLD ? RG : 1][J];
-    if constexpr (HOLD) {
+    // The unit's weights (and NVFP4 block scales, as f16x2) move to registers
+    // and the stage is freed at once, so the producer refills it while the
+    // tokens are computed.
+    constexpr bool FP4 = WF == MOE_NVFP4;
+    uint4 wg[RG][J], wu[RG][J];
+    uint32_t sg[FP4 ? RG : 1][J], su[FP4 ? RG : 1][J];
 #pragma unroll
-      for (int p = 0; p < RG; ++p)
+    for (int p = 0; p < RG; ++p)
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-          wg[p][j] = reinterpret_cast<const uint4*>(st + p * rb)[j * 32 + lane];
-          wu[p][j] = reinterpret_cast<const uint4*>(st + (RG + p) * rb)[j * 32 + lane];
+      for (int j = 0; j < J; ++j) {
+        wg[p][j] = reinterpret_cast<const uint4*>(st + p * rb)[j * 32 + lane];
+        wu[p][j] = reinterpret_cast<const uint4*>(st + (RG + p) * rb)[j * 32 + lane];
+        if constexpr (FP4) {
+          const int c = j * 32 + lane;
+          sg[p][j] = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + p * sb + c * 2));
+          su[p][j] = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + (RG + p) * sb + c * 2));
         }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
-    }
+      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[s]);
     float tg = 1.f, tu = 1.f;
     if (WF == MOE_NVFP4) {
       tg = shared ? a.tss_g[0] : a.ts_g[e];
@@ -359,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
     for (int q = 0; q < n; ++q) {
       const int t = shared ? q : a.ws.tok_of_slot[off + q];
       const int slot = shared ? a.T * a.k + q : off + q;
-      const uint8_t* xt = static_cast<const uint8_t*>(a.x) + (size_t)t * d * (WF == MOE_F32 ? 4 : 2);
+      const uint8_t* xt = WF == MOE_NVFP4 ? reinterpret_cast<const uint8_t*>(a.ws.xh16 + (size_t)t * d)
+                                          : static_cast<const uint8_t*>(a.x) + (size_t)t * d * (WF == MOE_F32 ? 4 : 2);
       XChunk<WF> xc[J];
 #pragma unroll
       for (int j = 0; j < J; ++j) load_x<WF>(xc[j], xt + (size_t)(j * 32 + lane) * Fmt<WF>::XB);
@@ -369,16 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
         float ag = 0.f, au = 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-          if constexpr (HOLD) {
+          if constexpr (FP4) {
+            ag += cdot4(wg[p][j], xc[j], sg[p][j]);
+            au += cdot4(wu[p][j], xc[j], su[p][j]);
+          } else {
             ag += cdot(wg[p][j], xc[j], make_float2(0.f, 0.f));
             au += cdot(wu[p][j], xc[j], make_float2(0.f, 0.f));
-          } else {
-            const int c = j * 32 + lane;
-            const float2 sg = e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + p * sb + c * 2));
-            const float2 su =
-                e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + 2 * RG * rb + (RG + p) * sb + c * 2));
-            ag += cdot(reinterpret_cast<const uint4*>(st + p * rb)[c], xc[j], sg);
-            au += cdot(reinterpret_cast<const uint4*>(st + (RG + p) * rb)[c], xc[j], su);
           }
         }
         v[2 * p] = ag * tg;
@@ -389,14 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_gateup_kernel(GemvArgs a, ui
       constexpr int SH = (2 * RG == 2) ? 4 : (2 * RG == 4) ? 3 : (2 * RG == 8) ? 2 : 1;
       const float up = __shfl_down_sync(FULLMASK, r, 1 << SH);
       const int idx = lane >> SH;
-      if ((lane & ((1 << SH) - 1)) == 0 && (idx & 1) == 0)
-        a.ws.h32[(size_t)slot * Fmax + f0 + (idx >> 1)] = silu(r) * up;
-    }
-    if constexpr (!HOLD) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
+      if ((lane & ((1 << SH) - 1)) == 0 && (idx & 1) == 0) {
+        if constexpr (WF == MOE_NVFP4) {
+          // r, up are the products with the scaled copy x / xs: store h / xs^2
+          const float xs = __ldcg(a.ws.xsc + t);
+          const float hv = silu(r * xs) * up * (1.f / xs);
+          range_bad |= !(fabsf(hv) <= 65504.f);
+          reinterpret_cast<__half*>(a.ws.h16)[(size_t)slot * Fmax + f0 + (idx >> 1)] = __float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f));
+        } else {
+          a.ws.h32[(size_t)slot * Fmax + f0 + (idx >> 1)] = silu(r) * up;
+        }
+      }
     }
   }
+  if (WF == MOE_NVFP4 && __any_sync(FULLMASK, range_bad) && lane == 0) atomicOr(a.ws.err, kErrRange);
 }
 
 // ------------------------------------------------------------------ down + combine
@@ -422,26 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint
   const int upe = d / RD;                            // units per expert
   const int has_sh = a.Fs > 0 ? 1 : 0;
   pdl_wait();
-  // The shared expert's units (every token) are the heaviest: deal them
-  // round-robin over the CTAs; the routed ones follow in contiguous shares.
-  const int n_act = a.ws.active[a.E];
-  const int n_sh = has_sh ? upe : 0;
-  const int n_sh_local = b < n_sh ? (n_sh - b + G - 1) / G : 0;
-  int r_lo, r_hi;
-  share(n_act * upe, b, G, r_lo, r_hi);
-  const int n_local = n_sh_local + (r_hi - r_lo);
+  __shared__ int s_run[2];
+  if (warp == 0) unit_range(a, upe, b, G, &s_run[0], &s_run[1]);
+  __syncthreads();
+  const int g_lo = s_run[0], n_local = s_run[1] - s_run[0];
   // local unit i -> (shared?, expert, first row)
   auto unit_of = [&](int i, bool& shared, int& e, int& r0) {
-    if (i < n_sh_local) {
-      shared = true;
-      e = 0;
-      r0 = (b + i * G) * RD;
-    } else {
-      const int u = r_lo + (i - n_sh_local);
-      shared = false;
-      e = a.ws.active[u / upe];
-      r0 = (u % upe) * RD;
-    }
+    const int g = g_lo + i, sq = g / upe;
+    shared = sq < has_sh;
+    e = shared ? 0 : a.ws.active[sq - has_sh];
+    r0 = (g % upe) * RD;
   };
 
   if (warp == 0) {
@@ -484,42 +510,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint
     const int s = i % kStages;
     if (!warp_wait_full(&ring.full[s], (i / kStages) & 1, wc)) break;
     const uint8_t* st = ring.stages + s * kStageBytes;
-    constexpr bool HOLD = WF != MOE_NVFP4;     // as in gemv_gateup
-    uint4 w[HOLD ? NR : 1][JD];
-    if constexpr (HOLD) {
+    constexpr bool FP4 = WF == MOE_NVFP4;      // as in gemv_gateup: weights to registers, stage freed
+    uint4 w[NR][JD];
+    uint32_t sc[FP4 ? NR : 1][JD];
 #pragma unroll
-      for (int r = 0; r < NR; ++r)
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int j = 0; j < JD; ++j)
-          w[r][j] = reinterpret_cast<const uint4*>(st + (SPLIT ? row_lane + 2 * r : r) * rb)[j * 32 + col_lane];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
-    }
+      for (int j = 0; j < JD; ++j) {
+        const int row = SPLIT ? row_lane + 2 * r : r;
+        w[r][j] = reinterpret_cast<const uint4*>(st + row * rb)[j * 32 + col_lane];
+        if constexpr (FP4)
+          sc[r][j] = e4m3x2_to_h2(*reinterpret_cast<const unsigned short*>(st + RD * rb + row * sb + (j * 32 + col_lane) * 2));
+      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[s]);
     const float ts = WF == MOE_NVFP4 ? (shared ? a.tss_d[0] : a.ts_d[e]) : 1.f;
     const int n = shared ? a.T : a.ws.counts[e];
     const int off = shared ? 0 : a.ws.offsets[e];
     for (int q = 0; q < n; ++q) {
       const int slot = shared ? a.T * a.k + q : off + q;
-      const float* h = a.ws.h32 + (size_t)slot * Fmax;
       HChunk<WF> hc[JD];
+      float xs2 = 1.f;
+      if constexpr (WF == MOE_NVFP4) {
+        const int t = shared ? q : a.ws.tok_of_slot[off + q];
+        const float xs = __ldcg(a.ws.xsc + t);
+        xs2 = xs * xs;
+        const __half* h = reinterpret_cast<const __half*>(a.ws.h16) + (size_t)slot * Fmax;
 #pragma unroll
-      for (int j = 0; j < JD; ++j) load_h<WF>(hc[j], h + (j * 32 + col_lane) * EPC);
+        for (int j = 0; j < JD; ++j) load_h16(hc[j], h + (j * 32 + col_lane) * EPC);
+      } else {
+        const float* h = a.ws.h32 + (size_t)slot * Fmax;
+#pragma unroll
+        for (int j = 0; j < JD; ++j) load_h<WF>(hc[j], h + (j * 32 + col_lane) * EPC);
+      }
       float v[NR];
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         float acc = 0.f;
-        const int row = SPLIT ? row_lane + 2 * r : r;
 #pragma unroll
         for (int j = 0; j < JD; ++j) {
-          const int c = j * 32 + col_lane;
-          if constexpr (HOLD) {
+          if constexpr (FP4)
+            acc += cdot4(w[r][j], hc[j].c, sc[r][j]);
+          else
             acc += hdot(w[r][j], hc[j], make_float2(0.f, 0.f));
-          } else {
-            const float2 sc = e4m3x2_to_f2(*reinterpret_cast<const unsigned short*>(st + RD * rb + row * sb + c * 2));
-            acc += hdot(reinterpret_cast<const uint4*>(st + row * rb)[c], hc[j], sc);
-          }
         }
-        v[r] = acc * ts;
+        v[r] = acc * ts * xs2;
       }
       const float tot = transpose_reduce<NR, LW>(v, lane);
       constexpr int SH = (LW == 32) ? (NR == 4 ? 3 : NR == 8 ? 2 : NR == 16 ? 1 : 0) : (NR == 16 ? 0 : 1);
@@ -528,10 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_down_kernel(GemvArgs a, uint
         const int row = SPLIT ? row_lane + 2 * li : li;
         a.ws.ypart[(size_t)slot * d + r0 + row] = tot;
       }
-    }
-    if constexpr (!HOLD) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[s]);
     }
     // Units never straddle a 32-row block: each of a token's experts
     // contributes 32 / RD units to it.
@@ -888,6 +919,48 @@ cudaError_t launch_mma(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* pro
   return e;
 }
 
+// f16 copy of the activations for the NVFP4 kernels: token t scaled by 2^-e
+// (its largest magnitude into [1, 2)), xsc[t] = 2^e.  One warp per token.
+// Needs only x, so it runs alongside the router; it waits for the router at
+// the end so that a kernel waiting on this one also sees the routing.
+__global__ void __launch_bounds__(256) gemv_x16_kernel(const __nv_bfloat16* __restrict__ x, __half* __restrict__ xh,
+                                                       float* __restrict__ xsc, int T, int d) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t < T) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const int n16 = d / 8;
+    uint32_t mx = 0;                               // largest |x| as bits (monotone for |x|)
+    for (int c = lane; c < n16; c += 32) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx = max(mx, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+    }
+    mx = __reduce_max_sync(FULLMASK, mx);
+    // 2^-e with e the exponent of the maximum (normal maxima only; a zero,
+    // subnormal, infinite or NaN maximum leaves the token unscaled)
+    const int eb = (int)(mx >> 23);
+    const bool scaled = eb >= 2 && eb <= 252;
+    const float inv = scaled ? __int_as_float((254 - eb) << 23) : 1.f;
+    if (lane == 0) xsc[t] = scaled ? __int_as_float(eb << 23) : 1.f;
+    uint4* dst = reinterpret_cast<uint4*>(xh + (size_t)t * d);
+    for (int c = lane; c < n16; c += 32) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xFFFF0000u) * inv);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  pdl_wait();
+}
+
 template <int WF, int J, int CPR>
 cudaError_t launch_fmt(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
   static bool attr_set = false;   // set once, before any stream capture
@@ -899,8 +972,23 @@ cudaError_t launch_fmt(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* pro
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  cudaError_t e = cudaSuccess;
+  if (WF == MOE_NVFP4) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.T + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemv_x16_kernel, static_cast<const __nv_bfloat16*>(a.x), a.ws.xh16, a.ws.xsc, a.T,
+                           a.d);
+    if (e != cudaSuccess) return e;
+  }
   if (prof) prof->begin(MOE_K_GEMV_GATEUP, s);
-  cudaError_t e = launch_pdl(gemv_gateup_kernel<WF, J>, num_sms, s, a, wait_ns);
+  e = launch_pdl(gemv_gateup_kernel<WF, J>, num_sms, s, a, wait_ns);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   if (prof) prof->begin(MOE_K_GEMV_DOWN, s);

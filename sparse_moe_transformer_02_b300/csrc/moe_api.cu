@@ -384,6 +384,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.xp, h->tc_capable ? Tm * (h->fp4 ? k + 1 : k) * d * 2 : 16},
       {(void**)&ws.xs, h->tc_capable && h->fp4 ? Tm * (k + 1) * 4 : 16},
       {(void**)&ws.ypart, Tg * (k + 1) * d * 4},
+      {(void**)&ws.xh16, c.weight_dtype == MOE_NVFP4 ? Tg * d * 2 : 16},
+      {(void**)&ws.xsc, c.weight_dtype == MOE_NVFP4 ? Tg * 4 : 16},
       {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
       {(void**)&ws.counters, (size_t)(64 + (Tm + 127) / 128) * 4},
       {(void**)&ws.wr_split, h->rtc_capable ? 3 * E * d * 2 : 16},

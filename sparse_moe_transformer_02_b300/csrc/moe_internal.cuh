@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -54,6 +55,8 @@ struct Workspace {
                           // NVFP4 weights f16 [max_T * (k + 1)][d] (routed slots, then the tokens)
   float* xs;              // [max_T * (k + 1)] power-of-two scale of each f16 row of xp
   float* ypart;           // [min(max_T, kGemvChunkT) * (k + 1)][d] GEMV down partials
+  __half* xh16;           // [min(max_T, kGemvChunkT)][d] NVFP4 GEMV: f16 activations, scaled per token
+  float* xsc;             // [min(max_T, kGemvChunkT)] their power-of-two scales
   float* yacc;            // [max_T][d] tcgen05 fp32 accumulator
   uint32_t* counters;     // router tickets: [0] grid, [1 + b] per token chunk / block
   __nv_bfloat16* wr_split;  // [3][E][d] router weights as bf16 hi, mid, lo (tensor-core router)

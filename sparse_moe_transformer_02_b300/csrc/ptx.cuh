@@ -287,6 +287,11 @@ __device__ __forceinline__ void e4m3x4_f16x2(uint32_t w, uint32_t& lo, uint32_t&
       : "=r"(lo), "=r"(hi)
       : "r"(w));
 }
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
