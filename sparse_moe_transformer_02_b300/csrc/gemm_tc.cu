@@ -21,7 +21,9 @@
 //  * pass 2 for large batches (token-major): A = h of 128 slots, B = 256 rows
 //    of Wd, D[slot][row]; each epilogue thread owns one slot, so it looks up
 //    one (token, gate) pair per tile and adds 16 consecutive outputs with four
-//    red.global.add.v4.f32 (a quarter of the atomic requests of pass 2).
+//    red.global.add.v4.f32; from 8192 tokens on, where the rate of those
+//    operations bounds the pass, it stages 64 gated outputs in shared memory
+//    and adds them with one bulk reduction (cp.reduce.async.bulk) instead.
 //  * finalise: y = bf16(y_acc (+ x)).
 //
 // One persistent CTA per SM, 6 warps: warp 0 issues TMA into a ring of
@@ -39,6 +41,12 @@ namespace {
 constexpr int kThreadsTc = 192;
 
 template <int MODE> struct TcCfg;
+constexpr int kRedCols = 64;     // token-major down pass: columns per bulk reduction (256 bytes)
+constexpr int kBulkRedT = 8192;  // batches from which 16-byte red operations bound the token-major pass
+
+template <int MODE> struct TcStaging { static constexpr int BYTES = 0; };
+template <> struct TcStaging<3> { static constexpr int BYTES = 2 * 128 * kRedCols * 4; };   // two row buffers
+
 template <> struct TcCfg<0> {     // gate/up: A_g + A_u + B per stage
   static constexpr int STAGES = 4;
   static constexpr int STAGE_BYTES = 2 * kTcBM * 128 + kTcBN * 128;
@@ -51,11 +59,14 @@ template <> struct TcCfg<1> {     // down, weight-major: A (128 Wd rows) + B (h 
   static constexpr int ACC_COLS = kTcBN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
 };
-template <> struct TcCfg<2> {     // down, token-major: A (h of 128 slots) + B (256 Wd rows)
+template <> struct TcCfg<2> {     // down, token-major: A (h of 128 slots) + B (256 Wd rows); red.v4 epilogue
   static constexpr int STAGES = 4;
   static constexpr int STAGE_BYTES = kTcBM * 128 + 2 * kTcBN * 128;
   static constexpr int ACC_COLS = 2 * kTcBN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
+};
+template <> struct TcCfg<3> : TcCfg<2> {   // the same with a bulk-reduction epilogue (largest batches)
+  static constexpr int STAGES = 3;
 };
 
 struct TcParams {
@@ -93,7 +104,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = dsm;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + S * C::STAGE_BYTES);
+  float* red_stage = reinterpret_cast<float*>(dsm + S * C::STAGE_BYTES);   // [2][128][kRedCols] (MODE 3)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + S * C::STAGE_BYTES + TcStaging<MODE>::BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -160,7 +172,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       const TcUnit un = get_unit(p, u);
       const bool sh = un.expert == p.E;
       const int K = sh ? p.Ks : p.K;
-      const int wrows = MODE == 2 ? 2 * kTcBN : kTcBM;          // weight rows per tile
+      const int wrows = MODE >= 2 ? 2 * kTcBN : kTcBM;          // weight rows per tile
       const int arow = sh ? un.m_tile * wrows : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * wrows;
       const CUtensorMap* ma0 = sh ? &p.tm_sa0 : &p.tm_a0;
       const CUtensorMap* ma1 = sh ? &p.tm_sa1 : &p.tm_a1;
@@ -174,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           mbar_arrive_expect_tx(&full[stage], bytes);
           // weights are streamed once: evict them first so that the activations,
           // h and the fp32 accumulator stay in L2
-          if (MODE == 2) {
+          if (MODE >= 2) {
             tma_load_2d(st, mb, k0, brow, &full[stage]);                          // h: 128 slots
             tma_load_2d_hint(st + kTcBM * 128, ma0, k0, arow, &full[stage], pol);  // Wd: 256 rows
           } else {
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         const bool sh = un.expert == p.E;
         const int n_pad = (un.n + 15) & ~15;
         const int K = sh ? p.Ks : p.K;
-        const uint32_t idesc = MODE == 2 ? idesc_bf16_f32(kTcBM, 2 * kTcBN) : idesc_bf16_f32(kTcBM, n_pad);
+        const uint32_t idesc = MODE >= 2 ? idesc_bf16_f32(kTcBM, 2 * kTcBN) : idesc_bf16_f32(kTcBM, n_pad);
         if (!mbar_wait(&tempty[buf], tph[buf] ^ 1, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::ACC_COLS;
@@ -233,7 +245,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
               const uint64_t bd = sdesc_sw128(st + 2 * kTcBM * 128 + kk * 32);
               tc_mma_f16(acc, sdesc_sw128(st + kk * 32), bd, idesc, accum);
               tc_mma_f16(acc + kTcBN, sdesc_sw128(st + kTcBM * 128 + kk * 32), bd, idesc, accum);
-            } else {   // MODE 1: A = Wd rows, B = h; MODE 2: A = h, B = Wd rows
+            } else {   // MODE 1: A = Wd rows, B = h; MODES 2, 3: A = h, B = Wd rows
               tc_mma_f16(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + kTcBM * 128 + kk * 32), idesc, accum);
             }
           }
@@ -263,6 +275,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     }
     uint32_t tph[2] = {0, 0};
     int buf = 0;
+    int red_buf = 0;
     int n_total = p.n_pre;
     bool waited = MODE >= 1;
     if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
@@ -297,7 +310,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         }
         __syncwarp();
       }
-      if (MODE == 2) {
+      if (MODE >= 2) {
         // this thread's slot (row of the tile): token and gate, once per tile
         const int r = q * 32 + lane;
         int t = 0;
@@ -316,16 +329,51 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
         float* yrow = p.yacc + (size_t)t * p.d + un.m_tile * (2 * kTcBN);
+        if constexpr (MODE == 2) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < 2 * kTcBN; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(acc + c0, v);
-          tmem_ld_wait();
-          if (r < un.n) {
+          for (int c0 = 0; c0 < 2 * kTcBN; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(acc + c0, v);
+            tmem_ld_wait();
+            if (r < un.n) {
 #pragma unroll
-            for (int i = 0; i < 16; i += 4)
-              red_add_v4_f32(yrow + c0 + i, g * __uint_as_float(v[i]), g * __uint_as_float(v[i + 1]),
-                             g * __uint_as_float(v[i + 2]), g * __uint_as_float(v[i + 3]));
+              for (int i = 0; i < 16; i += 4)
+                red_add_v4_f32(yrow + c0 + i, g * __uint_as_float(v[i]), g * __uint_as_float(v[i + 1]),
+                               g * __uint_as_float(v[i + 2]), g * __uint_as_float(v[i + 3]));
+            }
+          }
+        } else {
+          // Accumulate into y_acc with bulk reductions (one 256-byte row segment
+          // per operation, added at L2 by the copy engine) rather than 16-byte
+          // red operations, whose rate bounds this pass at prefill sizes.  Each
+          // thread stages its own row in one of two buffers, storing its 16-byte
+          // pieces in a rotated order so that a quarter-warp hits distinct banks.
+#pragma unroll 1
+          for (int c0 = 0; c0 < 2 * kTcBN; c0 += kRedCols) {
+            float* rs = red_stage + (size_t)(red_buf * 128 + r) * kRedCols;
+            if (r < un.n) bulk_wait_read<1>();        // this buffer's previous reduction has read it
+#pragma unroll
+            for (int h = 0; h < kRedCols; h += 16) {
+              uint32_t v[16];
+              tmem_ld16(acc + c0 + h, v);
+              tmem_ld_wait();
+              if (r < un.n) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int pc = (h / 4 + ((i + r) & 3));      // 16-byte piece, rotated within the 64-byte group
+                  const int j = (pc - h / 4) * 4;
+                  reinterpret_cast<float4*>(rs)[pc] =
+                      make_float4(g * __uint_as_float(v[j]), g * __uint_as_float(v[j + 1]),
+                                  g * __uint_as_float(v[j + 2]), g * __uint_as_float(v[j + 3]));
+                }
+              }
+            }
+            if (r < un.n) {
+              fence_proxy_async_smem();
+              bulk_red_add_f32(yrow + c0, smem_u32(rs), kRedCols * 4);
+              bulk_commit();
+            }
+            red_buf ^= 1;
           }
         }
         tc_fence_before();
@@ -372,6 +420,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       tph[buf] ^= 1;
       buf ^= 1;
     }
+    if (MODE == 3) bulk_wait_all();          // every reduction performed before the CTA ends
   }
   tc_fence_before();
   __syncthreads();
@@ -446,7 +495,7 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restric
 template <int MODE>
 size_t tc_smem_bytes() {
   using C = TcCfg<MODE>;
-  return 1024 + C::STAGES * C::STAGE_BYTES + (2 * C::STAGES + 4) * 8 + 16 + 8 * kTcBN * 4;
+  return 1024 + C::STAGES * C::STAGE_BYTES + TcStaging<MODE>::BYTES + (2 * C::STAGES + 4) * 8 + 16 + 8 * kTcBN * 4;
 }
 
 template <typename... KArgs, typename... Args>
@@ -501,6 +550,8 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
       e = cudaFuncSetAttribute(tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<1>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<2>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<3>());
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -554,7 +605,8 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
   if (prof) prof->begin(MOE_K_TC_DOWN, s);
   if (tok_major)
-    e = launch_ex(tc_kernel<2>, grid2, kThreadsTc, tc_smem_bytes<2>(), s, p);
+    e = a.T >= kBulkRedT ? launch_ex(tc_kernel<3>, grid2, kThreadsTc, tc_smem_bytes<3>(), s, p)
+                         : launch_ex(tc_kernel<2>, grid2, kThreadsTc, tc_smem_bytes<2>(), s, p);
   else
     e = launch_ex(tc_kernel<1>, grid2, kThreadsTc, tc_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);

@@ -302,6 +302,22 @@ __device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0
 __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0, 0x3232); }
 
 // ---------------------------------------------------------------- reductions
+// Bulk reduction shared -> global: dst[i] += src[i] over `bytes` (a multiple
+// of 16, both addresses 16-byte aligned), performed at L2 by the copy engine.
+// The issuing thread must have made its writes to src visible to the async
+// proxy (fence_proxy_async_smem) first.
+__device__ __forceinline__ void bulk_red_add_f32(float* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Returns once at most N of this thread's bulk groups still have to read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+// Returns once all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }

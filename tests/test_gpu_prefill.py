@@ -151,3 +151,13 @@ def test_token_major_no_shared_and_narrow_d(spec):
     x = I.make_tokens(spec, seed=3, T=700)
     _, y, idx, gate = run(spec, dev, x, 700, path=B.MOE_PATH_TC)
     check_layer(L, x, y, idx, gate, spec.top_k, "bf16")
+
+
+def test_token_major_bulk_reduction(small):
+    """From 8192 tokens on the token-major down pass adds its results with bulk
+    reductions from shared memory; every token against the oracle."""
+    L, dev = small
+    T = 8192
+    x = I.make_tokens(SMALL, seed=8192, T=T)
+    _, y, idx, gate = run(SMALL, dev, x, T, path=B.MOE_PATH_TC)
+    check_layer(L, x, y, idx, gate, SMALL.top_k, "bf16")
