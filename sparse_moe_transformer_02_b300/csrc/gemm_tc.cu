@@ -87,6 +87,13 @@ struct TcParams {
   float* yacc;
   unsigned int* err;
   uint64_t wait_ns;
+  // Gate/up progress, read by the down pass (see below): ready[e] counts the
+  // finished (tile, epilogue warp) pairs of expert e, ready[E + 1] the
+  // (CTA, epilogue warp) pairs done clearing y_acc.
+  unsigned int* ready;
+  const int32_t* counts;        // per-expert token counts (down pass: readiness targets)
+  int mt_gu, mt_gu_s;           // gate/up row tiles per routed / shared expert
+  int gu_ctas;                  // CTAs of the gate/up grid
 };
 
 __device__ __forceinline__ TcUnit get_unit(const TcParams& p, int u) {
@@ -143,11 +150,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();
   const WaitCtl wc{p.wait_ns, p.err, abort_flag};
-
   constexpr int LIST = MODE == 0 ? 0 : 1;       // unit list: gate/up or down
-  if (MODE >= 1) pdl_wait();
+  // Gate/up lets the down pass launch only once routing is known complete
+  // (each thread triggers right after its own grid-dependency wait), so the
+  // down pass can read the grouping at once; it then waits per expert on the
+  // readiness counters instead of on the whole gate/up grid, and its CTAs take
+  // the SMs that gate/up's last, partial wave leaves idle.
+  auto wait_routing = [] {
+    pdl_wait();
+    pdl_launch_dependents();
+  };
+  if (MODE >= 1) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -161,10 +175,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     bool waited = MODE >= 1;
     if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
     bool ok = true;
+    if (MODE >= 1) {
+      // the down pass adds into y_acc: every gate/up CTA must have cleared it
+      int w = 1;
+      if (lane == 0) w = counter_wait(p.ready + p.E + 1, 4u * p.gu_ctas, wc) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
+    }
     for (int u = blockIdx.x; ok; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
-        pdl_wait();
+        wait_routing();
         waited = true;
         n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
@@ -172,6 +192,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       const TcUnit un = get_unit(p, u);
       const bool sh = un.expert == p.E;
       const int K = sh ? p.Ks : p.K;
+      if (MODE >= 1) {
+        // this expert's h rows: all of its gate/up tiles, four epilogue warps each
+        const int tiles = ((sh ? p.T : __ldcg(p.counts + un.expert)) + kTcBN - 1) / kTcBN;
+        const unsigned target = 4u * (sh ? p.mt_gu_s : p.mt_gu) * tiles;
+        int w = 1;
+        if (lane == 0) {
+          w = counter_wait(p.ready + un.expert, target, wc) ? 1 : 0;
+          fence_proxy_async_global();          // h was written with plain stores; TMA reads it
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+      }
       const int wrows = MODE >= 2 ? 2 * kTcBN : kTcBM;          // weight rows per tile
       const int arow = sh ? un.m_tile * wrows : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * wrows;
       const CUtensorMap* ma0 = sh ? &p.tm_sa0 : &p.tm_a0;
@@ -221,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       for (int u = blockIdx.x; ok; u += gridDim.x) {
         if (u >= n_total) {
           if (waited) break;
-          pdl_wait();
+          wait_routing();
           waited = true;
           n_total = __ldcg(p.n_units + LIST);
           if (u >= n_total) break;
@@ -260,6 +291,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         buf ^= 1;
       }
       if (!ok && last_commit) drain_wait(last_commit, last_commit_par, p.wait_ns);
+    } else if (MODE == 0) {
+      wait_routing();                         // the idle lanes trigger too
     }
     __syncwarp();
   } else {
@@ -267,11 +300,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     const int q = warp & 3;                  // TMEM lane quarter of this warp
     const int ept = threadIdx.x - 64;        // 0..127
     if (MODE == 0) {
-      // clear the fp32 accumulator of pass 2 (x-independent, needs no routing)
+      // clear the fp32 accumulator of pass 2 (x-independent, needs no routing).
+      // Safe ahead of the grid-dependency wait: every call starts with a router
+      // that lets its dependents launch only after the previous kernel on the
+      // stream has completed, so no kernel of an earlier call is still running.
       float4* ya = reinterpret_cast<float4*>(p.yacc);
       const size_t n4 = (size_t)p.T * p.d / 4;
       for (size_t i = (size_t)blockIdx.x * 128 + ept; i < n4; i += (size_t)gridDim.x * 128)
         ya[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(p.ready + p.E + 1, 1u);
+      }
     }
     uint32_t tph[2] = {0, 0};
     int buf = 0;
@@ -282,7 +323,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     for (int u = blockIdx.x;; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
-        pdl_wait();
+        wait_routing();
         waited = true;
         n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
@@ -415,6 +456,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           }
         }
       }
+      if (MODE == 0) {
+        // this warp's rows of the tile are in h: publish them to the down pass
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(p.ready + un.expert, 1u);
+        }
+      }
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
       tph[buf] ^= 1;
@@ -462,12 +511,17 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(const __nv_bfloat16* __r
   }
 }
 
-// y = bf16(y_acc (+ x)), 8 values per thread.
+// y = bf16(y_acc (+ x)), 8 values per thread.  Also returns the gate/up
+// readiness counters to zero for the next call (the down pass, which reads
+// them, has completed).
 __global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restrict__ yacc,
                                                           const __nv_bfloat16* __restrict__ x,
-                                                          __nv_bfloat16* __restrict__ y, size_t n8, int residual) {
+                                                          __nv_bfloat16* __restrict__ y, size_t n8, int residual,
+                                                          unsigned int* ready, int n_ready) {
   pdl_launch_dependents();
   pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = __ldcg(reinterpret_cast<const float4*>(yacc) + 2 * i);
     const float4 b = __ldcg(reinterpret_cast<const float4*>(yacc) + 2 * i + 1);
@@ -529,14 +583,14 @@ int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n) {
   return (int)(routed + shared);
 }
 
-cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, int num_sms,
-                               cudaStream_t s, Prof* prof) {
+cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, unsigned int* ready,
+                               int n_ready, int num_sms, cudaStream_t s, Prof* prof) {
   const size_t n8 = n / 8;
   const int grid = (int)((n8 + 255) / 256 < (size_t)num_sms * 4 ? (n8 + 255) / 256 : (size_t)num_sms * 4);
   if (prof) prof->begin(MOE_K_TC_FINALIZE, s);
   const cudaError_t e = launch_ex(tc_finalize_kernel, grid > 0 ? grid : 1, 256, 0, s, yacc,
                                   static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), n8,
-                                  (int)residual);
+                                  (int)residual, ready, n_ready);
   if (prof) prof->end(s);
   return e;
 }
@@ -566,6 +620,10 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.err = a.ws.err;
   p.wait_ns = a.wait_ns;
   p.n_units = a.ws.n_units;
+  p.ready = a.ws.ready;
+  p.counts = a.ws.counts;
+  p.mt_gu = a.F / kTcBM;
+  p.mt_gu_s = a.Fs > 0 ? a.Fs / kTcBM : 1;
   // slot-ordered copy of the routed activations
   const int slots = a.T * a.k;
   const int gg = (slots + 7) / 8 < num_sms * 8 ? (slots + 7) / 8 : num_sms * 8;   // 8 warps per block
@@ -585,6 +643,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.n_pre = a.Fs > 0 ? (a.Fs / kTcBM) * ((a.T + kTcBN - 1) / kTcBN) : 0;
   p.units = a.ws.units_gu;
   const int grid1 = num_sms < a.max_units_gu ? num_sms : (a.max_units_gu > 0 ? a.max_units_gu : 1);
+  p.gu_ctas = grid1;
   if (prof) prof->begin(MOE_K_TC_GATEUP, s);
   e = launch_ex(tc_kernel<0>, grid1, kThreadsTc, tc_smem_bytes<0>(), s, p);
   if (prof) prof->end(s);
@@ -612,7 +671,8 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, num_sms, s, prof);
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 2,
+                            num_sms, s, prof);
 }
 
 }  // namespace moe

@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
     if (MODE == 0) {
       // clear the fp32 accumulator of pass 2 (x-independent, needs no routing).
       // Safe ahead of the grid-dependency wait: every call starts with a router
-      // launched without programmatic serialisation, so no kernel of an
-      // earlier call on this handle is still running.
+      // that lets its dependents launch only after the previous kernel on the
+      // stream has completed, so no kernel of an earlier call is still running.
       const int ept = threadIdx.x - 64;
       float4* ya = reinterpret_cast<float4*>(p.yacc);
       const size_t n4 = (size_t)p.T * p.d / 4;
@@ -569,7 +569,8 @@ cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof
   e = launch_pdl(tc4_kernel<1>, grid2, kThreads4, tc4_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, num_sms, s, prof);
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 2,
+                            num_sms, s, prof);
 }
 
 }  // namespace moe

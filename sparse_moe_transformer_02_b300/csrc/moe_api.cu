@@ -391,6 +391,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.wr_split, h->rtc_capable ? 3 * E * d * 2 : 16},
       {(void**)&ws.cand, h->rtc_capable ? Tm * (E / 64) * kMaxTopK * 8 : 16},
       {(void**)&ws.fin, Tg * (d / kFinRows) * 4},
+      {(void**)&ws.ready, (E + 2) * 4},
       {(void**)&ws.err, 16},
       {&ws.x_stage, Tm * d * act_bytes(c)},
       {&ws.y_stage, Tm * d * act_bytes(c)},
@@ -413,6 +414,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   cudaError_t e = cudaMemsetAsync(ws.counters, 0, (size_t)h->n_counters * 4, stream);
   if (e == cudaSuccess && h->rtc_capable) e = launch_router_split(w->router_w, ws.wr_split, E * d, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.fin, 0, Tg * (d / kFinRows) * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.ready, 0, (E + 2) * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.err, 0, 16, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {

@@ -62,6 +62,9 @@ struct Workspace {
   __nv_bfloat16* wr_split;  // [3][E][d] router weights as bf16 hi, mid, lo (tensor-core router)
   uint64_t* cand;         // [max_T][E / 64][kMaxTopK] tensor-core router: per-slice selection keys
   uint32_t* fin;          // [kGemvChunkT][d / 32] GEMV down completion counts (kept at zero between calls)
+  uint32_t* ready;        // [E + 2] tcgen05 gate/up progress (kept at zero between calls): [e] finished
+                          // tile quarters of expert e ([E] = the shared expert), [E + 1] CTA quarters
+                          // done clearing y_acc
   unsigned int* err;      // device error word
   void* x_stage;          // [max_T][d] moe_forward_host staging
   void* y_stage;
@@ -177,9 +180,9 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof);
 // Most unit-list entries a call can produce (token tiles of tile_n).
 int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k, int tile_n);
 int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n);
-// y = bf16(y_acc (+ x)) over T x d values.
-cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, int num_sms,
-                               cudaStream_t s, Prof* prof);
+// y = bf16(y_acc (+ x)) over T x d values; clears ready[0 .. n_ready).
+cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, unsigned int* ready,
+                               int n_ready, int num_sms, cudaStream_t s, Prof* prof);
 
 // NVFP4 weights on the tensor cores.  Tensor maps over the packed codes
 // (bytes [rows][K / 2], box 128 B x 128 rows, 128-byte swizzle) and the block

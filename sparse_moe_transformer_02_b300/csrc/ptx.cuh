@@ -96,6 +96,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
+// Bounded wait until *p >= target (acquire, GPU scope), for counters that
+// other CTAs of this or an earlier grid raise.  Follow it with
+// fence_proxy_async_global() before reading what they wrote through TMA.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool counter_wait(const unsigned* p, unsigned target, const WaitCtl& w) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 15u) == 0) {
+      if (*w.abort_flag) return false;
+      if (global_ns() - t0 > w.limit_ns) {
+        *w.abort_flag = 1;
+        atomicOr(w.err, 1u << 5);   // bit 5 = MOE_ERR_TIMEOUT
+        return false;
+      }
+    }
+  }
+}
+// Orders generic-proxy global writes observed so far before later async-proxy
+// (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

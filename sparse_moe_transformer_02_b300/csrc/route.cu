@@ -16,6 +16,8 @@
 //  * route_large: one CTA per 32 tokens computes all E logits of its tokens
 //    (fp32 SIMT tile), selects the top k and writes one selection-bitmap word
 //    per expert; the last CTA scans the bitmap into the grouping.
+#include <utility>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -23,6 +25,34 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;
+
+// Every call starts with a router.  It is launched with programmatic
+// serialisation, so its launch and set-up overlap the tail of the previous
+// kernel on the stream, but it waits for that kernel to complete before it
+// reads x (the previous layer's output) and before it lets the next kernels
+// launch: the expert kernels' work ahead of their own grid-dependency wait
+// (clearing the fp32 accumulator, the shared expert's tiles) can then never
+// meet a kernel of an earlier call.
+__device__ __forceinline__ void route_entry() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_route(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 constexpr int kLargeBT = 32;     // tokens per CTA in route_large
 
 __device__ __forceinline__ void load_x4(const void* x, int act_bf16, size_t off, float (&v)[4]) {
@@ -273,7 +303,7 @@ __device__ void group_from_counts(const RouteArgs& a, int nblk) {
 constexpr int kSmallTok = 8;
 
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
-  pdl_launch_dependents();
+  route_entry();
   extern __shared__ __align__(16) uint8_t xs[];     // [8][d] activations (f32 or bf16)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, d = a.d, T = a.T, k = a.k;
@@ -377,7 +407,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
 // and experts 4 tx + 128 j .. + 3 for j < E / 128.
 template <int EJ>
 __global__ void __launch_bounds__(kRouteThreads) route_large_kernel(RouteArgs a) {
-  pdl_launch_dependents();
+  route_entry();
   extern __shared__ __align__(16) float dsm[];
   const int E = a.E, d = a.d, T = a.T, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -523,7 +553,7 @@ __global__ void __launch_bounds__(192, 1) route_tc_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();
+  route_entry();
   const WaitCtl wc{p.wait_ns, a.ws.err, abort_flag};
   const int nkb = d / 64;
   if (warp == 0 && lane == 0) {
@@ -735,9 +765,9 @@ cudaError_t launch_route_tc(const RouteArgs& a, const CUtensorMap* tm_x, const C
   p.cand = cand;
   p.wait_ns = wait_ns;
   if (prof) prof->begin(MOE_K_ROUTE, s);
-  route_tc_kernel<<<dim3(a.E / 64, (a.T + 127) / 128), 192, smem, s>>>(p);
+  const cudaError_t e = launch_pdl_route(route_tc_kernel, dim3(a.E / 64, (a.T + 127) / 128), 192, smem, s, p);
   if (prof) prof->end(s);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
@@ -753,9 +783,9 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
       attr_set = true;
     }
     const dim3 grid((a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32), (a.T + kSmallTok - 1) / kSmallTok);
-    route_small_kernel<<<grid, kRouteThreads, smem, s>>>(a);
+    const cudaError_t e = launch_pdl_route(route_small_kernel, grid, kRouteThreads, smem, s, a);
     if (prof) prof->end(s);
-    return cudaGetLastError();
+    return e;
   }
   const int grid = (a.T + kLargeBT - 1) / kLargeBT;
   const int ej = (a.E + 127) / 128;
@@ -770,7 +800,8 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
         return cudaGetLastError();                                                                  \
       attr_set = true;                                                                              \
     }                                                                                               \
-    route_large_kernel<N><<<grid, kRouteThreads, smem, s>>>(a);                                     \
+    const cudaError_t e = launch_pdl_route(route_large_kernel<N>, dim3(grid), kRouteThreads, smem, s, a); \
+    if (e != cudaSuccess) return e;                                                                 \
     break;                                                                                          \
   }
     MOE_RL(1) MOE_RL(2) MOE_RL(3) MOE_RL(4)
