@@ -94,15 +94,41 @@ struct TcParams {
   const int32_t* counts;        // per-expert token counts (down pass: readiness targets)
   int mt_gu, mt_gu_s;           // gate/up row tiles per routed / shared expert
   int gu_ctas;                  // CTAs of the gate/up grid
+  // Small batches leave most SMs idle with one unit per (expert, row tile):
+  // pass 1 then splits every tile into ksplit parts along K (consecutive
+  // entries u of one tile, part u % ksplit).  Each part stores its partial
+  // sums to gu_part[part]; the last part to finish a warp's rows (gu_cnt)
+  // adds the parts in order (deterministic) and writes h.
+  int ksplit;
+  int P;                        // rows of h (T (k + 1))
+  float* gu_part;
+  unsigned int* gu_cnt;
 };
 
 __device__ __forceinline__ TcUnit get_unit(const TcParams& p, int u) {
   if (u < p.n_pre) {
-    const int tb = u / p.mt_s, m = u % p.mt_s;
+    const int base = u / p.ksplit, tb = base / p.mt_s, m = base % p.mt_s;
     return TcUnit{p.E, m, tb * kTcBN, min(kTcBN, p.T - tb * kTcBN)};
   }
   return p.units[u];
 }
+
+// Unit descriptors one step ahead: the entry a role needs next is loaded while
+// it works on the current one, so no role stalls on that load between units.
+struct UnitCursor {
+  TcUnit nxt;
+  int nxt_u = -1;
+  __device__ __forceinline__ TcUnit get(const TcParams& p, int u, int n_total) {
+    const TcUnit un = u == nxt_u ? nxt : get_unit(p, u);
+    const int v = u + (int)gridDim.x;
+    nxt_u = -1;
+    if (v < n_total) {
+      nxt = get_unit(p, v);
+      nxt_u = v;
+    }
+    return un;
+  }
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant__ TcParams p) {
@@ -181,6 +207,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       if (lane == 0) w = counter_wait(p.ready + p.E + 1, 4u * p.gu_ctas, wc) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
     }
+    UnitCursor cur;
     for (int u = blockIdx.x; ok; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
@@ -189,9 +216,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
       }
-      const TcUnit un = get_unit(p, u);
+      const TcUnit un = cur.get(p, u, n_total);
       const bool sh = un.expert == p.E;
       const int K = sh ? p.Ks : p.K;
+      const int kb = K / kTcBK, part = u % p.ksplit;
+      const int kbeg = part * kb / p.ksplit * kTcBK, kend = (part + 1) * kb / p.ksplit * kTcBK;
       if (MODE >= 1) {
         // this expert's h rows: all of its gate/up tiles, four epilogue warps each
         const int tiles = ((sh ? p.T : __ldcg(p.counts + un.expert)) + kTcBN - 1) / kTcBN;
@@ -210,7 +239,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       const uint32_t bytes = MODE == 0 ? 2 * kTcBM * 128 + kTcBN * 128 : (uint32_t)C::STAGE_BYTES;
       const CUtensorMap* mb = sh ? &p.tm_sb : &p.tm_b;
       const int brow = (MODE >= 1 && sh) ? p.T * p.k + un.slot0 : un.slot0;
-      for (int k0 = 0; k0 < K; k0 += kTcBK) {
+      for (int k0 = kbeg; k0 < kend; k0 += kTcBK) {
         if (!warp_wait(&empty[stage], phase ^ 1, wc)) { ok = false; break; }
         uint8_t* st = stages + stage * C::STAGE_BYTES;
         if (lane == 0) {
@@ -249,6 +278,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       bool ok = true;
       uint64_t* last_commit = nullptr;
       uint32_t last_commit_par = 0;
+      UnitCursor cur;
       for (int u = blockIdx.x; ok; u += gridDim.x) {
         if (u >= n_total) {
           if (waited) break;
@@ -257,21 +287,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           n_total = __ldcg(p.n_units + LIST);
           if (u >= n_total) break;
         }
-        const TcUnit un = get_unit(p, u);
+        const TcUnit un = cur.get(p, u, n_total);
         const bool sh = un.expert == p.E;
         const int n_pad = (un.n + 15) & ~15;
         const int K = sh ? p.Ks : p.K;
         const uint32_t idesc = MODE >= 2 ? idesc_bf16_f32(kTcBM, 2 * kTcBN) : idesc_bf16_f32(kTcBM, n_pad);
+        const int kb = K / kTcBK, part = u % p.ksplit;
+        const int kbeg = part * kb / p.ksplit * kTcBK, kend = (part + 1) * kb / p.ksplit * kTcBK;
         if (!mbar_wait(&tempty[buf], tph[buf] ^ 1, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::ACC_COLS;
-        for (int k0 = 0; k0 < K; k0 += kTcBK) {
+        for (int k0 = kbeg; k0 < kend; k0 += kTcBK) {
           if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(stages + stage * C::STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
-            const uint32_t accum = (k0 > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t accum = (k0 > kbeg || kk > 0) ? 1u : 0u;
             if (MODE == 0) {
               const uint64_t bd = sdesc_sw128(st + 2 * kTcBM * 128 + kk * 32);
               tc_mma_f16(acc, sdesc_sw128(st + kk * 32), bd, idesc, accum);
@@ -320,6 +352,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     int n_total = p.n_pre;
     bool waited = MODE >= 1;
     if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
+    UnitCursor cur;
     for (int u = blockIdx.x;; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
@@ -328,7 +361,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         n_total = __ldcg(p.n_units + LIST);
         if (u >= n_total) break;
       }
-      const TcUnit un = get_unit(p, u);
+      const TcUnit un = cur.get(p, u, n_total);
       const bool sh = un.expert == p.E;
       const int n_pad = (un.n + 15) & ~15;
       if (MODE == 1) {
@@ -427,6 +460,70 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
       const int row = un.m_tile * kTcBM + q * 32 + lane;
+      if (MODE == 0 && p.ksplit > 1) {
+        // one part of a split tile: store the partial sums of this warp's rows
+        const int part = u % p.ksplit, brow = sh ? p.T * p.k + un.slot0 : un.slot0;
+        for (int c0 = 0; c0 < n_pad; c0 += 16) {
+          uint32_t g[16], v[16];
+          tmem_ld16(acc + c0, g);
+          tmem_ld16(acc + kTcBN + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            if (col < un.n) {
+              float* pp = p.gu_part + ((size_t)(part * p.P + brow + col) * 2) * p.Fmax + row;
+              pp[0] = __uint_as_float(g[i]);
+              pp[p.Fmax] = __uint_as_float(v[i]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+        tph[buf] ^= 1;
+        buf ^= 1;
+        // the last part to arrive adds the parts in order and writes h
+        unsigned int* cnt = p.gu_cnt + (size_t)(u / p.ksplit) * 4 + q;
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(cnt, 1u) == (unsigned)p.ksplit - 1 ? 1 : 0;
+          if (last) __threadfence();
+        }
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        __syncwarp();
+        if (last) {
+          for (int col = 0; col < un.n; ++col) {
+            // all parts' loads issued together, then added in part order
+            float pa[kMaxKSplit], pb[kMaxKSplit];
+#pragma unroll
+            for (int pt = 0; pt < kMaxKSplit; ++pt) {
+              pa[pt] = pb[pt] = 0.f;
+              if (pt < p.ksplit) {
+                const float* pp = p.gu_part + ((size_t)(pt * p.P + brow + col) * 2) * p.Fmax + row;
+                pa[pt] = __ldcg(pp);
+                pb[pt] = __ldcg(pp + p.Fmax);
+              }
+            }
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int pt = 0; pt < kMaxKSplit; ++pt) {
+              a += pa[pt];
+              b += pb[pt];
+            }
+            const float h = a / (1.f + __expf(-a)) * b;
+            p.h16[(size_t)(brow + col) * p.Fmax + row] = __float2bfloat16_rn(h);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            *cnt = 0;                                 // ready for the next call
+            __threadfence();
+            atomicAdd(p.ready + un.expert, 1u);
+          }
+        }
+        continue;
+      }
       for (int c0 = 0; c0 < n_pad; c0 += 16) {
         if (MODE == 0) {
           uint32_t g[16], v[16];
@@ -622,6 +719,10 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.n_units = a.ws.n_units;
   p.ready = a.ws.ready;
   p.counts = a.ws.counts;
+  p.ksplit = a.gu_split;
+  p.P = a.T * (a.k + 1);
+  p.gu_part = a.ws.gu_part;
+  p.gu_cnt = a.ws.gu_cnt;
   p.mt_gu = a.F / kTcBM;
   p.mt_gu_s = a.Fs > 0 ? a.Fs / kTcBM : 1;
   // slot-ordered copy of the routed activations
@@ -640,7 +741,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.K = a.d; p.Ks = a.d;
   p.mt = a.F / kTcBM;
   p.mt_s = a.Fs > 0 ? a.Fs / kTcBM : 1;
-  p.n_pre = a.Fs > 0 ? (a.Fs / kTcBM) * ((a.T + kTcBN - 1) / kTcBN) : 0;
+  p.n_pre = a.Fs > 0 ? a.gu_split * (a.Fs / kTcBM) * ((a.T + kTcBN - 1) / kTcBN) : 0;
   p.units = a.ws.units_gu;
   const int grid1 = num_sms < a.max_units_gu ? num_sms : (a.max_units_gu > 0 ? a.max_units_gu : 1);
   p.gu_ctas = grid1;
@@ -660,6 +761,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.mt = a.d / a.dn_rows;
   p.mt_s = a.d / a.dn_rows;
   p.n_pre = 0;
+  p.ksplit = 1;
   p.units = a.ws.units_dn;
   const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
   if (prof) prof->begin(MOE_K_TC_DOWN, s);

@@ -21,6 +21,7 @@ constexpr int kTcBN = 128;           // tcgen05 path: largest token tile (MMA N)
 constexpr int kTcBM = 128;           // tcgen05 path: weight rows per tile (MMA M)
 constexpr int kTcBK = 64;            // tcgen05 path: reduction step per stage (128 bytes of bf16)
 constexpr int kTokMajorT = 512;      // tcgen05 path: T at which the down pass turns token-major
+constexpr int kMaxKSplit = 8;        // tcgen05 path: most parts a small batch's gate/up tiles split into along K
 constexpr int kTc4BN = 64;           // NVFP4 tcgen05 path: largest token tile
 constexpr int kTc4KS = 256;          // NVFP4 tcgen05 path: reduction step per stage (16 scale bytes per row)
 constexpr unsigned kErrTimeout = 1u << 5;
@@ -62,6 +63,8 @@ struct Workspace {
   __nv_bfloat16* wr_split;  // [3][E][d] router weights as bf16 hi, mid, lo (tensor-core router)
   uint64_t* cand;         // [max_T][E / 64][kMaxTopK] tensor-core router: per-slice selection keys
   uint32_t* fin;          // [kGemvChunkT][d / 32] GEMV down completion counts (kept at zero between calls)
+  float* gu_part;         // [kMaxKSplit][min(max_T, 64) * (k + 1)][2][F_max] partial gate/up sums (split tiles)
+  uint32_t* gu_cnt;       // [4 per gate/up tile] arrivals of a split tile's parts (kept at zero between calls)
   uint32_t* ready;        // [E + 2] tcgen05 gate/up progress (kept at zero between calls): [e] finished
                           // tile quarters of expert e ([E] = the shared expert), [E + 1] CTA quarters
                           // done clearing y_acc
@@ -105,6 +108,7 @@ struct RouteArgs {
   int build_tc_units;     // also build tcgen05 unit lists
   int dn_rows;            // Wd rows per down tile (128 weight-major, 256 token-major)
   int tile_n;             // token tile of the unit lists (kTcBN, or kTc4BN for NVFP4 weights)
+  int gu_split;           // parts along K of every gate/up tile (1 = none)
   int F, Fs;              // widths (for unit lists)
   int has_shared;
 };
@@ -172,6 +176,7 @@ struct TcArgs {
   const int32_t* idx;           // [T][k]
   int wpb;                      // > 0: the gather kernel places slots (bitmap words per router block)
   int T, d, F, Fs, E, k, add_residual;
+  int gu_split;                 // parts along K of every gate/up tile (as given to the router)
   Workspace ws;
   uint64_t wait_ns;
   int max_units_gu, max_units_dn;

@@ -248,20 +248,22 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
   for (int pass = 0; pass < 2; ++pass) {
     const int mt = pass == 0 ? mt_gu : mt_dn;
     const int sh_mt = pass == 0 ? sh_mt_gu : mt_dn;
+    const int rep = pass == 0 ? a.gu_split : 1;   // gate/up tiles split along K: one entry per part
     TcUnit* out = pass == 0 ? a.ws.units_gu : a.ws.units_dn;
-    for (int e = tid; e < E; e += blockDim.x) scratch[e] = mt * ((cnt[e] + tn - 1) / tn);
+    for (int e = tid; e < E; e += blockDim.x) scratch[e] = rep * mt * ((cnt[e] + tn - 1) / tn);
     __syncthreads();
     const int n_routed = block_exclusive_scan(scratch, E);
-    const int sh_units = sh_mt * sh_tb;
+    const int sh_units = rep * sh_mt * sh_tb;
     for (int u = tid; u < sh_units; u += blockDim.x) {
-      const int tb = u / sh_mt, m = u % sh_mt;
+      const int base = u / rep, tb = base / sh_mt, m = base % sh_mt;
       out[u] = TcUnit{E, m, tb * tn, min(tn, a.T - tb * tn)};
     }
     for (int e = tid; e < E; e += blockDim.x) {
       const int c = cnt[e];
       int u = sh_units + scratch[e];
       for (int tb = 0; tb * tn < c; ++tb)
-        for (int m = 0; m < mt; ++m) out[u++] = TcUnit{e, m, offs[e] + tb * tn, min(tn, c - tb * tn)};
+        for (int m = 0; m < mt; ++m)
+          for (int r = 0; r < rep; ++r) out[u++] = TcUnit{e, m, offs[e] + tb * tn, min(tn, c - tb * tn)};
     }
     if (tid == 0) a.ws.n_units[pass] = sh_units + n_routed;
     __syncthreads();

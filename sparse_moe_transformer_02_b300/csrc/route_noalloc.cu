@@ -103,6 +103,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int
   a.build_tc_units = 0;
   a.dn_rows = kTcBM;
   a.tile_n = kTcBN;
+  a.gu_split = 1;
   a.F = 0;
   a.Fs = 0;
   a.has_shared = 0;
