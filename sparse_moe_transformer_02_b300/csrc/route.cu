@@ -10,9 +10,9 @@
 // what lets each expert's weights be streamed once per call.
 //
 // Two variants:
-//  * route_small (T <= 64): one warp per expert computes the logits of all
-//    tokens; the last CTA to finish (atomic ticket) selects, groups and
-//    writes everything.  One launch.
+//  * route_small (T <= 64): each CTA computes the logits of eight experts for
+//    eight tokens; the last CTA of each token chunk selects, the last of those
+//    groups (atomic tickets).  One launch.
 //  * route_large: one CTA per 32 tokens computes all E logits of its tokens
 //    (fp32 SIMT tile), selects the top k and writes one selection-bitmap word
 //    per expert; the last CTA scans the bitmap into the grouping.
@@ -300,66 +300,79 @@ __device__ void group_from_counts(const RouteArgs& a, int nblk) {
 }
 
 // ------------------------------------------------------------------ small T
-// grid (ceil(E / 8), ceil(T / 8)): warp w of CTA (bx, by) scores expert 8 bx + w
-// against tokens 8 by .. 8 by + 7, whose activations are staged in shared memory.
+// grid (ceil(E / 8), ceil(T / 8)): CTA (bx, by) scores experts 8 bx .. 8 bx + 7
+// against tokens 8 by .. 8 by + 7, whose activations are staged in shared
+// memory as fp32.  Warp w takes four of the experts (w % 2) and a quarter of
+// the reduction (w / 2); each step a lane loads four router values of each of
+// its experts and four activations of each token and does 128 FMAs with them
+// (about one instruction per FMA).  The four quarters are added in a fixed
+// order through shared memory.
 constexpr int kSmallTok = 8;
+constexpr int kSmallExp = 4;       // experts per warp
+constexpr int kSmallKq = 4;        // parts of the reduction per CTA
 
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
   route_entry();
-  extern __shared__ __align__(16) uint8_t xs[];     // [8][d] activations (f32 or bf16)
+  extern __shared__ __align__(16) float xs[];       // [8][d] fp32 activations
+  __shared__ float part[kSmallKq][2 * kSmallExp * kSmallTok];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, d = a.d, T = a.T, k = a.k;
   const int t0 = blockIdx.y * kSmallTok;
   const int nt = min(kSmallTok, T - t0);
-  const int es = a.act_bf16 ? 2 : 4;
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.x) + (size_t)t0 * d * es);
-    const int n16 = nt * d * es / 16;
-    for (int i = threadIdx.x; i < n16; i += kRouteThreads) reinterpret_cast<uint4*>(xs)[i] = __ldg(src + i);
+  if (a.act_bf16) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + (size_t)t0 * d);
+    const int n16 = nt * d / 8;
+    for (int i = threadIdx.x; i < n16; i += kRouteThreads) {
+      const uint4 v = __ldg(src + i);
+      float4* dst = reinterpret_cast<float4*>(xs) + 2 * i;
+      dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                           __uint_as_float(v.y & 0xFFFF0000u));
+      dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
+                           __uint_as_float(v.w & 0xFFFF0000u));
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t0 * d);
+    const int n4 = nt * d / 4;
+    for (int i = threadIdx.x; i < n4; i += kRouteThreads) reinterpret_cast<float4*>(xs)[i] = __ldg(src + i);
   }
   __syncthreads();
-  const int e = blockIdx.x * (kRouteThreads / 32) + warp;
-  if (e < E) {
-    const float* w = a.Wr + (size_t)e * d;
-    float acc[kSmallTok];
+  const int eg = warp & 1, kq = warp >> 1;
+  const int e0 = blockIdx.x * 2 * kSmallExp + eg * kSmallExp;
+  const int kd = d / kSmallKq, kbeg = kq * kd;       // d / 4 is a multiple of 16 values
+  {
+    float acc[kSmallExp * kSmallTok];                   // [expert j][token t]
 #pragma unroll
-    for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
-    // 16 loads of the router row in flight per lane (one round trip for d = 2048)
-    for (int cb = lane * 4; cb < d; cb += 128 * 16) {
-      float4 wr[16];
+    for (int i = 0; i < kSmallExp * kSmallTok; ++i) acc[i] = 0.f;
+    for (int c = kbeg + lane * 4; c < kbeg + kd; c += 128) {
+      float4 wr[kSmallExp];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        wr[i] = cb + 128 * i < d ? __ldg(reinterpret_cast<const float4*>(w + cb + 128 * i))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kSmallExp; ++j)
+        wr[j] = e0 + j < E ? __ldg(reinterpret_cast<const float4*>(a.Wr + (size_t)(e0 + j) * d + c))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = cb + 128 * i;
-        if (c >= d) break;
+      for (int t = 0; t < kSmallTok; ++t) {
+        if (t < nt) {
+          const float4 xv = *reinterpret_cast<const float4*>(xs + (size_t)t * d + c);
 #pragma unroll
-        for (int t = 0; t < kSmallTok; ++t) {
-          if (t < nt) {
-            float xv[4];
-            if (a.act_bf16) {
-              const uint2 r = *reinterpret_cast<const uint2*>(xs + ((size_t)t * d + c) * 2);
-              xv[0] = __uint_as_float(r.x << 16);
-              xv[1] = __uint_as_float(r.x & 0xFFFF0000u);
-              xv[2] = __uint_as_float(r.y << 16);
-              xv[3] = __uint_as_float(r.y & 0xFFFF0000u);
-            } else {
-              const float4 r = *reinterpret_cast<const float4*>(xs + ((size_t)t * d + c) * 4);
-              xv[0] = r.x; xv[1] = r.y; xv[2] = r.z; xv[3] = r.w;
-            }
-            acc[t] = fmaf(wr[i].x, xv[0], acc[t]);
-            acc[t] = fmaf(wr[i].y, xv[1], acc[t]);
-            acc[t] = fmaf(wr[i].z, xv[2], acc[t]);
-            acc[t] = fmaf(wr[i].w, xv[3], acc[t]);
+          for (int j = 0; j < kSmallExp; ++j) {
+            float& r = acc[j * kSmallTok + t];
+            r = fmaf(wr[j].x, xv.x, r);
+            r = fmaf(wr[j].y, xv.y, r);
+            r = fmaf(wr[j].z, xv.z, r);
+            r = fmaf(wr[j].w, xv.w, r);
           }
         }
       }
     }
-    const float tot = transpose_reduce<kSmallTok, 32>(acc, lane);    // lane l: token l >> 2
-    const int tt = lane >> 2;
-    if ((lane & 3) == 0 && tt < nt) a.ws.logits[(size_t)(t0 + tt) * E + e] = tot + (a.b ? a.b[e] : 0.f);
+    const float tot = transpose_reduce<kSmallExp * kSmallTok, 32>(acc, lane);   // lane l: expert l / 8, token l % 8
+    part[kq][eg * kSmallExp * kSmallTok + lane] = tot;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * kSmallExp * kSmallTok) {
+    const int v = threadIdx.x;                          // (expert group, expert, token)
+    const float tot = ((part[0][v] + part[1][v]) + part[2][v]) + part[3][v];
+    const int e = blockIdx.x * 2 * kSmallExp + (v >> 3), tt = v & 7;
+    if (e < E && tt < nt) a.ws.logits[(size_t)(t0 + tt) * E + e] = tot + (a.b ? a.b[e] : 0.f);
   }
   // Two-level tail.  The last of the expert-chunk CTAs of this token chunk
   // selects the chunk's tokens (one warp per token); the last of those does
@@ -776,7 +789,7 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
   (void)num_sms;
   if (prof) prof->begin(MOE_K_ROUTE, s);
   if (a.T <= kSmallT) {
-    const size_t smem = (size_t)kSmallTok * a.d * (a.act_bf16 ? 2 : 4);
+    const size_t smem = (size_t)kSmallTok * a.d * 4;
     static bool attr_set = false;  // once, before any stream capture
     if (!attr_set) {
       if (cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
@@ -784,7 +797,8 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
         return cudaGetLastError();
       attr_set = true;
     }
-    const dim3 grid((a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32), (a.T + kSmallTok - 1) / kSmallTok);
+    const int epc = 2 * kSmallExp;   // experts per CTA
+    const dim3 grid((a.E + epc - 1) / epc, (a.T + kSmallTok - 1) / kSmallTok);
     const cudaError_t e = launch_pdl_route(route_small_kernel, grid, kRouteThreads, smem, s, a);
     if (prof) prof->end(s);
     return e;
