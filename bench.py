@@ -130,6 +130,22 @@ def dram_traffic(kernel, workload):
     return rec.get("bytes_per_launch")
 
 
+def max_over_ranks(v, device):
+    """The largest of the ranks' values, on every rank (v itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, t_max_s, world):
+    """Whole-job rate of independent replicas: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / t_max_s
+
+
 def make_device_layers(kind, n_layers, device, seed):
     """n_layers independent Flint-shaped layers drawn on the device (bf16), or NVFP4
     layers that share one host-quantised expert set copied to distinct buffers."""
@@ -235,8 +251,11 @@ def run_ours(args, rank, world, local_rank):
         _, _, cnt = h.route(xi, stream=stream)
         stream.synchronize()
         U.append(int((cnt > 0).sum().item()))
-    tc_path = kind in ("bf16", "stack") and args.path != "gemv"
-    kernels_per_fwd = 5 if tc_path else 3
+    # kernels one forward launches: router, slot placement / activation copy,
+    # gate/up, down, finalise on the tensor-core path; router, (NVFP4: f16
+    # activation copy,) gate/up, down-and-combine on the GEMV path
+    tc_path = args.path != "gemv"
+    kernels_per_fwd = 5 if tc_path else (4 if kind == "nvfp4" else 3)
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -265,14 +284,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_ms = ev0.elapsed_time(ev1)
     clocks = sampler.stop() if sampler else None
+    t_ms = max_over_ranks(t_ms, device)
     if world > 1:
-        tt = torch.tensor([t_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
         dist.barrier()
 
     ms_step = t_ms / args.steps
-    value = world * T * n_layers * args.steps / (t_ms / 1e3)
+    value = job_throughput(T * n_layers * args.steps, t_ms / 1e3, world)
 
     # per-kernel timing (separate, eager pass with event pairs around each launch)
     for h in handles:
@@ -352,13 +369,9 @@ def run_ours(args, rank, world, local_rank):
         else:
             for h in handles:
                 h.forward_host(xh, yh, stream=stream)
-    e_s = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([e_s], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_s = float(tt.item())
+    e_s = max_over_ranks(time.perf_counter() - t0, device)
     io_layers = 1 if chain else n_layers
-    e2e = {"value": round(world * T * n_layers * e_steps / e_s, 1), "unit": "tokens/s",
+    e2e = {"value": round(job_throughput(T * n_layers * e_steps, e_s, world), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": T * spec.d * 2 * io_layers, "d2h_bytes_per_step": T * spec.d * 2 * io_layers}
 
     sweep = {}
