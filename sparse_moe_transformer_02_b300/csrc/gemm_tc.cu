@@ -88,7 +88,8 @@ struct TcParams {
   unsigned int* err;
   uint64_t wait_ns;
   // Gate/up progress, read by the down pass (see below): ready[e] counts the
-  // finished (tile, epilogue warp) pairs of expert e, ready[E + 1] the
+  // finished (tile, epilogue warp) pairs of expert e, ready[E + 2] the
+  // (CTA, epilogue warp) pairs done with all their tiles, ready[E + 1] the
   // (CTA, epilogue warp) pairs done clearing y_acc.
   unsigned int* ready;
   const int32_t* counts;        // per-expert token counts (down pass: readiness targets)
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       ok = __shfl_sync(0xFFFFFFFFu, w, 0) != 0;
     }
     UnitCursor cur;
+    bool gu_done = false;                  // down pass: every gate/up tile seen finished
     for (int u = blockIdx.x; ok; u += gridDim.x) {
       if (u >= n_total) {
         if (waited) break;
@@ -221,16 +223,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       const int K = sh ? p.Ks : p.K;
       const int kb = K / kTcBK, part = u % p.ksplit;
       const int kbeg = part * kb / p.ksplit * kTcBK, kend = (part + 1) * kb / p.ksplit * kTcBK;
-      if (MODE >= 1) {
-        // this expert's h rows: all of its gate/up tiles, four epilogue warps each
+      if (MODE >= 1 && !gu_done) {
+        // this expert's h rows: all of its gate/up tiles, four epilogue warps
+        // each.  Once the whole gate/up grid is seen finished, no unit waits.
         const int tiles = ((sh ? p.T : __ldcg(p.counts + un.expert)) + kTcBN - 1) / kTcBN;
         const unsigned target = 4u * (sh ? p.mt_gu_s : p.mt_gu) * tiles;
-        int w = 1;
+        int w = 1, all = 0;
         if (lane == 0) {
-          w = counter_wait(p.ready + un.expert, target, wc) ? 1 : 0;
+          all = ld_acquire_gpu(p.ready + p.E + 2) >= 4u * p.gu_ctas ? 1 : 0;
+          if (!all) w = counter_wait(p.ready + un.expert, target, wc) ? 1 : 0;
           fence_proxy_async_global();          // h was written with plain stores; TMA reads it
         }
         if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+        gu_done = __shfl_sync(0xFFFFFFFFu, all, 0) != 0;
       }
       const int wrows = MODE >= 2 ? 2 * kTcBN : kTcBM;          // weight rows per tile
       const int arow = sh ? un.m_tile * wrows : (MODE == 0 ? un.expert * p.F : un.expert * p.d) + un.m_tile * wrows;
@@ -566,6 +571,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       tph[buf] ^= 1;
       buf ^= 1;
     }
+    if (MODE == 0) {
+      // all of this warp's tiles are published
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(p.ready + p.E + 2, 1u);
+      }
+    }
     if (MODE == 3) bulk_wait_all();          // every reduction performed before the CTA ends
   }
   tc_fence_before();
@@ -773,7 +786,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 2,
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 3,
                             num_sms, s, prof);
 }
 

@@ -569,7 +569,7 @@ cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof
   e = launch_pdl(tc4_kernel<1>, grid2, kThreads4, tc4_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 2,
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 3,
                             num_sms, s, prof);
 }
 
