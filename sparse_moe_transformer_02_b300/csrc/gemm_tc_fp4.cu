@@ -24,7 +24,8 @@
 // TMA brings the codes (16 KB per matrix, 128-byte swizzle), the block scales
 // (2 KB per matrix) and the activation rows (f16, 16-row boxes, only as many
 // as the tile has tokens).  Four converter warps (one per TMEM lane quarter)
-// decode 64 K values at a time into a double-buffered A area of tensor memory
+// decode 64 (pass 1) or 128 (pass 2) K values at a time into a double-buffered
+// A area of tensor memory
 // (tcgen05.st), one thread issues the MMAs, four epilogue warps drain the
 // double-buffered accumulators:
 //  * pass 1 (gate/up): h = silu(a) * u with a = D_g s_g xs, u = D_u s_u xs;
@@ -41,9 +42,9 @@ namespace moe {
 namespace {
 
 constexpr int kThreads4 = 320;                  // producer, MMA, 4 epilogue warps, 4 converter warps
-constexpr int kSub = 64;                        // K values per converted A buffer
+constexpr int kBoxK = 64;                       // K values per activation-row box (128 bytes of f16)
 constexpr int kBRows = 16;                      // activation rows per TMA box
-constexpr int kSubPerStage = kTc4KS / kSub;     // 4
+constexpr int kBoxPerStage = kTc4KS / kBoxK;    // 4
 
 template <int MODE> struct Tc4Cfg;
 template <> struct Tc4Cfg<0> {                  // gate/up
@@ -51,12 +52,13 @@ template <> struct Tc4Cfg<0> {                  // gate/up
   static constexpr int STAGES = 3;
   static constexpr int A_BYTES = 128 * kTc4KS / 2;            // codes per matrix
   static constexpr int S_BYTES = 128 * kTc4KS / 16;           // block scales per matrix
-  static constexpr int B_BYTES = kSubPerStage * kTc4BN * 128; // activation rows
+  static constexpr int B_BYTES = kBoxPerStage * kTc4BN * 128; // activation rows
   static constexpr int B_OFF = NMAT * A_BYTES;
   static constexpr int S_OFF = B_OFF + B_BYTES;
   static constexpr int STAGE_BYTES = S_OFF + NMAT * S_BYTES;
   static constexpr int ACC_COLS = NMAT * kTc4BN;              // per accumulator buffer
-  static constexpr int A_COLS = NMAT * kSub / 2;              // per A buffer
+  static constexpr int SUB = 64;                              // K values converted per A buffer
+  static constexpr int A_COLS = NMAT * SUB / 2;               // per A buffer
   static constexpr int TMEM_COLS = 512;
 };
 template <> struct Tc4Cfg<1> {                  // down
@@ -64,12 +66,15 @@ template <> struct Tc4Cfg<1> {                  // down
   static constexpr int STAGES = 4;
   static constexpr int A_BYTES = 128 * kTc4KS / 2;
   static constexpr int S_BYTES = 128 * kTc4KS / 16;
-  static constexpr int B_BYTES = kSubPerStage * kTc4BN * 128;
+  static constexpr int B_BYTES = kBoxPerStage * kTc4BN * 128;
   static constexpr int B_OFF = NMAT * A_BYTES;
   static constexpr int S_OFF = B_OFF + B_BYTES;
   static constexpr int STAGE_BYTES = S_OFF + NMAT * S_BYTES;
   static constexpr int ACC_COLS = NMAT * kTc4BN;
-  static constexpr int A_COLS = NMAT * kSub / 2;
+  // one matrix: its 4 MMAs per 64 values finish quickly, so each converter
+  // hand-off carries twice as much to halve the hand-offs per stage
+  static constexpr int SUB = 128;
+  static constexpr int A_COLS = NMAT * SUB / 2;
   static constexpr int TMEM_COLS = 256;
 };
 static_assert(Tc4Cfg<0>::STAGE_BYTES % 1024 == 0 && Tc4Cfg<1>::STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
       const int arow = (sh ? 0 : un.expert * p.rows_e) + un.m_tile * 128;
       const int brow = sh ? p.T * p.k + un.slot0 : un.slot0;
       const int nbox = (un.n + kBRows - 1) / kBRows;
-      const uint32_t bytes = NM * (C::A_BYTES + C::S_BYTES) + kSubPerStage * nbox * kBRows * 128;
+      const uint32_t bytes = NM * (C::A_BYTES + C::S_BYTES) + kBoxPerStage * nbox * kBRows * 128;
       for (int k0 = 0; k0 < K; k0 += kTc4KS) {
         if (!warp_wait(&empty[stage], phase ^ 1, wc)) { ok = false; break; }
         uint8_t* st = stages + stage * C::STAGE_BYTES;
@@ -208,9 +213,9 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
             tma_load_2d_hint(st + C::S_OFF + m * C::S_BYTES, sh ? &p.ssc[m] : &p.sc[m], k0 / 16, arow,
                              &full[stage], pol);
           }
-          for (int j = 0; j < kSubPerStage; ++j)
+          for (int j = 0; j < kBoxPerStage; ++j)
             for (int rb = 0; rb < nbox; ++rb)
-              tma_load_2d(st + C::B_OFF + j * (kTc4BN * 128) + rb * (kBRows * 128), &p.tm_b, k0 + j * kSub,
+              tma_load_2d(st + C::B_OFF + j * (kTc4BN * 128) + rb * (kBRows * 128), &p.tm_b, k0 + j * kBoxK,
                           brow + rb * kBRows, &full[stage]);
         }
         __syncwarp();
@@ -243,17 +248,19 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
         for (int k0 = 0; k0 < K && ok; k0 += kTc4KS) {
           if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
           const uint32_t sb = smem_u32(stages + stage * C::STAGE_BYTES + C::B_OFF);
-          for (int j = 0; j < kSubPerStage; ++j, ++g) {
+          for (int j = 0; j < kTc4KS / C::SUB; ++j, ++g) {
             const int ab = g & 1;
             if (!mbar_wait(&afull[ab], (g >> 1) & 1, wc)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kSub / 16; ++kk) {
-              const uint64_t bd = sdesc_sw128(sb + j * (kTc4BN * 128) + kk * 32);
-              const uint32_t accum = (k0 > 0 || j > 0 || kk > 0) ? 1u : 0u;
+            for (int kk = 0; kk < C::SUB / 16; ++kk) {
+              // values j SUB + 16 kk .. + 15: box (j SUB + 16 kk) / 64 of the stage, 32 bytes per 16 values
+              const int kv = j * C::SUB + kk * 16;
+              const uint64_t bd = sdesc_sw128(sb + (kv / kBoxK) * (kTc4BN * 128) + (kv % kBoxK) * 2);
+              const uint32_t accum = (k0 > 0 || kv > 0) ? 1u : 0u;
 #pragma unroll
               for (int m = 0; m < NM; ++m)
-                tc_mma_f16_ts(acc + m * kTc4BN, tmem_a + ab * C::A_COLS + m * (kSub / 2) + kk * 8, bd, idesc, accum);
+                tc_mma_f16_ts(acc + m * kTc4BN, tmem_a + ab * C::A_COLS + m * (C::SUB / 2) + kk * 8, bd, idesc, accum);
             }
             tc_commit(&aempty[ab]);
             last_commit = &aempty[ab];
@@ -284,31 +291,37 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
       for (int k0 = 0; k0 < K; k0 += kTc4KS) {
         if (!warp_wait(&full[stage], phase, wc)) { ok = false; break; }
         const uint8_t* st = stages + stage * C::STAGE_BYTES;
-        for (int j = 0; j < kSubPerStage; ++j, ++g) {
+        for (int j = 0; j < kTc4KS / C::SUB; ++j, ++g) {
           const int ab = g & 1;
           if (!warp_wait(&aempty[ab], ((g >> 1) & 1) ^ 1, wc)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int m = 0; m < NM; ++m) {
-            // this row's 64 codes of sub-step j: 16-byte pieces 2j and 2j + 1,
-            // stored at piece ^ (r % 8) by the 128-byte swizzle
-            const uint8_t* rowp = st + m * C::A_BYTES + r * 128;
-            const uint4 c0 = *reinterpret_cast<const uint4*>(rowp + (((2 * j) ^ (r & 7)) << 4));
-            const uint4 c1 = *reinterpret_cast<const uint4*>(rowp + (((2 * j + 1) ^ (r & 7)) << 4));
-            const uint32_t sw = *reinterpret_cast<const uint32_t*>(st + C::S_OFF + m * C::S_BYTES + r * 16 + 4 * j);
-            uint32_t s01, s23;
-            e4m3x4_f16x2(sw, s01, s23);
-            const uint32_t sb[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint32_t v[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {            // word i: codes 8i .. 8i + 7, block i / 2
-              uint32_t h[4];
-              e2m1x8_f16x2(cw[i], h);
+            for (int c64 = 0; c64 < C::SUB / 64; ++c64) {
+              // this row's 64 codes of values 64 q64 .. + 63 (q64 = j SUB / 64 + c64
+              // of the stage): 16-byte pieces 2 q64 and 2 q64 + 1, stored at
+              // piece ^ (r % 8) by the 128-byte swizzle
+              const int q64 = j * (C::SUB / 64) + c64;
+              const uint8_t* rowp = st + m * C::A_BYTES + r * 128;
+              const uint4 c0 = *reinterpret_cast<const uint4*>(rowp + (((2 * q64) ^ (r & 7)) << 4));
+              const uint4 c1 = *reinterpret_cast<const uint4*>(rowp + (((2 * q64 + 1) ^ (r & 7)) << 4));
+              const uint32_t sw =
+                  *reinterpret_cast<const uint32_t*>(st + C::S_OFF + m * C::S_BYTES + r * 16 + 4 * q64);
+              uint32_t s01, s23;
+              e4m3x4_f16x2(sw, s01, s23);
+              const uint32_t sb4[4] = {dup_lo(s01), dup_hi(s01), dup_lo(s23), dup_hi(s23)};
+              const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+              uint32_t v[32];
 #pragma unroll
-              for (int c = 0; c < 4; ++c) v[4 * i + c] = hmul2(h[c], sb[i >> 1]);
+              for (int i = 0; i < 8; ++i) {          // word i: codes 8i .. 8i + 7, block i / 2
+                uint32_t h[4];
+                e2m1x8_f16x2(cw[i], h);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[4 * i + c] = hmul2(h[c], sb4[i >> 1]);
+              }
+              tmem_st32(tmem_a + ((uint32_t)(q * 32) << 16) + ab * C::A_COLS + m * (C::SUB / 2) + c64 * 32, v);
             }
-            tmem_st32(tmem_a + ((uint32_t)(q * 32) << 16) + ab * C::A_COLS + m * (kSub / 2), v);
           }
           tmem_st_wait();
           tc_fence_before();
