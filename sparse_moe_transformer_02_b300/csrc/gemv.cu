@@ -53,20 +53,9 @@ static_assert(kStages % kConsumers == 0, "a ring stage must belong to exactly on
 
 template <int WF> struct Fmt;
 template <> struct Fmt<MOE_F32>   { static constexpr int EPC = 4;  static constexpr int XB = 16; };
-template <> struct Fmt<MOE_BF16>  { static constexpr int EPC = 8;  static constexpr int XB = 16; };
 template <> struct Fmt<MOE_NVFP4> { static constexpr int EPC = 32; static constexpr int XB = 64; };
-// EPC: elements per 16-byte weight chunk; XB: bytes of activations matching one chunk.
-
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-// Two e4m3 codes (low byte first) -> two floats.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
-}
+// EPC: elements per 16-byte weight chunk; XB: bytes of activations matching one chunk
+// (bf16 weights use the tensor-pipe GEMV kernels further down).
 
 // Activations matching one weight chunk, held in registers.
 template <int WF> struct XChunk { uint4 v[Fmt<WF>::XB / 16]; };

@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_large_kernel(RouteArgs a)
   route_entry();
   extern __shared__ __align__(16) float dsm[];
   const int E = a.E, d = a.d, T = a.T, k = a.k;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = blockIdx.x * kLargeBT;
   const int Ep = EJ * 128;                  // E rounded up to 128
   float* xs = dsm;                          // [32 tok][32 kk]
