@@ -60,9 +60,11 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
 
 /* Which expert-FFN kernels moe_forward uses. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* tcgen05 grouped GEMM when the weights allow it (bf16), else the GEMV kernels */
+  MOE_PATH_AUTO = 0,   /* tcgen05 grouped GEMM when the weights allow it, else the GEMV kernels */
   MOE_PATH_GEMV = 1,   /* always the weight-streaming GEMV kernels */
-  MOE_PATH_TC = 2      /* always the tcgen05 grouped GEMM (bf16 weights and activations only) */
+  MOE_PATH_TC = 2      /* always the tcgen05 grouped GEMM: bf16 activations with bf16 weights (d, F, F_s
+                          multiples of 128) or NVFP4 weights (multiples of 256; the codes are decoded into
+                          tensor memory and x and h are carried in f16 with exact power-of-two scales) */
 } moe_path;
 
 typedef struct {
@@ -190,7 +192,8 @@ typedef enum {
   MOE_K_ROUTE = 0,         /* router + top-k + grouping */
   MOE_K_GEMV_GATEUP = 1,   /* weight-streaming gate/up + SwiGLU */
   MOE_K_GEMV_DOWN = 2,     /* weight-streaming down + gated combine */
-  MOE_K_TC_GATHER = 3,     /* slot-ordered copy of routed activations */
+  MOE_K_TC_GATHER = 3,     /* slot-ordered copy of the activations (f16 with scales for NVFP4 weights);
+                              after a large-batch router also the slots' grouped positions */
   MOE_K_TC_GATEUP = 4,     /* tcgen05 gate/up + SwiGLU */
   MOE_K_TC_DOWN = 5,       /* tcgen05 down + gated accumulate */
   MOE_K_TC_FINALIZE = 6,   /* fp32 accumulator -> output */
