@@ -34,6 +34,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "units.cuh"
 
 namespace moe {
 namespace {
@@ -593,11 +594,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
 // slot], one warp per slot.  After a large-batch router (wpb > 0) the warp
 // also places the slot: it computes the grouped position of slot s = (t, j)
 // from the selection bitmap and writes tok_of_slot, src_of_slot and slot_of.
+// First the grid writes the unit lists of both passes.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const __nv_bfloat16* __restrict__ x,
                                                         const int32_t* __restrict__ idx, Workspace ws, int T,
-                                                        int E, int k, int d, int wpb) {
+                                                        int E, int k, int d, int wpb, UnitBuild ub) {
   pdl_launch_dependents();
   pdl_wait();
+  build_unit_lists(ws, ub);
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
   const int per_row = d / 8;                       // 16-byte pieces per row
@@ -617,7 +620,16 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(const __nv_bfloat16* __r
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)pos * d);
-    for (int c = lane; c < per_row; c += 32) dst[c] = __ldg(src + c);
+    // eight 16-byte loads in flight per lane before the stores
+    for (int c0 = 0; c0 < per_row; c0 += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i + lane < per_row) v[i] = __ldg(src + c0 + 32 * i + lane);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i + lane < per_row) dst[c0 + 32 * i + lane] = v[i];
+    }
   }
 }
 
@@ -741,9 +753,15 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   // slot-ordered copy of the routed activations
   const int slots = a.T * a.k;
   const int gg = (slots + 7) / 8 < num_sms * 8 ? (slots + 7) / 8 : num_sms * 8;   // 8 warps per block
+  UnitBuild ub;
+  ub.E = a.E; ub.T = a.T; ub.tn = kTcBN;
+  ub.sh_tb = a.Fs > 0 ? (a.T + kTcBN - 1) / kTcBN : 0;
+  ub.mt[0] = a.F / kTcBM; ub.mt[1] = a.d / a.dn_rows;
+  ub.sh_mt[0] = a.Fs > 0 ? a.Fs / kTcBM : 0; ub.sh_mt[1] = a.d / a.dn_rows;
+  ub.rep[0] = a.gu_split; ub.rep[1] = 1;
   if (prof) prof->begin(MOE_K_TC_GATHER, s);
   cudaError_t e = launch_ex(tc_gather_kernel, gg > 0 ? gg : 1, 256, 0, s, static_cast<const __nv_bfloat16*>(a.x),
-                            a.idx, a.ws, a.T, a.E, a.k, a.d, a.wpb);
+                            a.idx, a.ws, a.T, a.E, a.k, a.d, a.wpb, ub);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // pass 1: gate/up

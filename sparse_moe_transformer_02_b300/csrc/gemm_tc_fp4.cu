@@ -37,6 +37,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "units.cuh"
 
 namespace moe {
 namespace {
@@ -429,12 +430,14 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
 // grouped slot s, row T k + t is token t (the shared expert's operand).  Each
 // row is scaled by 2^-e (its largest magnitude into [1, 2)) and xs[row] = 2^e.
 // One warp per row.  After a large-batch router (wpb > 0) the warp also places
-// the slot (tok_of_slot, src_of_slot, slot_of).
+// the slot (tok_of_slot, src_of_slot, slot_of).  First the grid writes the
+// unit lists of both passes.
 __global__ void __launch_bounds__(256) tc4_gather_kernel(const __nv_bfloat16* __restrict__ x,
                                                          const int32_t* __restrict__ idx, Workspace ws, int T, int E,
-                                                         int k, int d, int wpb) {
+                                                         int k, int d, int wpb, UnitBuild ub) {
   pdl_launch_dependents();
   pdl_wait();
+  build_unit_lists(ws, ub);
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
   const int per_row = d / 8;                       // 16-byte pieces of bf16
@@ -522,9 +525,15 @@ cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof
   // f16 activation rows (and slot placement after a large-batch router)
   const int rows = a.T * (a.k + 1);
   const int gg = (rows + 7) / 8 < num_sms * 8 ? (rows + 7) / 8 : num_sms * 8;   // 8 warps per block
+  UnitBuild ub;   // NVFP4 tiles: 128 weight rows, kTc4BN tokens, no split
+  ub.E = a.E; ub.T = a.T; ub.tn = kTc4BN;
+  ub.sh_tb = a.Fs > 0 ? (a.T + kTc4BN - 1) / kTc4BN : 0;
+  ub.mt[0] = a.F / 128; ub.mt[1] = a.d / 128;
+  ub.sh_mt[0] = a.Fs > 0 ? a.Fs / 128 : 0; ub.sh_mt[1] = a.d / 128;
+  ub.rep[0] = 1; ub.rep[1] = 1;
   if (prof) prof->begin(MOE_K_TC_GATHER, s);
   cudaError_t e = launch_pdl(tc4_gather_kernel, gg > 0 ? gg : 1, 256, 0, s,
-                             static_cast<const __nv_bfloat16*>(a.x), a.idx, a.ws, a.T, a.E, a.k, a.d, a.wpb);
+                             static_cast<const __nv_bfloat16*>(a.x), a.idx, a.ws, a.T, a.E, a.k, a.d, a.wpb, ub);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
 

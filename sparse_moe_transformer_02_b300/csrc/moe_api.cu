@@ -403,6 +403,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.units_gu, (size_t)(h->max_units_gu > 0 ? h->max_units_gu : 1) * sizeof(TcUnit)},
       {(void**)&ws.units_dn, (size_t)(h->max_units_dn > 0 ? h->max_units_dn : 1) * sizeof(TcUnit)},
       {(void**)&ws.n_units, 2 * 4},
+      {(void**)&ws.uprefix, (size_t)2 * (E + 1) * 4},
       {(void**)&ws.h32, Tg * (k + 1) * Fmax * 4},
       {(void**)&ws.h16, (h->tc_capable ? Tm : Tg) * (k + 1) * Fmax * 2},
       {(void**)&ws.xp, h->tc_capable ? Tm * (h->fp4 ? k + 1 : k) * d * 2 : 16},

@@ -29,7 +29,7 @@ constexpr unsigned kErrRange = 1u << 6;     // an f16 intermediate saturated (NV
 
 // One unit of tcgen05 work: expert (E = the shared expert), weight-row tile,
 // first slot (for the shared expert: first token) and token count (<= kTcBN).
-struct TcUnit {
+struct __align__(16) TcUnit {   // one 16-byte load or store
   int32_t expert, m_tile, slot0, n;
 };
 
@@ -50,6 +50,7 @@ struct Workspace {
   TcUnit* units_gu;       // tcgen05 gate/up units
   TcUnit* units_dn;       // tcgen05 down units
   int32_t* n_units;       // [2] unit counts (gate/up, down)
+  int32_t* uprefix;       // [2][E + 1] first unit-list entry of each routed expert after the shared ones
   float* h32;             // [min(max_T, kGemvChunkT) * (k + 1)][F_max] GEMV intermediate
   __nv_bfloat16* h16;     // [max(max_T, ...) * (k + 1)][F_max] bf16 intermediate (tcgen05 and bf16 GEMV)
   __nv_bfloat16* xp;      // tcgen05 slot-ordered copy of the activations: bf16 [max_T * k][d], or for

@@ -216,8 +216,8 @@ __device__ int block_exclusive_scan(int* a, int n) {
   return total;
 }
 
-// Everything after the counts are known: offsets, active-expert list, tcgen05
-// unit lists.  cnt: smem [E] counts; offs: smem [E + 1].  Runs in one CTA.
+// Everything after the counts are known: offsets, active-expert list, the
+// per-expert first entries of the tcgen05 unit lists.  cnt: smem [E] counts; offs: smem [E + 1].  Runs in one CTA.
 __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* scratch) {
   const int E = a.E, tid = threadIdx.x;
   for (int e = tid; e < E; e += blockDim.x) offs[e] = cnt[e];
@@ -241,7 +241,8 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
   }
   __syncthreads();
   if (!a.build_tc_units) return;
-  // tcgen05 units: shared expert first, then routed experts in index order.
+  // tcgen05 unit lists: per list, the first entry of every routed expert
+  // after the shared expert's entries (the gather kernel writes the entries)
   const int mt_gu = a.F / kTcBM, mt_dn = a.d / a.dn_rows, tn = a.tile_n;
   const int sh_tb = a.has_shared ? (a.T + tn - 1) / tn : 0;
   const int sh_mt_gu = a.has_shared ? a.Fs / kTcBM : 0;
@@ -249,23 +250,14 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
     const int mt = pass == 0 ? mt_gu : mt_dn;
     const int sh_mt = pass == 0 ? sh_mt_gu : mt_dn;
     const int rep = pass == 0 ? a.gu_split : 1;   // gate/up tiles split along K: one entry per part
-    TcUnit* out = pass == 0 ? a.ws.units_gu : a.ws.units_dn;
     for (int e = tid; e < E; e += blockDim.x) scratch[e] = rep * mt * ((cnt[e] + tn - 1) / tn);
     __syncthreads();
     const int n_routed = block_exclusive_scan(scratch, E);
-    const int sh_units = rep * sh_mt * sh_tb;
-    for (int u = tid; u < sh_units; u += blockDim.x) {
-      const int base = u / rep, tb = base / sh_mt, m = base % sh_mt;
-      out[u] = TcUnit{E, m, tb * tn, min(tn, a.T - tb * tn)};
+    for (int e = tid; e < E; e += blockDim.x) a.ws.uprefix[pass * (E + 1) + e] = scratch[e];
+    if (tid == 0) {
+      a.ws.uprefix[pass * (E + 1) + E] = n_routed;
+      a.ws.n_units[pass] = rep * sh_mt * sh_tb + n_routed;
     }
-    for (int e = tid; e < E; e += blockDim.x) {
-      const int c = cnt[e];
-      int u = sh_units + scratch[e];
-      for (int tb = 0; tb * tn < c; ++tb)
-        for (int m = 0; m < mt; ++m)
-          for (int r = 0; r < rep; ++r) out[u++] = TcUnit{e, m, offs[e] + tb * tn, min(tn, c - tb * tn)};
-    }
-    if (tid == 0) a.ws.n_units[pass] = sh_units + n_routed;
     __syncthreads();
   }
 }
@@ -274,7 +266,7 @@ __device__ void finish_grouping(const RouteArgs& a, int* cnt, int* offs, int* sc
 // (wpb selection-bitmap words per expert and block; sel[w][e] bit t % 32 is
 // set when token 32 w + t % 32 chose expert e) and bcnt[b][e] is block b's
 // count for expert e.  One CTA turns the counts into offsets, the active list
-// and the unit lists, and stores the exclusive prefix of the block counts in
+// and the unit-list prefixes, and stores the exclusive prefix of the block counts in
 // bpref[b][e]; the per-slot placement (slot_position) runs afterwards, in
 // parallel, in whichever kernel needs it.
 __device__ void group_from_counts(const RouteArgs& a, int nblk) {
