@@ -40,6 +40,11 @@ namespace moe {
 namespace {
 
 constexpr int kThreadsTc = 192;
+// Down pass: units are claimed from a grid-wide counter (a CTA that started
+// late, after a long gate/up tile, takes fewer of them) and handed from the
+// producer warp to the MMA thread and the epilogue warps through a ring of
+// kRing entries in shared memory.
+constexpr int kRing = 8;
 
 template <int MODE> struct TcCfg;
 constexpr int kRedCols = 64;     // token-major down pass: columns per bulk reduction (256 bytes)
@@ -102,6 +107,7 @@ struct TcParams {
   // sums to gu_part[part]; the last part to finish a warp's rows (gu_cnt)
   // adds the parts in order (deterministic) and writes h.
   int ksplit;
+  unsigned int* sched;          // down pass: next unit to claim (kept at zero between calls)
   int P;                        // rows of h (T (k + 1))
   float* gu_part;
   unsigned int* gu_cnt;
@@ -149,6 +155,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* col_tok = abort_flag + 3;                               // [4 warps][kTcBN] token of each column (pass 2)
   float* col_gate = reinterpret_cast<float*>(col_tok + 4 * kTcBN);   // [4 warps][kTcBN] its gate
+  uint64_t* ufull = reinterpret_cast<uint64_t*>(col_gate + 4 * kTcBN);   // [kRing] unit posted (pass 2)
+  uint64_t* uempty = ufull + kRing;                                        // [kRing] unit taken by all roles
+  TcUnit* ring = reinterpret_cast<TcUnit*>(uempty + kRing);                // [kRing]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -160,6 +169,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 128);
     }
+    if (MODE >= 1)
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&ufull[i], 1);
+        mbar_init(&uempty[i], 5);     // the MMA thread and the four epilogue warps
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -211,15 +225,57 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     }
     UnitCursor cur;
     bool gu_done = false;                  // down pass: every gate/up tile seen finished
-    for (int u = blockIdx.x; ok; u += gridDim.x) {
-      if (u >= n_total) {
-        if (waited) break;
-        wait_routing();
-        waited = true;
-        n_total = __ldcg(p.n_units + LIST);
-        if (u >= n_total) break;
+    // down pass: while a unit's loads are issued, the next unit's descriptor
+    // load and the claim of the one after it are in flight.  With few units
+    // per CTA (small batches) a CTA claims its next unit only when it is done
+    // issuing the current one, so that the first CTAs to start do not take
+    // two units each while other SMs have none.
+    int u = blockIdx.x, claim = 0;
+    const bool ahead = n_total > 2 * (int)gridDim.x;
+    TcUnit un_nx{-1, 0, 0, 0};
+    if (MODE >= 1 && ok) {
+      if (lane == 0) claim = (int)atomicAdd(p.sched, 1u);
+      u = __shfl_sync(0xFFFFFFFFu, claim, 0);
+      if (u < n_total) un_nx = get_unit(p, u);
+      if (ahead && lane == 0 && u < n_total) claim = (int)atomicAdd(p.sched, 1u);
+    }
+    for (int it = 0; ok; ++it) {
+      TcUnit un;
+      if constexpr (MODE == 0) {
+        if (it > 0) u += gridDim.x;
+        if (u >= n_total) {
+          if (waited) break;
+          wait_routing();
+          waited = true;
+          n_total = __ldcg(p.n_units + LIST);
+          if (u >= n_total) break;
+        }
+        un = cur.get(p, u, n_total);
+      } else {
+        if (it > 0 && !ahead) {
+          if (lane == 0) claim = (int)atomicAdd(p.sched, 1u);
+          const int u_nx = __shfl_sync(0xFFFFFFFFu, claim, 0);
+          un_nx = TcUnit{-1, 0, 0, 0};
+          if (u_nx < n_total) un_nx = get_unit(p, u_nx);
+        }
+        un = un_nx;
+        // post the unit (or the end mark) to the other roles
+        const int slot = it % kRing;
+        if (!warp_wait(&uempty[slot], ((it / kRing) & 1) ^ 1, wc)) { ok = false; break; }
+        if (lane == 0) {
+          ring[slot] = un;
+          mbar_arrive(&ufull[slot]);
+        }
+        __syncwarp();
+        if (un.expert < 0) break;
+        if (ahead) {
+          const int u_nx = __shfl_sync(0xFFFFFFFFu, claim, 0);
+          un_nx = TcUnit{-1, 0, 0, 0};
+          if (u_nx < n_total) un_nx = get_unit(p, u_nx);
+          if (lane == 0 && u_nx < n_total) claim = (int)atomicAdd(p.sched, 1u);
+        }
+        u = 0;
       }
-      const TcUnit un = cur.get(p, u, n_total);
       const bool sh = un.expert == p.E;
       const int K = sh ? p.Ks : p.K;
       const int kb = K / kTcBK, part = u % p.ksplit;
@@ -285,15 +341,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
       uint64_t* last_commit = nullptr;
       uint32_t last_commit_par = 0;
       UnitCursor cur;
-      for (int u = blockIdx.x; ok; u += gridDim.x) {
-        if (u >= n_total) {
-          if (waited) break;
-          wait_routing();
-          waited = true;
-          n_total = __ldcg(p.n_units + LIST);
-          if (u >= n_total) break;
+      int u = blockIdx.x;
+      for (int it = 0; ok; ++it) {
+        TcUnit un;
+        if constexpr (MODE == 0) {
+          if (it > 0) u += gridDim.x;
+          if (u >= n_total) {
+            if (waited) break;
+            wait_routing();
+            waited = true;
+            n_total = __ldcg(p.n_units + LIST);
+            if (u >= n_total) break;
+          }
+          un = cur.get(p, u, n_total);
+        } else {
+          const int slot = it % kRing;
+          if (!mbar_wait(&ufull[slot], (it / kRing) & 1, wc)) { ok = false; break; }
+          un = ring[slot];
+          mbar_arrive(&uempty[slot]);
+          if (un.expert < 0) break;
+          u = 0;
         }
-        const TcUnit un = cur.get(p, u, n_total);
         const bool sh = un.expert == p.E;
         const int n_pad = (un.n + 15) & ~15;
         const int K = sh ? p.Ks : p.K;
@@ -359,15 +427,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     bool waited = MODE >= 1;
     if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
     UnitCursor cur;
-    for (int u = blockIdx.x;; u += gridDim.x) {
-      if (u >= n_total) {
-        if (waited) break;
-        wait_routing();
-        waited = true;
-        n_total = __ldcg(p.n_units + LIST);
-        if (u >= n_total) break;
+    int u = blockIdx.x;
+    for (int it = 0;; ++it) {
+      TcUnit un;
+      if constexpr (MODE == 0) {
+        if (it > 0) u += gridDim.x;
+        if (u >= n_total) {
+          if (waited) break;
+          wait_routing();
+          waited = true;
+          n_total = __ldcg(p.n_units + LIST);
+          if (u >= n_total) break;
+        }
+        un = cur.get(p, u, n_total);
+      } else {
+        const int slot = it % kRing;
+        if (!warp_wait(&ufull[slot], (it / kRing) & 1, wc)) break;
+        un = ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&uempty[slot]);
+        if (un.expert < 0) break;
+        u = 0;
       }
-      const TcUnit un = cur.get(p, u, n_total);
       const bool sh = un.expert == p.E;
       const int n_pad = (un.n + 15) & ~15;
       if (MODE == 1) {
@@ -671,7 +752,8 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restric
 template <int MODE>
 size_t tc_smem_bytes() {
   using C = TcCfg<MODE>;
-  return 1024 + C::STAGES * C::STAGE_BYTES + TcStaging<MODE>::BYTES + (2 * C::STAGES + 4) * 8 + 16 + 8 * kTcBN * 4;
+  return 1024 + C::STAGES * C::STAGE_BYTES + TcStaging<MODE>::BYTES + (2 * C::STAGES + 4) * 8 + 16 + 8 * kTcBN * 4 +
+         kRing * (16 + sizeof(TcUnit));
 }
 
 template <typename... KArgs, typename... Args>
@@ -750,6 +832,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.gu_cnt = a.ws.gu_cnt;
   p.mt_gu = a.F / kTcBM;
   p.mt_gu_s = a.Fs > 0 ? a.Fs / kTcBM : 1;
+  p.sched = nullptr;
   // slot-ordered copy of the routed activations
   const int slots = a.T * a.k;
   const int gg = (slots + 7) / 8 < num_sms * 8 ? (slots + 7) / 8 : num_sms * 8;   // 8 warps per block
@@ -793,6 +876,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.mt_s = a.d / a.dn_rows;
   p.n_pre = 0;
   p.ksplit = 1;
+  p.sched = a.ws.ready + a.E + 3;
   p.units = a.ws.units_dn;
   const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
   if (prof) prof->begin(MOE_K_TC_DOWN, s);
@@ -804,7 +888,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 3,
+  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 4,
                             num_sms, s, prof);
 }
 

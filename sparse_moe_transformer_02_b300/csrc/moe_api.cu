@@ -416,7 +416,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.wr_split, h->rtc_capable ? 3 * E * d * 2 : 16},
       {(void**)&ws.cand, h->rtc_capable ? Tm * (E / 64) * kMaxTopK * 8 : 16},
       {(void**)&ws.fin, Tg * (d / kFinRows) * 4},
-      {(void**)&ws.ready, (E + 3) * 4},
+      {(void**)&ws.ready, (E + 4) * 4},
       {(void**)&ws.gu_part, h->max_tiles_small > 0 ? (size_t)kMaxKSplit * (Tm < (size_t)kSmallT ? Tm : (size_t)kSmallT) * (k + 1) * 2 * Fmax * 4 : 16},
       {(void**)&ws.gu_cnt, (size_t)(h->max_tiles_small > 0 ? h->max_tiles_small : 1) * 4 * 4},
       {(void**)&ws.err, 16},
@@ -441,7 +441,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   cudaError_t e = cudaMemsetAsync(ws.counters, 0, (size_t)h->n_counters * 4, stream);
   if (e == cudaSuccess && h->rtc_capable) e = launch_router_split(w->router_w, ws.wr_split, E * d, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.fin, 0, Tg * (d / kFinRows) * 4, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws.ready, 0, (E + 3) * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.ready, 0, (E + 4) * 4, stream);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(ws.gu_cnt, 0, (size_t)(h->max_tiles_small > 0 ? h->max_tiles_small : 1) * 4 * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws.err, 0, 16, stream);

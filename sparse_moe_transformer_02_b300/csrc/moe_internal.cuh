@@ -66,9 +66,10 @@ struct Workspace {
   uint32_t* fin;          // [kGemvChunkT][d / 32] GEMV down completion counts (kept at zero between calls)
   float* gu_part;         // [kMaxKSplit][min(max_T, 64) * (k + 1)][2][F_max] partial gate/up sums (split tiles)
   uint32_t* gu_cnt;       // [4 per gate/up tile] arrivals of a split tile's parts (kept at zero between calls)
-  uint32_t* ready;        // [E + 3] tcgen05 gate/up progress (kept at zero between calls): [e] finished
+  uint32_t* ready;        // [E + 4] tcgen05 gate/up progress (kept at zero between calls): [e] finished
                           // tile quarters of expert e ([E] = the shared expert), [E + 1] CTA quarters
-                          // done clearing y_acc, [E + 2] CTA quarters done with all their tiles
+                          // done clearing y_acc, [E + 2] CTA quarters done with all their tiles;
+                          // [E + 3] the down pass's next unit to claim
   unsigned int* err;      // device error word
   void* x_stage;          // [max_T][d] moe_forward_host staging
   void* y_stage;
