@@ -192,8 +192,9 @@ typedef enum {
   MOE_K_ROUTE = 0,         /* router + top-k + grouping */
   MOE_K_GEMV_GATEUP = 1,   /* weight-streaming gate/up + SwiGLU */
   MOE_K_GEMV_DOWN = 2,     /* weight-streaming down + gated combine */
-  MOE_K_TC_GATHER = 3,     /* slot-ordered copy of the activations (f16 with scales for NVFP4 weights);
-                              after a large-batch router also the slots' grouped positions */
+  MOE_K_TC_GATHER = 3,     /* tcgen05 unit lists, slot-ordered copy of the activations (f16 with scales
+                              for NVFP4 weights); after a large-batch router also the slots' grouped
+                              positions */
   MOE_K_TC_GATEUP = 4,     /* tcgen05 gate/up + SwiGLU */
   MOE_K_TC_DOWN = 5,       /* tcgen05 down + gated accumulate */
   MOE_K_TC_FINALIZE = 6,   /* fp32 accumulator -> output */
