@@ -68,7 +68,7 @@ typedef enum {
 } moe_path;
 
 typedef struct {
-  int32_t d;             /* hidden width; multiple of 64 */
+  int32_t d;             /* hidden width; multiple of 64, at most 6400 */
   int32_t ffn;           /* routed expert FFN width F; multiple of 64 */
   int32_t shared_ffn;    /* shared expert FFN width F_s (multiple of 64), 0 = no shared expert */
   int32_t num_experts;   /* E, 1..512 */
@@ -136,17 +136,37 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
 moe_status moe_destroy(moe_handle h);
 
 /*
- * Routing only.  x [T][d] (act_dtype), 16-byte aligned.  Writes idx [T][k]
- * int32 (larger gate first) and gate [T][k] fp32 (required), and counts [E]
- * int32 = tokens routed to each expert (optional, NULL to skip).
+ * Routing only: the gating network that scores each token against the routed
+ * experts and keeps a few of them (kongchang.com, section "Architecture: The
+ * 40B Total vs. 2.5B Active Trade-off"), 6 of 256 per token in Flint
+ * (evermx.com review, Feature Overview, "Sparse architecture").  The router
+ * function, tie rule and renormalisation are this library's readings (top of
+ * this file).
+ *
+ * x [T][d] (act_dtype), 16-byte aligned.  Writes idx [T][k] int32 (larger
+ * gate first) and gate [T][k] fp32 (required), and counts [E] int32 = tokens
+ * routed to each expert (optional, NULL to skip).  All buffers are
+ * caller-owned device memory.  Errors: MOE_ERR_INVALID_ARG for a NULL handle,
+ * x, idx or gate, T < 0 or T > max_tokens, or misaligned pointers (checked
+ * before any launch); MOE_ERR_CUDA if a launch fails.
  */
 moe_status moe_route(moe_handle h, const void* x, int32_t T, int32_t* idx, float* gate,
                      int32_t* counts, cudaStream_t stream);
 
 /*
- * Full layer.  x [T][d] and y [T][d] in act_dtype, 16-byte aligned, not
- * overlapping.  idx_out [T][k] and gate_out [T][k] receive the routing when
- * non-NULL.  T <= max_tokens.
+ * Full layer: routing as in moe_route, each selected expert and the
+ * always-active shared expert on the token (evermx.com review, Feature
+ * Overview, "Sparse architecture"; futurpulse.com, section "How does Flint use
+ * 39.8B parameters efficiently?"), gate-weighted sum, and the residual add
+ * that joins the 47 MoE layers when add_residual is set (swarmz.net, section
+ * "The architecture, in plain terms").
+ *
+ * x [T][d] and y [T][d] in act_dtype, caller-owned device memory, 16-byte
+ * aligned, not overlapping.  idx_out [T][k] and gate_out [T][k] receive the
+ * routing when non-NULL.  T <= max_tokens.  Errors: MOE_ERR_INVALID_ARG for a
+ * NULL handle or buffer, T out of range, misalignment or overlapping x and y
+ * (checked before any launch); MOE_ERR_CUDA if a launch fails.  Device-side
+ * timeouts and f16 saturation show up in moe_check.
  */
 moe_status moe_forward(moe_handle h, const void* x, int32_t T, void* y, int32_t* idx_out,
                        float* gate_out, cudaStream_t stream);
@@ -162,7 +182,10 @@ moe_status moe_forward_host(moe_handle h, const void* x_host, int32_t T, void* y
 
 /*
  * The token-slot grouping of the last moe_route / moe_forward call on this
- * handle (with the same T): offsets [E+1] (exclusive scan of counts),
+ * handle (with the same T).  Grouping token-slots by expert is the scheduling
+ * step the pages single out for MoE throughput (kongchang.com, section
+ * "Architecture: The 40B Total vs. 2.5B Active Trade-off"; uneven expert use:
+ * futurpulse.com, section "How does Flint use 39.8B parameters efficiently?"): offsets [E+1] (exclusive scan of counts),
  * tok_of_slot [T*k] (token of each grouped slot; slots of one expert are
  * contiguous and in (token, j) order) and slot_of [T][k] (grouped position
  * of slot (t, j)).  Any output may be NULL.  Enqueued on `stream`.
@@ -186,6 +209,16 @@ moe_status moe_check(moe_handle h, cudaStream_t stream);
  * moe_check then reports it.  The GPU is not hung and the context stays usable.
  */
 moe_status moe_debug_expire_wait(moe_handle h, int32_t timeout_us, cudaStream_t stream);
+
+/*
+ * Failure injection (no counterpart on the pages; test support): from now on
+ * the nth device allocation the library makes (counting from 1) fails as if
+ * the device were out of memory; nth == 0 switches injection off.  The count
+ * is process-wide.  Lets a test check that moe_create reports MOE_ERR_OOM
+ * and holds nothing afterwards, without exhausting a GPU.  nth < 0 returns
+ * MOE_ERR_INVALID_ARG.
+ */
+moe_status moe_debug_fail_alloc(int32_t nth);
 
 /* Kernels of the layer, as counted by the profiling calls below. */
 typedef enum {
@@ -231,15 +264,17 @@ moe_status moe_profile_read(moe_handle h, float* ms, int32_t* launches);
  * MOE_F32 or MOE_BF16, 16-byte aligned), router_w [E][d] fp32 (16-byte
  * aligned) and router_b [E] fp32 or NULL.
  *
- * Limits: 1 <= T <= 64, E <= 512, k <= 8 (k <= E), d a multiple of 64; larger
- * sizes return MOE_ERR_INVALID_ARG.  Scratch lives in one fixed array of about
+ * Limits: 1 <= T <= 64, E <= 512, k <= 8 (k <= E), d a multiple of 64 and at
+ * most 6400; larger sizes return MOE_ERR_INVALID_ARG.  Scratch lives in one fixed array of about
  * 144 KiB inside the library's device image; every device that loads the
  * library holds it until the process exits.  The first call on a device looks
  * up that array's device address (cudaGetSymbolAddress) once, so make the
  * first call on each device before any stream capture.  All calls share the
  * array and it keeps the last call's contents: calls that overlap on the GPU
  * (other streams, other host threads) race and must be serialised.  Calls no
- * cudaMalloc, cudaFree or allocating library routine.
+ * cudaMalloc, cudaFree or allocating library routine.  The address is cached
+ * for the life of the process: after a cudaDeviceReset of a device, do not
+ * call this function on that device again.
  */
 moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int32_t num_experts, int32_t top_k,
                              int32_t act_dtype, const float* router_w, const float* router_b,

@@ -20,7 +20,7 @@ MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_TC = 0, 1, 2
 
 EXPORTED = ["moe_status_string", "moe_create", "moe_destroy", "moe_route", "moe_forward",
             "moe_forward_host", "moe_get_grouping", "moe_check", "moe_debug_expire_wait",
-            "moe_profile_enable", "moe_profile_read", "moe_route_noalloc"]
+            "moe_profile_enable", "moe_profile_read", "moe_route_noalloc", "moe_debug_fail_alloc"]
 KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize"]
 
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_enable.argtypes = [vp, i32, i32]
         L.moe_profile_read.restype = ctypes.c_int
         L.moe_profile_read.argtypes = [vp, vp, vp]
+        L.moe_debug_fail_alloc.restype = ctypes.c_int
+        L.moe_debug_fail_alloc.argtypes = [i32]
         L.moe_route_noalloc.restype = ctypes.c_int
         L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
@@ -125,6 +127,11 @@ def moe_check(h, stream: int = 0) -> int:
 
 def moe_debug_expire_wait(h, timeout_us: int, stream: int = 0) -> int:
     return lib().moe_debug_expire_wait(h, timeout_us, stream)
+
+
+def moe_debug_fail_alloc(nth: int) -> int:
+    """Make the library's nth device allocation from now on fail (0 = off)."""
+    return lib().moe_debug_fail_alloc(int(nth))
 
 
 def moe_profile_enable(h, enable: int, max_launches: int = 4096) -> int:

@@ -800,18 +800,12 @@ cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t
 }
 
 cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc_smem_bytes<0>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<1>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<2>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<3>());
+  {
+    cudaError_t e = ensure_smem_limit(tc_kernel<0>, (int)tc_smem_bytes<0>());
+    if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<1>, (int)tc_smem_bytes<1>());
+    if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<2>, (int)tc_smem_bytes<2>());
+    if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<3>, (int)tc_smem_bytes<3>());
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int Fmax = a.F > a.Fs ? a.F : a.Fs;
   TcParams p;

@@ -513,14 +513,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t sme
 }  // namespace
 
 cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc4_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc4_smem_bytes<0>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc4_smem_bytes<1>());
+  {
+    cudaError_t e = ensure_smem_limit(tc4_kernel<0>, (int)tc4_smem_bytes<0>());
+    if (e == cudaSuccess) e = ensure_smem_limit(tc4_kernel<1>, (int)tc4_smem_bytes<1>());
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   // f16 activation rows (and slot placement after a large-batch router)
   const int rows = a.T * (a.k + 1);

@@ -890,13 +890,10 @@ cudaError_t launch_pdl(K kernel, int grid, cudaStream_t s, const GemvArgs& a, ui
 }
 
 cudaError_t launch_mma(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
-  static bool attr_set = false;   // set once, before any stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_mma_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  {
+    cudaError_t e = ensure_smem_limit(gemv_mma_gateup_kernel, (int)kSmem);
+    if (e == cudaSuccess) e = ensure_smem_limit(gemv_mma_down_kernel, (int)kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   if (prof) prof->begin(MOE_K_GEMV_GATEUP, s);
   cudaError_t e = launch_pdl(gemv_mma_gateup_kernel, num_sms, s, a, wait_ns);
@@ -952,14 +949,10 @@ __global__ void __launch_bounds__(256) gemv_x16_kernel(const __nv_bfloat16* __re
 
 template <int WF, int J, int CPR>
 cudaError_t launch_fmt(const GemvArgs& a, int num_sms, cudaStream_t s, Prof* prof, uint64_t wait_ns) {
-  static bool attr_set = false;   // set once, before any stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_gateup_kernel<WF, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_down_kernel<WF, CPR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  {
+    cudaError_t e = ensure_smem_limit(gemv_gateup_kernel<WF, J>, (int)kSmem);
+    if (e == cudaSuccess) e = ensure_smem_limit(gemv_down_kernel<WF, CPR>, (int)kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaError_t e = cudaSuccess;
   if (WF == MOE_NVFP4) {

@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/moe.h: argument validation,
 // workspace ownership, tensor maps, kernel sequencing on the caller's stream.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "moe_internal.cuh"
 
@@ -28,6 +31,44 @@ struct moe_layer {
   void* block = nullptr;
   Prof prof;
 };
+
+namespace moe {
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  struct Done { int dev; const void* func; int bytes; };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Done& d : done)
+    if (d.dev == dev && d.func == func && d.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (Done& d : done)
+    if (d.dev == dev && d.func == func) {
+      d.bytes = bytes;
+      return cudaSuccess;
+    }
+  done.push_back({dev, func, bytes});
+  return cudaSuccess;
+}
+
+std::atomic<int> g_fail_alloc{0};   // > 0: allocations left until the injected failure
+
+cudaError_t dev_malloc(void** p, size_t bytes) {
+  int v = g_fail_alloc.load();
+  while (v > 0 && !g_fail_alloc.compare_exchange_weak(v, v - 1)) {
+  }
+  if (v == 1) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
+
+}  // namespace moe
 
 namespace {
 
@@ -68,6 +109,7 @@ moe_status validate_config(const moe_config* c) {
   if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC || c->gemv_max_tokens < 0 || c->wait_timeout_ms < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->d % 64 || c->ffn % 64 || c->shared_ffn % 64) return MOE_ERR_UNSUPPORTED;
+  if (c->d > kMaxHidden) return MOE_ERR_UNSUPPORTED;
   if (c->num_experts > kMaxExperts || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   const bool combo = (c->act_dtype == MOE_F32 && c->weight_dtype == MOE_F32) ||
                      (c->act_dtype == MOE_BF16 && (c->weight_dtype == MOE_BF16 || c->weight_dtype == MOE_NVFP4));
@@ -426,7 +468,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
   size_t total = 0;
   for (const Part& p : parts) total += up256(p.bytes);
   ws.bytes = total;
-  if (cudaMalloc(&h->block, total) != cudaSuccess) {
+  if (dev_malloc(&h->block, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return MOE_ERR_OOM;
@@ -587,6 +629,12 @@ moe_status moe_check(moe_handle h, cudaStream_t stream) {
   }
   if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
   if (word & kErrRange) return MOE_ERR_RANGE;
+  return MOE_OK;
+}
+
+moe_status moe_debug_fail_alloc(int32_t nth) {
+  if (nth < 0) return MOE_ERR_INVALID_ARG;
+  g_fail_alloc.store(nth);
   return MOE_OK;
 }
 

@@ -132,6 +132,26 @@ struct GemvArgs {
   Workspace ws;
 };
 
+// Raise `func`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device, so it is set once per
+// (device, kernel) pair; the bookkeeping is guarded by a mutex, so several
+// host threads may make first calls at once.  Make the first call on each
+// device before any stream capture.
+cudaError_t ensure_smem_limit(const void* func, int bytes);
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel* func, int bytes) {
+  return ensure_smem_limit(reinterpret_cast<const void*>(func), bytes);
+}
+
+// Every device allocation of the library goes through here, so that
+// moe_debug_fail_alloc can make the nth one fail.
+cudaError_t dev_malloc(void** p, size_t bytes);
+
+// Largest hidden width d: the small-batch router stages 8 tokens x d fp32
+// activations in shared memory under a 200 KiB limit.
+constexpr int kRouteSmallSmem = 200 * 1024;
+constexpr int kMaxHidden = kRouteSmallSmem / (8 * 4);
+
 // Launchers (return the launch status).
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* prof);
 // Tensor-core router for T > 64 with bf16 activations (E a multiple of 64).

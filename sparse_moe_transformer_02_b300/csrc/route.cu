@@ -300,6 +300,7 @@ __device__ void group_from_counts(const RouteArgs& a, int nblk) {
 // (about one instruction per FMA).  The four quarters are added in a fixed
 // order through shared memory.
 constexpr int kSmallTok = 8;
+static_assert(kSmallTok * 4 * kMaxHidden <= kRouteSmallSmem, "router staging must fit its shared-memory limit");
 constexpr int kSmallExp = 4;       // experts per warp
 constexpr int kSmallKq = 4;        // parts of the reduction per CTA
 
@@ -759,11 +760,9 @@ cudaError_t launch_router_split(const float* w, __nv_bfloat16* out, size_t n, cu
 cudaError_t launch_route_tc(const RouteArgs& a, const CUtensorMap* tm_x, const CUtensorMap* tm_wr, uint64_t* cand,
                             uint64_t wait_ns, cudaStream_t s, Prof* prof) {
   const size_t smem = 1024 + (size_t)kRtStages * kRtStageBytes + (2 * kRtStages + 1) * 8 + 16;
-  static bool attr_set = false;   // once, before any stream capture
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return cudaGetLastError();
-    attr_set = true;
+  {
+    const cudaError_t e = ensure_smem_limit(route_tc_kernel, (int)smem);
+    if (e != cudaSuccess) return e;
   }
   RouteTcParams p;
   p.tm_x = *tm_x;
@@ -782,12 +781,10 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
   if (prof) prof->begin(MOE_K_ROUTE, s);
   if (a.T <= kSmallT) {
     const size_t smem = (size_t)kSmallTok * a.d * 4;
-    static bool attr_set = false;  // once, before any stream capture
-    if (!attr_set) {
-      if (cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-          cudaSuccess)
-        return cudaGetLastError();
-      attr_set = true;
+    if (a.d > kMaxHidden) return cudaErrorInvalidValue;
+    {
+      const cudaError_t e0 = ensure_smem_limit(route_small_kernel, kRouteSmallSmem);
+      if (e0 != cudaSuccess) return e0;
     }
     const int epc = 2 * kSmallExp;   // experts per CTA
     const dim3 grid((a.E + epc - 1) / epc, (a.T + kSmallTok - 1) / kSmallTok);
@@ -801,12 +798,10 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s, Prof* 
   switch (ej) {
 #define MOE_RL(N)                                                                                   \
   case N: {                                                                                         \
-    static bool attr_set = false;  /* once, before any stream capture */                            \
-    if (!attr_set) {                                                                                \
-      if (cudaFuncSetAttribute(route_large_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                               (int)((32 * 32 + 32 * N * 128) * sizeof(float))) != cudaSuccess)     \
-        return cudaGetLastError();                                                                  \
-      attr_set = true;                                                                              \
+    {                                                                                               \
+      const cudaError_t e0 = ensure_smem_limit(route_large_kernel<N>,                               \
+                                               (int)((32 * 32 + 32 * N * 128) * sizeof(float)));    \
+      if (e0 != cudaSuccess) return e0;                                                             \
     }                                                                                               \
     const cudaError_t e = launch_pdl_route(route_large_kernel<N>, dim3(grid), kRouteThreads, smem, s, a); \
     if (e != cudaSuccess) return e;                                                                 \

@@ -41,7 +41,10 @@ constexpr size_t kScratchBytes = kOffTicket + kAlign;     // about 144 KiB
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
-// Device address of g_route_scratch, looked up once per device.
+// Device address of g_route_scratch, looked up once per device.  The cache
+// assumes each device's context lives as long as the process: after a
+// cudaDeviceReset the module is loaded again and the array may move, so a
+// process that resets a device must not call moe_route_noalloc on it again.
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
@@ -75,7 +78,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int
   if (T < 0 || T > kNoAllocMaxT) return MOE_ERR_INVALID_ARG;           // beyond the scratch array's size
   if (num_experts < 1 || num_experts > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > num_experts)
     return MOE_ERR_INVALID_ARG;
-  if (d <= 0 || d % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (d <= 0 || d % 64 != 0 || d > kMaxHidden) return MOE_ERR_INVALID_ARG;
   if (act_dtype != MOE_F32 && act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(router_w) & 15u) ||
       (reinterpret_cast<uintptr_t>(router_b) & 3u) || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
@@ -123,5 +126,9 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t T, int32_t d, int
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
-  return launch_route(a, 0, stream, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_route(a, 0, stream, nullptr) != cudaSuccess) {
+    cudaGetLastError();   // leave no launch error behind for the caller's next check
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }

@@ -59,6 +59,7 @@ def fake_weights():
     (dict(max_tokens=0), B.MOE_ERR_INVALID_ARG),
     (dict(path=7), B.MOE_ERR_INVALID_ARG),
     (dict(d=100), B.MOE_ERR_UNSUPPORTED),
+    (dict(d=6464), B.MOE_ERR_UNSUPPORTED),           # the router's staging limit is d <= 6400
     (dict(ffn=96), B.MOE_ERR_UNSUPPORTED),
     (dict(num_experts=1024), B.MOE_ERR_UNSUPPORTED),
     (dict(top_k=9, num_experts=64), B.MOE_ERR_UNSUPPORTED),
@@ -91,6 +92,22 @@ def test_create_rejects_bad_weight_pointers(lib):
     w.s_gate = None                               # NVFP4 scales missing
     cfg = good_cfg(d=1024, ffn=512, shared_ffn=512, act_dtype=B.MOE_BF16, weight_dtype=B.MOE_NVFP4)
     assert B.moe_create(cfg, w, 0)[0] == B.MOE_ERR_INVALID_ARG
+
+
+def test_failure_injection_arguments(lib):
+    assert B.moe_debug_fail_alloc(-1) == B.MOE_ERR_INVALID_ARG
+    assert B.moe_debug_fail_alloc(0) == B.MOE_OK
+
+
+def test_noalloc_rejects_bad_sizes_on_the_host(lib):
+    # every rejection happens before the library looks at the device
+    cases = [dict(T=65), dict(T=-1), dict(d=6464), dict(d=96), dict(E=513), dict(k=9), dict(k=7, E=6),
+             dict(act=B.MOE_NVFP4)]
+    for c in cases:
+        a = dict(T=8, d=1024, E=256, k=6, act=B.MOE_BF16)
+        a.update(c)
+        st = B.moe_route_noalloc(0x1000, a["T"], a["d"], a["E"], a["k"], a["act"], 0x2000, 0, 0x3000, 0x4000)
+        assert st == B.MOE_ERR_INVALID_ARG, c
 
 
 def test_null_handle_calls(lib):
