@@ -255,3 +255,36 @@ def tied_router(spec: LayerSpec, seed: int, layer: int, pairs) -> dict:
         L["router_w"][dst] = L["router_w"][src]
         L["router_b"][dst] = L["router_b"][src]
     return L
+
+
+def make_layer_torch(spec: LayerSpec, seed: int, layer: int, device) -> dict:
+    """One layer drawn on a torch device (bf16 or fp32 storage), keyed by the
+    moe_weights field names: same distributions as ``make_layer`` but torch's
+    generator, so full-size stacks are made in seconds.  Router weights are
+    fp32; the Zipf bias, when asked for, is the same as ``make_layer``'s."""
+    import torch
+    assert spec.weight in ("bf16", "f32")
+    E, d, F, Fs = spec.num_experts, spec.d, spec.ffn, spec.shared_ffn
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000 + int(layer))
+    dt = torch.bfloat16 if spec.weight == "bf16" else torch.float32
+    w = {"router_w": torch.randn(E, d, generator=g, device=device) * spec.sigma_router}
+    if spec.bias == "zipf":
+        w["router_b"] = torch.from_numpy(zipf_bias(seed, layer, E)).to(device)
+    else:
+        w["router_b"] = torch.zeros(E, device=device)
+    shapes = [("w_gate", (E, F, d)), ("w_up", (E, F, d)), ("w_down", (E, d, F))]
+    if Fs > 0:
+        shapes += [("ws_gate", (Fs, d)), ("ws_up", (Fs, d)), ("ws_down", (d, Fs))]
+    for name, shape in shapes:
+        w[name] = (torch.randn(*shape, generator=g, device=device) * spec.sigma_w).to(dt)
+    return w
+
+
+def make_tokens_torch(spec: LayerSpec, seed: int, T: int, device):
+    """Activations x[T][d] N(0, sigma_x^2) drawn on a torch device, in the spec's activation type."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 7919 + 17)
+    x = torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x
+    return x.to(torch.bfloat16) if spec.act == "bf16" else x

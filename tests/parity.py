@@ -27,6 +27,38 @@ MAX_ABS = 2e-2
 REL_L2 = {"f32": 1e-2, "bf16": 1e-2, "nvfp4": 5e-2}
 
 
+class DeviceExperts:
+    """A per-expert stack of device weights [E][rows][cols] that the oracle can
+    index like a numpy array: item e is copied to the host on demand (bf16 as
+    uint16 bit patterns, fp32 as float32).  These are the layer's inputs, drawn
+    by the input generator; nothing here comes from the library."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, e):
+        return host_array(self.t[int(e)])
+
+
+def host_array(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def host_layer(dev: dict) -> dict:
+    """Oracle view of a layer held on the device (keys as in inputs.make_layer):
+    router and shared expert copied whole, routed experts fetched lazily."""
+    L = {"router_w": host_array(dev["router_w"]), "router_b": host_array(dev["router_b"])}
+    for n in ("w_gate", "w_up", "w_down"):
+        L[n] = DeviceExperts(dev[n])
+    for n in ("ws_gate", "ws_up", "ws_down"):
+        if dev.get(n) is not None:
+            L[n] = host_array(dev[n])
+    return L
+
+
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
     """Spacing of bf16 values at |v| (normal range)."""
     e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
@@ -44,8 +76,9 @@ def to_torch_x(x: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(x).to(device)
 
 
-def check_routing(l: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, k: int):
-    """Returns (idx_use, gate_use, n_near): the routing the reference output uses."""
+def check_routing(l: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, k: int, stats: dict = None):
+    """Returns (idx_use, gate_use, n_near): the routing the reference output uses.
+    ``stats`` (optional) receives the largest gate error seen."""
     T, E = l.shape
     srt = -np.sort(-l, axis=1)
     gap = srt[:, k - 1] - srt[:, k] if E > k else np.full(T, np.inf)
@@ -66,12 +99,17 @@ def check_routing(l: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, k: i
         assert np.all(lv[:-1] >= lv[1:] - 1e-5), (t, g, lv)
     gate_use = topk_gates(l, idx_use)
     # gates, matched by expert
+    worst = 0.0
     for t in range(T):
         ref = dict(zip(idx_use[t].tolist(), gate_use[t].tolist()))
         for j in range(k):
             e = int(idx_gpu[t, j])
             if e in ref:
-                assert abs(gate_gpu[t, j] - ref[e]) <= GATE_ATOL, (t, j, gate_gpu[t, j], ref[e])
+                err = abs(gate_gpu[t, j] - ref[e])
+                worst = max(worst, err)
+                assert err <= GATE_ATOL, (t, j, gate_gpu[t, j], ref[e])
+    if stats is not None:
+        stats["gate_err"] = worst
     return idx_use, gate_use, n_near
 
 
@@ -85,7 +123,8 @@ def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tens
     l = router_logits(xs, W.Wr, W.b)
     ig = idx_gpu.cpu().numpy()[sel].astype(np.int64)
     gg = gate_gpu.cpu().numpy()[sel].astype(np.float64)
-    idx_use, gate_use, n_near = check_routing(l, ig, gg, k)
+    stats = {}
+    idx_use, gate_use, n_near = check_routing(l, ig, gg, k, stats)
     y_ref = moe_forward_with_routing(xs, W, idx_use, gate_use, residual=residual)
     yg = to_f64(y_gpu)[sel]
     err = yg - y_ref
@@ -95,4 +134,4 @@ def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tens
     bound = MAX_ABS + (bf16_ulp(y_ref) if residual and y_gpu.dtype == torch.bfloat16 else 0.0)
     assert np.all(np.abs(err) <= bound), (max_abs, rel)
     assert rel <= REL_L2[fmt], (max_abs, rel)
-    return {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near}
+    return {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near, "gate_err": stats["gate_err"]}

@@ -1,4 +1,6 @@
-"""Decode-sized batches (weight-streaming GEMV path) against the oracle."""
+"""Decode-sized batches against the oracle: the default path (tcgen05 for bf16
+weights, GEMV kernels for fp32) and the weight-streaming GEMV kernels forced
+at the Flint shape."""
 import numpy as np
 import pytest
 import torch
@@ -89,6 +91,17 @@ def test_flint_decode_bf16(flint_bf16, T):
     print("flint decode", T, r)
 
 
+@pytest.mark.parametrize("T", [8, 64])
+def test_flint_decode_bf16_gemv_path(flint_bf16, T):
+    """The GEMV kernels (tensor-pipe mma.sync weight streaming for bf16) at the
+    Flint shape, every output element against the oracle."""
+    spec, L, dev = flint_bf16
+    x = I.make_tokens(spec, seed=200 + T, T=T)
+    _, y, idx, gate = run(spec, dev, x, 64, path=B.MOE_PATH_GEMV)
+    r = check_layer(L, x, y, idx, gate, spec.top_k, "bf16")
+    print("flint decode gemv", T, r)
+
+
 def test_flint_decode_residual_and_ragged(flint_bf16):
     spec, L, dev = flint_bf16
     x = I.make_tokens(spec, seed=7, T=37)
@@ -97,9 +110,12 @@ def test_flint_decode_residual_and_ragged(flint_bf16):
 
 
 def test_deterministic_and_host_entry(flint_bf16):
+    """The GEMV path combines each token's expert outputs in a fixed order, so
+    two runs agree bit for bit (the tcgen05 path adds with unordered reductions
+    and promises no bitwise repeatability)."""
     spec, L, dev = flint_bf16
     x_np = I.make_tokens(spec, seed=3, T=24)
-    layer, y, idx, gate = run(spec, dev, x_np, 64)
+    layer, y, idx, gate = run(spec, dev, x_np, 64, path=B.MOE_PATH_GEMV)
     y2 = layer.forward(to_torch_x(x_np))
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))

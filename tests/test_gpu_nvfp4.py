@@ -72,7 +72,9 @@ def test_nvfp4_large_activations(small):
     keeps h / xs^2 in f16, so nothing saturates and the result still matches
     the oracle, relative to the output's magnitude.  The routing is the
     library's (logits of ~10^3 have fp32 rounding far above the near-tie
-    gap); gates are recomputed in float64 for that routing."""
+    gap), checked to be valid: k distinct experts per token, each inside the
+    float64 top-k up to the fp32 rounding of those logits.  Gates are
+    recomputed in float64 for that routing."""
     from oracle.moe_oracle import LayerWeights, moe_forward_with_routing, router_logits, topk_gates
     from oracle.moe_oracle import _widen
     L, dev = small
@@ -82,7 +84,14 @@ def test_nvfp4_large_activations(small):
     W = LayerWeights(L)
     xf = _widen(xb)
     ig = idx.cpu().numpy().astype(np.int64)
-    y_ref = moe_forward_with_routing(xf, W, ig, topk_gates(router_logits(xf, W.Wr, W.b), ig))
+    l = router_logits(xf, W.Wr, W.b)
+    # fp32 logits of this size are exact to about |x| |w| d 2^-24 each
+    tol = 4.0 * 2.0 ** -24 * (np.abs(xf) @ np.abs(W.Wr).T).max()
+    kth = -np.sort(-l, axis=1)[:, SMALL.top_k - 1]
+    for t in range(ig.shape[0]):
+        assert len(set(ig[t].tolist())) == SMALL.top_k and ig[t].min() >= 0 and ig[t].max() < SMALL.num_experts
+        assert np.all(l[t, ig[t]] >= kth[t] - tol), (t, ig[t])
+    y_ref = moe_forward_with_routing(xf, W, ig, topk_gates(l, ig))
     err = y.double().cpu().numpy() - y_ref
     scale = np.abs(y_ref).max()
     assert np.abs(err).max() <= 2e-2 * scale

@@ -67,7 +67,7 @@ def test_flint_prefill_4096(flint_bf16):
     T = 4096
     x = I.make_tokens(spec, seed=4096, T=T)
     layer, y, idx, gate = run(spec, dev, x, T)
-    # routing and grouping on every token, outputs on a seeded sample
+    # routing, grouping and outputs on every token
     W = LayerWeights(L)
     l = router_logits(x.astype(np.float64) if x.dtype != np.uint16 else
                       (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64), W.Wr, W.b)
@@ -78,9 +78,7 @@ def test_flint_prefill_4096(flint_bf16):
     assert np.array_equal(offs.cpu().numpy(), offsets)
     assert np.array_equal(tos.cpu().numpy(), tok_of_slot)
     assert np.array_equal(so.cpu().numpy(), slot_of)
-    sample = np.sort(np.random.default_rng(0).choice(T, 64, replace=False))
-    sample[-1] = T - 1
-    r = check_layer(L, x, y, idx, gate, spec.top_k, "bf16", tokens=sample)
+    r = check_layer(L, x, y, idx, gate, spec.top_k, "bf16")          # every token
     print("flint prefill 4096", r)
 
 

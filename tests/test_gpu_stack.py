@@ -1,26 +1,31 @@
-"""Stacked MoE layers with residual adds and Zipf-skewed routing (full width,
-T = 2048), against the oracle on sampled tokens:
-  - every layer teacher-forced from the oracle's own input to that layer
-    (the GPU runs layer l on the oracle's x_l), within the single-layer bounds;
-  - the chain run exactly as the bench runs it (each layer reads the previous
-    layer's GPU output), against the oracle's chain, by rel-L2 (bf16 rounding
-    of the residual stream may differ by one unit in the last place where the
-    two sums straddle a rounding boundary, and such a difference is carried on).
+"""The 47-layer stack with residual adds and Zipf-skewed routing (full width,
+T = 2048), chained on the GPU exactly as the bench runs it (layer l + 1 reads
+layer l's output).  Every layer is checked against the oracle fed the GPU's
+own input to that layer, on 64 seeded sampled tokens (teacher forcing), within
+the single-layer bounds; the oracle's own 47-layer chain on the same tokens is
+compared at the end and its rel-L2 reported (a one-unit bf16 difference in the
+residual stream can move a later near-tie, so the per-layer check is the gate).
+
+The Flint stack is 47 MoE layers (swarmz.net, "Recursive Flint: 40B Open
+Model, 2.5B Active", section "The architecture, in plain terms").  Layers are
+drawn on the device one at a time and freed after use; the oracle reads the
+routed experts it needs from the device.
 """
 import numpy as np
 import pytest
 import torch
 
-from parity import check_layer, to_f64, to_torch_x
+from parity import check_layer, host_layer, to_f64
 from oracle.formats import round_to_bf16
-from oracle.moe_oracle import LayerWeights, moe_forward, moe_stack
+from oracle.moe_oracle import LayerWeights, moe_forward
 from sparse_moe_transformer_02_b300 import binding as B
 from sparse_moe_transformer_02_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-N_LAYERS = 4
+N_LAYERS = 47
 T = 2048
+N_SAMPLE = 64
 
 
 def bits_of(v: np.ndarray) -> np.ndarray:
@@ -28,37 +33,40 @@ def bits_of(v: np.ndarray) -> np.ndarray:
     return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
 
-def test_stack_of_zipf_layers_with_residual():
-    spec = I.FLINT_STACK_ZIPF
-    Ls = [I.make_layer(spec, seed=3, layer=l) for l in range(N_LAYERS)]
-    layers = [B.layer_from_spec(spec, B.upload_layer(L), T) for L in Ls]
-    x_np = I.make_tokens(spec, seed=3, T=T)
-    sample = np.sort(np.random.default_rng(1).choice(T, 16, replace=False))
-    Ws = [LayerWeights(L) for L in Ls]
+def gpu_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
-    # teacher forcing: layer l on the oracle's own x_l (all T tokens on the GPU,
-    # the sampled ones checked)
-    xl = x_np
-    for l, (layer, W) in enumerate(zip(layers, Ws)):
+
+def test_stack47_zipf_layers_teacher_forced():
+    spec = I.FLINT_STACK_ZIPF
+    seed = 3
+    x = I.make_tokens_torch(spec, seed=seed, T=T, device="cuda")
+    sample = np.sort(np.random.default_rng(1).choice(T, N_SAMPLE, replace=False))
+    sample[-1] = T - 1
+    x_ref = None                           # the oracle's own chain on the sampled tokens
+    worst = {"max_abs": 0.0, "rel_l2": 0.0, "gate_err": 0.0, "near_ties": 0}
+    for l in range(N_LAYERS):
+        dev = I.make_layer_torch(spec, seed=seed, layer=l, device="cuda")
+        layer = B.layer_from_spec(spec, dev, T)
         idx = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
         gate = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
-        y = layer.forward(to_torch_x(xl), idx=idx, gate=gate)
+        y = layer.forward(x, idx=idx, gate=gate)
         torch.cuda.synchronize()
-        r = check_layer(Ls[l], xl, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=sample)
-        print("layer", l, r)
-        if l + 1 < N_LAYERS:          # the oracle's x_{l+1} for every token
-            yref, _, _ = moe_forward(xl, W, spec.top_k, residual=True)
-            xl = bits_of(round_to_bf16(yref))
-
-    # the chain as the bench runs it
-    x = to_torch_x(x_np)
-    for layer in layers:
-        x = layer.forward(x)
-    torch.cuda.synchronize()
-    for layer in layers:
-        assert layer.check() == B.MOE_OK
-    ref, _ = moe_stack(x_np, Ws, spec.top_k, tokens=sample)
+        assert layer.check() == B.MOE_OK, l
+        L = host_layer(dev)
+        x_np = gpu_bits(x)
+        r = check_layer(L, x_np, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=sample)
+        for key in ("max_abs", "rel_l2", "gate_err"):
+            worst[key] = max(worst[key], r[key])
+        worst["near_ties"] += r["near_ties"]
+        W = LayerWeights(L)
+        xin = x_np[sample] if x_ref is None else bits_of(x_ref)
+        yref, _, _ = moe_forward(xin, W, spec.top_k, residual=True)
+        x_ref = round_to_bf16(yref)
+        layer.close()
+        del dev, L, W
+        x = y
     yg = to_f64(x)[sample]
-    rel = np.linalg.norm(yg - ref) / np.linalg.norm(ref)
-    assert np.all(np.isfinite(yg)) and rel <= 1e-2, rel
-    print("chained", N_LAYERS, "layers: rel-L2", rel)
+    rel = float(np.linalg.norm(yg - x_ref) / np.linalg.norm(x_ref))
+    print("stack47 per-layer worst", worst, "| chained rel-L2 after 47 layers", rel)
+    assert np.all(np.isfinite(yg))

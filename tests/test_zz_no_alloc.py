@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from parity import GATE_ATOL, to_torch_x
+from parity import GATE_ATOL, check_routing, to_torch_x
+from oracle.moe_oracle import LayerWeights, router_logits
 from sparse_moe_transformer_02_b300 import binding as B
 from sparse_moe_transformer_02_b300 import inputs as I
 
@@ -33,6 +34,38 @@ def test_noalloc_route_matches_handle_route_twice():
         assert torch.equal(idx, idx_ref), call
         assert torch.equal(cnt, cnt_ref), call
         assert float((gate - gate_ref).abs().max()) <= GATE_ATOL, call
+    layer.close()
+
+
+def test_noalloc_wide_router_f32_without_bias_or_counts():
+    """E = 512 experts (16 logits per lane in the top-k), k = 8, fp32
+    activations, no router bias and no counts buffer, right after a handle's
+    moe_route has left the shared scratch in another state; checked against
+    moe_route and against the oracle's routing (bit-exact where the 8th/9th
+    logit gap exceeds 1e-4)."""
+    spec = I.LayerSpec(d=512, ffn=128, shared_ffn=128, num_experts=512, top_k=8, act="f32", weight="f32",
+                       sigma_router=0.05)
+    L = I.make_layer(spec, seed=13)
+    dev = B.upload_layer(L)
+    dev_nob = dict(dev)
+    dev_nob["router_b"] = None
+    layer = B.layer_from_spec(spec, dev_nob, 64)
+    s = torch.cuda.current_stream().cuda_stream
+    W = LayerWeights(L)
+    for call, (T, seed) in enumerate(((40, 41), (64, 42))):
+        x_np = I.make_tokens(spec, seed=seed, T=T)
+        x = to_torch_x(x_np)
+        idx_ref, gate_ref, _ = layer.route(x)
+        idx = torch.full((T, spec.top_k), -1, dtype=torch.int32, device="cuda")
+        gate = torch.full((T, spec.top_k), -1.0, dtype=torch.float32, device="cuda")
+        st = B.moe_route_noalloc(x.data_ptr(), T, spec.d, spec.num_experts, spec.top_k, B.MOE_F32,
+                                 dev["router_w"].data_ptr(), 0, idx.data_ptr(), gate.data_ptr(), 0, s)
+        assert st == B.MOE_OK, (call, B.moe_status_string(st))
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx_ref), call
+        assert float((gate - gate_ref).abs().max()) <= GATE_ATOL, call
+        l = router_logits(x_np.astype(np.float64), W.Wr, np.zeros(spec.num_experts))
+        check_routing(l, idx.cpu().numpy().astype(np.int64), gate.cpu().numpy().astype(np.float64), spec.top_k)
     layer.close()
 
 
