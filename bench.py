@@ -1,24 +1,32 @@
 #!/usr/bin/env python3
-"""MoE-layer throughput on B300: tokens/s through one sparse MoE FFN layer,
-with the achieved HBM GB/s (decode) or bf16 TFLOP/s (prefill) of the
-dominant kernel against the measured peak.
+"""MoE-layer throughput on B300: tokens/s through sparse MoE FFN layers of the
+Flint shape, with the achieved HBM GB/s or bf16 TFLOP/s of the layer and of its
+dominant kernel against the measured peaks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one forward pass of the whole layer (router, top-k, grouping,
-expert gate/up + SwiGLU, down + gated combine + shared expert) through L
-distinct layers' weights, so the weights streamed per step are far larger
-than L2 and every layer reads HBM.  Inputs are seeded synthetic tensors with
-the Flint-shaped layer's sizes (d=2048, 256 routed experts + 1 shared,
-expert FFN 512, top-6); weights are drawn on the device.
+Headline workload (default): the 47-layer MoE stack of the Flint decoder
+(d = 2048, 256 routed experts + 1 shared, expert FFN 512, top-6), T = 2048
+tokens, router bias drawn so expert load follows Zipf(1.1), residual add
+between layers, layers chained (layer l + 1 reads layer l's output).  One
+step = one pass of all 47 layers (router, top-k, grouping, expert gate/up +
+SwiGLU, down + gated combine + shared expert + residual); value = tokens x
+layers / time.  The other configurations (decode T = 1, 8, 32, 64; prefill
+T = 4096 and 16384; NVFP4 decode T = 32) are measured in the same run and
+reported under "sweep", each against its binding roof.  Weights and
+activations are seeded synthetic draws made on the device.
 
-Under torchrun (N > 1) every rank runs an independent replica on its own GPU
-(the layer has no cross-GPU step); value = tokens of all ranks / max time.
+With --gpus N (N > 1) the script starts N ranks itself under
+torch.distributed.run; every rank runs an independent replica on its own GPU
+(the layer has no cross-GPU step); value = units of all ranks / slowest rank's
+time.
 """
 import argparse
 import hashlib
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -28,21 +36,22 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# name: (layer kind, tokens, layers in the rotation, chained)
 WORKLOADS = {
-    # name: (layer spec name, tokens, layers in the rotation)
-    "decode64": ("bf16", 64, 16),
-    "decode32": ("bf16", 32, 16),
-    "decode8": ("bf16", 8, 16),
-    "decode1": ("bf16", 1, 16),
-    "prefill4096": ("bf16", 4096, 8),
-    "prefill16384": ("bf16", 16384, 4),   # ~384 tokens per expert: past the ridge, tensor peak binds
-    "nvfp4_32": ("nvfp4", 32, 32),
-    "stack47": ("stack", 2048, 47),      # 47 chained layers, residual adds, Zipf(1.1) load
+    "stack47": ("stack", 2048, 47, True),
+    "decode1": ("bf16", 1, 16, False),
+    "decode8": ("bf16", 8, 16, False),
+    "decode32": ("bf16", 32, 16, False),
+    "decode64": ("bf16", 64, 16, False),
+    "prefill4096": ("bf16", 4096, 8, False),
+    "prefill16384": ("bf16", 16384, 4, False),   # ~384 tokens per expert: past the ridge, tensor peak binds
+    "nvfp4_32": ("nvfp4", 32, 32, False),
 }
-DEFAULT = "decode64"
-SWEEP = ["decode1", "decode8", "decode32"]
-B_EXP_BF16 = 3 * 2048 * 512 * 2                    # bytes of one expert's three matrices
-B_EXP_NVFP4 = 3 * (2048 * 512 // 2 + 2048 * 512 // 16 + 4)
+DEFAULT = "stack47"
+SWEEP = ["decode1", "decode8", "decode32", "decode64", "prefill4096", "prefill16384", "nvfp4_32"]
+D, E_ROUTED, F_EXP, TOPK = 2048, 256, 512, 6
+B_EXP_BF16 = 3 * D * F_EXP * 2                       # bytes of one expert's three bf16 matrices
+B_EXP_NVFP4 = 3 * (D * F_EXP // 2 + D * F_EXP // 16 + 4)
 
 
 def peaks():
@@ -106,17 +115,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ helpers
-def src_sha(*files):
-    h = hashlib.sha256()
-    for f in files:
-        h.update(open(os.path.join(ROOT, "sparse_moe_transformer_02_b300", "csrc", f), "rb").read())
-    return h.hexdigest()[:16]
-
-
 def csrc_sha():
     """Hash of every kernel source: a traffic figure is kept only while the code it was taken on is unchanged."""
     d = os.path.join(ROOT, "sparse_moe_transformer_02_b300", "csrc")
-    return src_sha(*sorted(f for f in os.listdir(d) if f.endswith((".cu", ".cuh"))))
+    h = hashlib.sha256()
+    for f in sorted(f for f in os.listdir(d) if f.endswith((".cu", ".cuh"))):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def dram_traffic(kernel, workload):
@@ -146,96 +151,92 @@ def job_throughput(units_per_rank, t_max_s, world):
     return world * units_per_rank / t_max_s
 
 
-def make_device_layers(kind, n_layers, device, seed):
-    """n_layers independent Flint-shaped layers drawn on the device (bf16), or NVFP4
-    layers that share one host-quantised expert set copied to distinct buffers."""
-    import torch
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launcher_command(argv, n):
+    """The torch.distributed.run command that starts n ranks of this script with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+
+
+def layer_bytes_flops(kind, T, U_mean):
+    """Algorithmic bytes and flops of one layer: the touched experts' weights
+    (realised routing) + the shared expert + router + x in and y out; bf16
+    tensor flops of the k + 1 expert passes + the fp32 router's."""
+    b_exp = B_EXP_NVFP4 if kind == "nvfp4" else B_EXP_BF16
+    byt = (U_mean + 1) * b_exp + 4 * D * E_ROUTED + 4 * E_ROUTED + T * D * 2 * 2
+    flops = 2 * T * (TOPK + 1) * 3 * D * F_EXP + 2 * T * D * E_ROUTED
+    return byt, flops
+
+
+def kernel_bytes_flops(kname, kind, T, U_mean):
+    """Algorithmic bytes and tensor flops of one launch of a kernel of the layer."""
+    b_exp = B_EXP_NVFP4 if kind == "nvfp4" else B_EXP_BF16
+    byt = {"route": 4 * D * E_ROUTED + 4 * E_ROUTED + T * D * 2,
+           "gemv_gateup": (U_mean + 1) * b_exp * 2 / 3 + T * D * 2,
+           "gemv_down": (U_mean + 1) * b_exp / 3 + T * D * 2,
+           "tc_gateup": (U_mean + 1) * b_exp * 2 / 3 + T * D * 2,
+           "tc_down": (U_mean + 1) * b_exp / 3,
+           "tc_gather": 2 * T * TOPK * D * 2,
+           "tc_finalize": T * D * (4 + 2)}.get(kname, 0)
+    flops = {"tc_gateup": 2 * T * (TOPK + 1) * 2 * D * F_EXP,
+             "tc_down": 2 * T * (TOPK + 1) * D * F_EXP,
+             "gemv_gateup": 2 * T * (TOPK + 1) * 2 * D * F_EXP,
+             "gemv_down": 2 * T * (TOPK + 1) * D * F_EXP,
+             "route": 2 * T * D * E_ROUTED}.get(kname, 0)
+    return byt, flops
+
+
+def binding(byt, flops, t_s, pk):
+    """The binding roof of work that moves byt bytes and does flops bf16 flops in t_s seconds."""
+    t_mem = byt / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    if t_tc > t_mem:
+        ach = flops / t_s / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops"], 4), "t_lb_us": round(t_tc * 1e6, 2)}
+    ach = byt / t_s / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / pk["hbm_gbs"], 4), "t_lb_us": round(t_mem * 1e6, 2)}
+
+
+# ------------------------------------------------------------------ layer sets on the device
+def make_layer_set(kind, n_layers, device, seed):
+    """n_layers independent Flint-shaped layers on the device.  bf16 and stack
+    layers are drawn there; NVFP4 layers share one host-quantised expert set,
+    copied to distinct buffers per layer (so every layer still reads HBM)."""
     from sparse_moe_transformer_02_b300 import binding as B
     from sparse_moe_transformer_02_b300 import inputs as I
     spec = {"bf16": I.FLINT_BF16, "nvfp4": I.FLINT_NVFP4, "stack": I.FLINT_STACK_ZIPF}[kind]
-    E, d, F, Fs = spec.num_experts, spec.d, spec.ffn, spec.shared_ffn
-    g = torch.Generator(device=device)
-    layers = []
-    base = None
     if kind == "nvfp4":
         base = B.upload_layer(I.make_layer(spec, seed=seed), device)
-    for li in range(n_layers):
-        g.manual_seed(seed * 1000 + li)
-        w = {"router_w": torch.randn(E, d, generator=g, device=device) * spec.sigma_router,
-             "router_b": torch.zeros(E, device=device)}
-        if spec.bias == "zipf":
-            w["router_b"] = torch.from_numpy(I.zipf_bias(seed, li, E)).to(device)
-        if kind in ("bf16", "stack"):
-            for name, shape in (("w_gate", (E, F, d)), ("w_up", (E, F, d)), ("w_down", (E, d, F)),
-                                ("ws_gate", (Fs, d)), ("ws_up", (Fs, d)), ("ws_down", (d, Fs))):
-                w[name] = (torch.randn(*shape, generator=g, device=device) * spec.sigma_w).to(torch.bfloat16)
-        else:
-            for name, t in base.items():
-                if name not in ("router_w", "router_b"):
-                    w[name] = t.clone()
-        layers.append(w)
-    return spec, layers
+        layers = []
+        for li in range(n_layers):
+            w = {k: (t.clone() if k not in ("router_w", "router_b") else t) for k, t in base.items()}
+            layers.append(w)
+        return spec, layers
+    return spec, [I.make_layer_torch(spec, seed=seed, layer=li, device=device) for li in range(n_layers)]
 
 
-def oracle_tokens_per_s(kind, T, seed, budget_s=20.0):
-    """The CPU oracle (float64 numpy) on a bounded sample of the workload, timed in a
-    fresh interpreter whose BLAS is limited to one thread."""
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", kind, str(T), str(seed), str(budget_s)]
-    # (the stack's oracle sample is one layer of the stack)
-    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
-    if res.returncode != 0:
-        raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
-    r = json.loads(res.stdout.strip().splitlines()[-1])
-    return r["tokens_per_s"], {"kind": "oracle", "cores": 1, "sample": r["sample"]}
-
-
-def oracle_sample_main(kind, T, seed, budget_s):
-    """Child side of oracle_tokens_per_s: prints {"tokens_per_s", "sample"}."""
-    import oracle
-    from sparse_moe_transformer_02_b300 import inputs as I
-    spec = {"bf16": I.FLINT_BF16, "nvfp4": I.FLINT_NVFP4, "stack": I.FLINT_STACK_ZIPF}[kind]
-    L = I.make_layer(spec, seed=seed)
-    W = oracle.LayerWeights(L)
-    x = I.make_tokens(spec, seed=seed, T=max(T, 1))
-    done, t_used = 0, 0.0
-    n = min(T, 8)
-    while t_used < budget_s and done < T:
-        t0 = time.perf_counter()
-        oracle.moe_forward(x[done:done + n], W, spec.top_k, residual=spec.add_residual)
-        t_used += time.perf_counter() - t0
-        done += n
-    print(json.dumps({"tokens_per_s": done / t_used,
-                      "sample": f"{done} of the workload's {T} tokens through one layer ({kind} weights), "
-                                f"float64 numpy oracle, 1 BLAS thread, {t_used:.1f} s"}))
-
-
-# ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world, local_rank):
+def measure(args, name, spec, kind, wts, T, chain, device, stream, rank, world, steps, sample_clocks,
+            want_e2e):
+    """Time one workload on an existing layer set; returns the result dict."""
     import torch
     import torch.distributed as dist
     from sparse_moe_transformer_02_b300 import binding as B
-    from sparse_moe_transformer_02_b300 import build
+    from sparse_moe_transformer_02_b300 import inputs as I
 
-    build.build()
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    kind, T, n_layers = WORKLOADS[args.workload]
-    if args.layers:
-        n_layers = args.layers
-    spec, wts = make_device_layers(kind, n_layers, device, seed=args.seed + rank)
-    stream = torch.cuda.Stream(device)
     handles = []
     with torch.cuda.stream(stream):
         for w in wts:
             handles.append(B.layer_from_spec(spec, w, max_tokens=max(T, 64), stream=stream,
                                              path={"auto": 0, "gemv": 1, "tc": 2}[args.path]))
-    g = torch.Generator(device=device)
-    g.manual_seed(args.seed + 77 + rank)
-    x = (torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x).to(torch.bfloat16)
+    x = I.make_tokens_torch(spec, seed=args.seed + 77 + rank + T, T=T, device=device)
     ys = [torch.empty_like(x) for _ in handles]
-    chain = kind == "stack"          # layer l + 1 reads layer l's output
     ins = [x] + ys[:-1] if chain else [x] * len(handles)
     torch.cuda.synchronize()
 
@@ -243,19 +244,19 @@ def run_ours(args, rank, world, local_rank):
         for h, xi, y in zip(handles, ins, ys):
             h.forward(xi, y, stream=stream)
 
-    # realised routing: distinct experts per layer (on each layer's actual input)
     step()
     stream.synchronize()
+    for h in handles:
+        st = h.check(stream)
+        if st != B.MOE_OK:
+            raise RuntimeError(f"{name}: device error {B.moe_status_string(st)}")
+    # realised routing: distinct experts per layer (on each layer's actual input)
     U = []
     for h, xi in zip(handles, ins):
         _, _, cnt = h.route(xi, stream=stream)
         stream.synchronize()
         U.append(int((cnt > 0).sum().item()))
-    # kernels one forward launches: router, slot placement / activation copy,
-    # gate/up, down, finalise on the tensor-core path; router, (NVFP4: f16
-    # activation copy,) gate/up, down-and-combine on the GEMV path
-    tc_path = args.path != "gemv"
-    kernels_per_fwd = 5 if tc_path else (4 if kind == "nvfp4" else 3)
+    Umean = sum(U) / len(U)
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -266,18 +267,26 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
+    # at least ~0.4 s of timed work so that the clock samples mean something
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    one = ev0.elapsed_time(ev1)
+    n_steps = steps if steps else max(10, int(math.ceil(400.0 / max(one, 1e-3))))
 
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(torch.cuda.current_device()) if (rank == 0 and sample_clocks) else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(n_steps):
             graph.replay()
         ev1.record(stream)
     ev1.synchronize()
@@ -287,14 +296,17 @@ def run_ours(args, rank, world, local_rank):
     t_ms = max_over_ranks(t_ms, device)
     if world > 1:
         dist.barrier()
+    del graph
 
-    ms_step = t_ms / args.steps
-    value = job_throughput(T * n_layers * args.steps, t_ms / 1e3, world)
+    n_layers = len(handles)
+    ms_step = t_ms / n_steps
+    value = job_throughput(T * n_layers * n_steps, t_ms / 1e3, world)
+    pk = peaks()
 
-    # per-kernel timing (separate, eager pass with event pairs around each launch)
+    # per-kernel timing: a separate eager pass with event pairs around each launch
     for h in handles:
-        B._ok(B.moe_profile_enable(h.h, 1, 64 * kernels_per_fwd), "moe_profile_enable")
-    prof_steps = 5
+        B._ok(B.moe_profile_enable(h.h, 1, 64), "moe_profile_enable")
+    prof_steps = 3
     for _ in range(prof_steps):
         step()
     tot = {}
@@ -306,177 +318,252 @@ def run_ours(args, rank, world, local_rank):
             a[0] += ms
             a[1] += n
         B.moe_profile_enable(h.h, 0, 0)
+    launches_per_fwd = sum(v[1] for v in tot.values()) / (prof_steps * n_layers)
     dom = max(tot, key=lambda kk: tot[kk][0])
     dom_ms = tot[dom][0] / max(tot[dom][1], 1)
-    pk = peaks()
-    Umean = sum(U) / len(U)
-    b_exp = B_EXP_NVFP4 if kind == "nvfp4" else B_EXP_BF16
-    d, E, F = spec.d, spec.num_experts, spec.ffn
-    per_kernel_bytes = {
-        "route": 4 * d * E + 4 * E + T * d * 2,
-        "gemv_gateup": (Umean + 1) * b_exp * 2 / 3 + T * d * 2,
-        "gemv_down": (Umean + 1) * b_exp / 3 + T * d * 2,
-        "tc_gateup": (Umean + 1) * b_exp * 2 / 3 + T * d * 2,
-        "tc_down": (Umean + 1) * b_exp / 3,
-        "tc_gather": 2 * T * spec.top_k * d * 2,
-        "tc_finalize": T * d * (4 + 2),
-    }
-    layer_bytes = (Umean + 1) * b_exp + 4 * d * E + 4 * E + T * d * 2 * 2
-    layer_flops = 2 * T * (spec.top_k + 1) * 3 * d * F + 2 * T * d * E
-    # the dominant kernel's binding roof: whichever of HBM bytes / measured
-    # bandwidth and tensor flops / measured bf16 peak takes longer
-    per_kernel_flops = {"tc_gateup": 2 * T * (spec.top_k + 1) * 2 * d * F,
-                        "tc_down": 2 * T * (spec.top_k + 1) * d * F}
-    dom_bytes = per_kernel_bytes.get(dom, 0)
-    dom_flops = per_kernel_flops.get(dom, 0)
-    if dom_flops / (pk["bf16_tflops"] * 1e12) > dom_bytes / (pk["hbm_gbs"] * 1e9):
-        bound, unit, peak = "tensor", "TFLOP/s", pk["bf16_tflops"]
-        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    else:
-        bound, unit, peak = "hbm", "GB/s", pk["hbm_gbs"]
-        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = dram_traffic(dom, args.workload)
-    roofline = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": pk["source"],
-                "kernel_ms": round(dom_ms, 5),
-                "per_kernel_ms": {kk: round(v[0] / max(v[1], 1), 5) for kk, v in tot.items() if v[1]}}
-    layer_time_s = ms_step / 1e3 / n_layers
-    layer = {"us_per_layer": round(layer_time_s * 1e6, 2), "distinct_experts_mean": round(Umean, 2),
-             "algorithmic_bytes": int(layer_bytes), "hbm_gbs": round(layer_bytes / layer_time_s / 1e9, 1),
-             "hbm_frac_of_measured": round(layer_bytes / layer_time_s / 1e9 / pk["hbm_gbs"], 4),
-             "hbm_frac_of_8tbs": round(layer_bytes / layer_time_s / 1e9 / 8000.0, 4),
-             "tflops": round(layer_flops / layer_time_s / 1e12, 2)}
+    kb, kf = kernel_bytes_flops(dom, kind, T, Umean)
+    roof = binding(kb, kf, dom_ms * 1e-3, pk)
+    roof.update({"kernel": dom, "kernel_ms": round(dom_ms, 5), "traffic": dram_traffic(dom, name),
+                 "algorithmic_bytes": int(kb), "flops": int(kf), "peak_source": pk["source"],
+                 "per_kernel_ms": {kk: round(v[0] / max(v[1], 1), 5) for kk, v in tot.items() if v[1]}})
 
-    # end to end with host buffers, host<->device copies inside the timed region:
-    # independent layers go through moe_forward_host (copy in, forward, copy out);
-    # the chained stack copies its input in and its output out around the chain
-    xh = x.cpu().pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    for h in handles[:2]:
-        h.forward_host(xh, yh, stream=stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e_steps = max(1, min(args.steps, 10))
+    lb, lf = layer_bytes_flops(kind, T, Umean)
+    t_layer = ms_step / 1e3 / n_layers
+    lay = binding(lb, lf, t_layer, pk)
+    layer = {"us_per_layer": round(t_layer * 1e6, 2), "distinct_experts_mean": round(Umean, 2),
+             "algorithmic_bytes": int(lb), "flops": int(lf), "bound": lay["bound"],
+             "roof_frac": lay["frac"], "t_lb_us": lay["t_lb_us"],
+             "hbm_gbs": round(lb / t_layer / 1e9, 1),
+             "hbm_frac_of_measured": round(lb / t_layer / 1e9 / pk["hbm_gbs"], 4),
+             "hbm_frac_of_8tbs": round(lb / t_layer / 1e9 / 8000.0, 4),
+             "tflops": round(lf / t_layer / 1e12, 2),
+             "tensor_frac_of_measured": round(lf / t_layer / 1e12 / pk["bf16_tflops"], 4)}
+
+    e2e = None
+    if want_e2e:
+        # end to end with host buffers, host<->device copies inside the timed
+        # region: independent layers go through moe_forward_host (copy in,
+        # forward, copy out); the chained stack copies its input in and its
+        # output out around the chain
+        xh = x.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        for h in handles[:2]:
+            h.forward_host(xh, yh, stream=stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e_steps = max(1, min(n_steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            if chain:
+                with torch.cuda.stream(stream):
+                    x.copy_(xh, non_blocking=True)
+                    step()
+                    yh.copy_(ys[-1], non_blocking=True)
+                stream.synchronize()
+            else:
+                for h in handles:
+                    h.forward_host(xh, yh, stream=stream)
+        e_s = max_over_ranks(time.perf_counter() - t0, device)
+        io_layers = 1 if chain else n_layers
+        e2e = {"value": round(job_throughput(T * n_layers * e_steps, e_s, world), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * spec.d * 2 * io_layers, "d2h_bytes_per_step": T * spec.d * 2 * io_layers}
+
+    for h in handles:
+        h.close()
+    del ys, ins, x
+    return {"name": name, "value": value, "tokens_per_s": round(value, 1), "T": T, "layers": n_layers,
+            "steps": n_steps, "ms_per_step": round(ms_step, 5), "layer": layer, "roofline": roof,
+            "clocks": clocks, "e2e": e2e, "launches_per_forward": launches_per_fwd,
+            "gpu_launches": int(round(n_steps * n_layers * launches_per_fwd))}
+
+
+# ------------------------------------------------------------------ the CPU oracle as a baseline
+def oracle_rates(kind, T, seed, budget_s, steps=1, procs=1):
+    """The float64 oracle on bounded samples of the workload, in a fresh
+    interpreter that never touches CUDA: one layer of the workload's kind,
+    tokens split over `procs` worker processes (one BLAS thread each).
+    Returns ([tokens/s per step], description)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", kind, str(T), str(seed), str(budget_s),
+           str(steps), str(procs)]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
+    r = json.loads(res.stdout.strip().splitlines()[-1])
+    return r["rates"], r["sample"]
+
+
+def _oracle_worker(args):
+    x, k, residual = args
+    W = _ORACLE_STATE["W"]
+    import oracle
     t0 = time.perf_counter()
-    for _ in range(e_steps):
-        if chain:
-            with torch.cuda.stream(stream):
-                x.copy_(xh, non_blocking=True)
-                step()
-                yh.copy_(ys[-1], non_blocking=True)
-            stream.synchronize()
-        else:
-            for h in handles:
-                h.forward_host(xh, yh, stream=stream)
-    e_s = max_over_ranks(time.perf_counter() - t0, device)
-    io_layers = 1 if chain else n_layers
-    e2e = {"value": round(job_throughput(T * n_layers * e_steps, e_s, world), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": T * spec.d * 2 * io_layers, "d2h_bytes_per_step": T * spec.d * 2 * io_layers}
+    oracle.moe_forward(x, W, k, residual=residual)
+    return time.perf_counter() - t0
+
+
+_ORACLE_STATE = {}
+
+
+def oracle_sample_main(kind, T, seed, budget_s, steps, procs):
+    """Child side of oracle_rates: prints {"rates", "sample"}.  The layer is
+    made once; worker processes are forked from this CUDA-free interpreter
+    after that, so they share it."""
+    import multiprocessing as mp
+    import oracle
+    from sparse_moe_transformer_02_b300 import inputs as I
+    spec = {"bf16": I.FLINT_BF16, "nvfp4": I.FLINT_NVFP4, "stack": I.FLINT_STACK_ZIPF}[kind]
+    L = I.make_layer(spec, seed=seed)
+    _ORACLE_STATE["W"] = oracle.LayerWeights(L)
+    x = I.make_tokens(spec, seed=seed, T=max(T, 1))
+    chunk = min(T, 4)
+    pool = mp.get_context("fork").Pool(procs) if procs > 1 else None
+    rates, total_tok, total_t = [], 0, 0.0
+    pos = 0
+    for _ in range(steps):
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            jobs = []
+            for _ in range(procs):
+                jobs.append((x[pos:pos + chunk], spec.top_k, spec.add_residual))
+                pos = (pos + chunk) % max(T - chunk + 1, 1)
+            if pool:
+                pool.map(_oracle_worker, jobs)
+            else:
+                _oracle_worker(jobs[0])
+            done += chunk * len(jobs)
+        dt = time.perf_counter() - t0
+        rates.append(done / dt)
+        total_tok += done
+        total_t += dt
+    if pool:
+        pool.close()
+        pool.join()
+    print(json.dumps({"rates": rates,
+                      "sample": f"{total_tok} tokens of the workload's {T} ({chunk} per call) through one layer "
+                                f"({kind} weights), float64 numpy oracle, {procs} process(es) x 1 BLAS thread, "
+                                f"{total_t:.1f} s"}))
+
+
+def cpu_baseline(kind, T, seed):
+    """The oracle single-threaded and on all host cores (token-parallel processes)."""
+    cores = os.cpu_count() or 1
+    out = {"kind": "oracle", "unit": "tokens/s", "host_cores": cores}
+    r1, s1 = oracle_rates(kind, T, seed, budget_s=10.0)
+    out["single_thread"] = {"value": round(r1[0], 3), "cores": 1, "sample": s1}
+    rn, sn = oracle_rates(kind, T, seed, budget_s=10.0, procs=cores)
+    out.update({"value": round(rn[0], 3), "cores": cores, "sample": sn})
+    return out
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from sparse_moe_transformer_02_b300 import build
+
+    build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+
+    kind, T, n_layers, chain = WORKLOADS[args.workload]
+    if args.layers:
+        n_layers = args.layers
+    spec, wts = make_layer_set(kind, n_layers, device, seed=args.seed + rank)
+    head = measure(args, args.workload, spec, kind, wts, T, chain, device, stream, rank, world, args.steps,
+                   sample_clocks=True, want_e2e=True)
+    del wts
+    torch.cuda.empty_cache()
 
     sweep = {}
-    if args.sweep and rank == 0 and world == 1 and args.workload.startswith("decode"):
+    if args.sweep and world == 1:
+        sets = {}
         for wname in SWEEP:
-            sweep[wname] = sweep_point(args, wname, handles, spec, device, stream)
+            if wname == args.workload:
+                continue
+            k2, T2, n2, ch2 = WORKLOADS[wname]
+            key = (k2, n2)
+            if key not in sets:
+                sets.clear()
+                torch.cuda.empty_cache()
+                sets[key] = make_layer_set(k2, n2, device, seed=args.seed + 1)
+            sp2, w2 = sets[key]
+            r = measure(args, wname, sp2, k2, w2, T2, ch2, device, stream, rank, world, 0, sample_clocks=True,
+                        want_e2e=False)
+            r.pop("e2e", None)
+            r.pop("value", None)
+            sweep[wname] = r
+        sets.clear()
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            v, info = oracle_tokens_per_s(kind, T, seed=args.seed)
-            cpu = dict(info, value=round(v, 3), unit="tokens/s")
+            cpu = cpu_baseline(kind, T, seed=args.seed)
         except Exception as exc:          # the GPU numbers stand without it
             cpu = {"kind": "oracle", "value": None, "error": str(exc)[-300:]}
 
-    for h in handles:
-        h.close()
     if rank == 0:
-        out = {"metric": "MoE-layer tokens/s", "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-               "dtype": "nvfp4" if kind == "nvfp4" else "bf16",
-               "data": "synthetic (seeded N(0,0.02) weights drawn on the device, N(0,1) activations)",
-               "config": {"workload": f"flint_moe_layer_{args.workload}", "tokens": T, "d": spec.d,
+        out = {"metric": "MoE-layer tokens/s", "value": round(head["value"], 1), "unit": "tokens/s",
+               "n_gpus": world, "steps": head["steps"], "warmup": args.warmup,
+               "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "nvfp4" if kind == "nvfp4" else "bf16",
+               "data": "synthetic (seeded N(0,0.02) weights and N(0,1) activations drawn on the device)",
+               "config": {"workload": f"flint_moe_{args.workload}", "tokens": T, "d": spec.d,
                           "experts": spec.num_experts, "shared_experts": 1, "top_k": spec.top_k,
-                          "expert_ffn": spec.ffn, "weights": kind, "layers_per_step": n_layers,
-                          "l2": f"inputs larger than L2: {n_layers} distinct layers' weights per step",
-                          "chained": chain, "router_bias": spec.bias,
+                          "expert_ffn": spec.ffn, "weights": kind, "layers_per_step": head["layers"],
+                          "chained": chain, "router_bias": spec.bias, "residual": bool(spec.add_residual),
+                          "l2": f"inputs larger than L2: {head['layers']} distinct layers' weights per step",
                           "parallelism": f"replicas{world}", "path": args.path},
-               "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-               "gpu_launches": args.steps * n_layers * kernels_per_fwd, "clocks": clocks}
+               "layer": head["layer"], "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
+               "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
         if sweep:
             out["sweep"] = sweep
         print(json.dumps(out), flush=True)
-
-
-def sweep_point(args, wname, handles, spec, device, stream):
-    """Tokens/s and HBM GB/s of the same layers at another decode batch size."""
-    import torch
-    kind, T, _ = WORKLOADS[wname]
-    g = torch.Generator(device=device)
-    g.manual_seed(args.seed + 1234 + T)
-    x = (torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x).to(torch.bfloat16)
-    ys = [torch.empty_like(x) for _ in handles]
-    U = []
-    for h in handles:
-        _, _, cnt = h.route(x, stream=stream)
-        stream.synchronize()
-        U.append(int((cnt > 0).sum().item()))
-
-    def step():
-        for h, y in zip(handles, ys):
-            h.forward(x, y, stream=stream)
-    for _ in range(3):
-        step()
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(args.steps, 10)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(n):
-            graph.replay()
-        ev1.record(stream)
-    ev1.synchronize()
-    t = ev0.elapsed_time(ev1) / 1e3 / n / len(handles)
-    Um = sum(U) / len(U)
-    byt = (Um + 1) * B_EXP_BF16 + 4 * spec.d * spec.num_experts + 4 * spec.num_experts + T * spec.d * 4
-    return {"tokens_per_s": round(T / t, 1), "us_per_layer": round(t * 1e6, 2), "distinct_experts_mean": Um,
-            "hbm_gbs": round(byt / t / 1e9, 1), "hbm_frac_of_measured": round(byt / t / 1e9 / peaks()["hbm_gbs"], 4)}
 
 
 # ------------------------------------------------------------------ reference arm (the CPU oracle)
 def run_reference(args, rank):
     if rank != 0:
         return
-    kind, T, _ = WORKLOADS[args.workload]
-    for _ in range(args.warmup):
-        oracle_tokens_per_s(kind, T, seed=args.seed, budget_s=0.5)
-    vals, infos = [], []
+    kind, T, _, chain = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        v, info = oracle_tokens_per_s(kind, T, seed=args.seed, budget_s=2.0)
-        vals.append(v)
-        infos.append(info)
+    rates, sample = oracle_rates(kind, T, args.seed, budget_s=2.0, steps=args.warmup + args.steps, procs=cores)
     total = time.perf_counter() - t0
-    v = statistics.median(vals)
+    timed = rates[args.warmup:]
+    v = statistics.median(timed)
     out = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": round(v, 3), "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(1e3 * total / max(args.steps, 1), 3), "higher_is_better": True,
+           "ms_per_step": round(1e3 * total / max(args.steps + args.warmup, 1), 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": f"flint_moe_layer_{args.workload}", "tokens": T},
-           "cpu_baseline": dict(infos[-1], value=round(v, 3), unit="tokens/s"),
+           "config": {"workload": f"flint_moe_{args.workload}", "tokens": T, "weights": kind, "chained": chain},
+           "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": round(v, 3),
+                            "unit": "tokens/s"},
            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------------ rank plumbing self-test (CPU)
+def run_rank_selftest(rank, world):
+    """Exercises the multi-rank plumbing without a GPU: gloo ranks, each
+    'times' a fixed amount of host work, max over ranks, job throughput."""
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cpu")
+    t = 0.25 * (rank + 1)
+    t_max = max_over_ranks(t, dev)
+    if rank == 0:
+        print(json.dumps({"metric": "selftest units/s", "value": job_throughput(100, t_max, world),
+                          "n_gpus": world, "t_max": t_max}), flush=True)
+
+
 def main():
     if len(sys.argv) > 1 and sys.argv[1] == "--oracle-sample":
-        oracle_sample_main(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]), float(sys.argv[5]))
+        a = sys.argv[2:]
+        oracle_sample_main(a[0], int(a[1]), int(a[2]), float(a[3]), int(a[4]), int(a[5]))
         return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,25 +576,37 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--rank-selftest", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # start the ranks ourselves, one per GPU, and pass their exit status on
+        sys.exit(subprocess.call(launcher_command(sys.argv[1:], args.gpus)))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    import torch.distributed as dist
+    if args.rank_selftest:
+        if world > 1:
+            dist.init_process_group("gloo")
+        try:
+            run_rank_selftest(rank, world)
+        finally:
+            if world > 1:
+                dist.destroy_process_group()
+        return
     if world > 1:
         import torch
-        import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
         run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
-            import torch.distributed as dist
             dist.destroy_process_group()
 
 

@@ -42,3 +42,21 @@ def test_two_replicas_take_the_slowest_rank():
 def test_single_process_passes_through():
     assert bench.max_over_ranks(2.0, torch.device("cpu")) == 2.0
     assert bench.job_throughput(64, 2.0, 1) == 32.0
+
+
+def test_bench_starts_its_own_ranks():
+    """`bench.py --gpus 2` with no launcher around it starts two ranks under
+    torch.distributed.run; here they run the CPU self-test of the rank
+    plumbing (gloo), and rank 0 reports n_gpus = 2 and the job rate over the
+    slowest rank."""
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"), "--gpus", "2",
+                          "--rank-selftest"], capture_output=True, text=True, env=env, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    r = json.loads(lines[0])
+    assert r["n_gpus"] == 2 and r["t_max"] == 0.5 and r["value"] == 400.0
