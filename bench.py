@@ -49,6 +49,11 @@ WORKLOADS = {
 }
 DEFAULT = "stack47"
 SWEEP = ["decode1", "decode8", "decode32", "decode64", "prefill4096", "prefill16384", "nvfp4_32"]
+# measured on the headline's resident 47-layer stack: the persistent decode kernel
+STACK_DECODE = {"stack47_decode1": 1, "stack47_decode8": 8}
+# the 4-bit output layer (vocabulary 146,432 x d 2048, NVFP4), four copies in rotation
+HEAD = {"lmhead1": 1, "lmhead8": 8}
+HEAD_COPIES = 4
 D, E_ROUTED, F_EXP, TOPK = 2048, 256, 512, 6
 B_EXP_BF16 = 3 * D * F_EXP * 2                       # bytes of one expert's three bf16 matrices
 B_EXP_NVFP4 = 3 * (D * F_EXP // 2 + D * F_EXP // 16 + 4)
@@ -378,6 +383,118 @@ def measure(args, name, spec, kind, wts, T, chain, device, stream, rank, world, 
             "gpu_launches": int(round(n_steps * n_layers * launches_per_fwd))}
 
 
+def measure_stack_decode(args, name, spec, wts, T, device, stream):
+    """The persistent kernel over the whole stack (one launch per pass), T tokens."""
+    import torch
+    from sparse_moe_transformer_02_b300 import binding as B
+    from sparse_moe_transformer_02_b300 import inputs as I
+    st = B.MoeStack(spec, wts, max_tokens=max(T, 8), stream=stream)
+    if not st.persistent(T):
+        st.close()
+        return {"skipped": "the persistent kernel does not serve this shape"}
+    x = I.make_tokens_torch(spec, seed=args.seed + 500 + T, T=T, device=device)
+    y = torch.empty_like(x)
+    with torch.cuda.stream(stream):
+        _, _, it, _ = st.forward(x, trace=True, stream=stream)
+    stream.synchronize()
+    if st.check(stream) != B.MOE_OK:
+        raise RuntimeError(f"{name}: device error")
+    U = [len(set(it[l].flatten().tolist())) for l in range(st.L)]
+    Umean = sum(U) / len(U)
+    for _ in range(args.warmup):
+        st.forward(x, y, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        st.forward(x, y, stream=stream)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 50
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    clocks = sampler.stop()
+    t = ev0.elapsed_time(ev1) / 1e3 / n
+    del graph
+    st.close()
+    pk = peaks()
+    lb, lf = layer_bytes_flops("stack", T, Umean)
+    t_layer = t / len(wts)
+    lay = binding(lb, lf, t_layer, pk)
+    roof = binding(lb * len(wts), lf * len(wts), t, pk)
+    roof.update({"kernel": "stack_decode_kernel", "kernel_ms": round(t * 1e3, 5), "traffic": dram_traffic("stack_decode", name),
+                 "algorithmic_bytes": int(lb * len(wts)), "flops": int(lf * len(wts)), "peak_source": pk["source"]})
+    return {"name": name, "tokens_per_s": round(T / t, 1), "layer_tokens_per_s": round(T * len(wts) / t, 1), "T": T,
+            "layers": len(wts), "steps": n, "ms_per_step": round(t * 1e3, 5),
+            "layer": {"us_per_layer": round(t_layer * 1e6, 2), "distinct_experts_mean": round(Umean, 2),
+                      "algorithmic_bytes": int(lb), "bound": lay["bound"], "roof_frac": lay["frac"],
+                      "t_lb_us": lay["t_lb_us"], "hbm_gbs": round(lb / t_layer / 1e9, 1),
+                      "hbm_frac_of_measured": round(lb / t_layer / 1e9 / pk["hbm_gbs"], 4),
+                      "hbm_frac_of_8tbs": round(lb / t_layer / 1e9 / 8000.0, 4)},
+            "roofline": roof, "clocks": clocks, "launches_per_forward": 1, "gpu_launches": n}
+
+
+def measure_head(args, name, T, device, stream):
+    """The 4-bit output layer at T tokens, HEAD_COPIES copies of the head in rotation."""
+    import torch
+    from sparse_moe_transformer_02_b300 import binding as B
+    from sparse_moe_transformer_02_b300 import inputs as I
+    h = I.make_head(seed=args.seed)
+    base = [torch.from_numpy(h["packed"]).to(device), torch.from_numpy(h["scales"]).to(device),
+            torch.from_numpy(h["tscale"]).to(device)]
+    heads = [B.LmHead(*(t.clone() for t in base), max_tokens=8) for _ in range(HEAD_COPIES)]
+    V, d = h["packed"].shape[0], h["packed"].shape[1] * 2
+    x = I.make_tokens_torch(I.FLINT_BF16, seed=args.seed + 900 + T, T=T, device=device)
+    outs = [torch.empty((T, V), dtype=torch.float32, device=device) for _ in heads]
+
+    def step():
+        for hd, o in zip(heads, outs):
+            hd.forward(x, o, stream=stream)
+    step()
+    stream.synchronize()
+    for hd in heads:
+        if hd.check(stream) != B.MOE_OK:
+            raise RuntimeError(f"{name}: device error")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 100
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    clocks = sampler.stop()
+    t = ev0.elapsed_time(ev1) / 1e3 / n / len(heads)
+    del graph
+    for hd in heads:
+        hd.close()
+    pk = peaks()
+    byt = V * d // 2 + V * d // 16 + 4 + T * d * 2 + T * V * 4
+    flops = 2 * T * V * d
+    roof = binding(byt, 0, t, pk)
+    roof.update({"kernel": "lm_head_kernel", "kernel_ms": round(t * 1e3, 5), "traffic": dram_traffic("lm_head", name),
+                 "algorithmic_bytes": int(byt), "flops": int(flops), "peak_source": pk["source"]})
+    return {"name": name, "tokens_per_s": round(T / t, 1), "T": T, "vocab": V, "d": d, "us_per_call": round(t * 1e6, 2),
+            "roofline": roof, "clocks": clocks, "launches_per_forward": 1, "gpu_launches": n * len(heads)}
+
+
 # ------------------------------------------------------------------ the CPU oracle as a baseline
 def oracle_rates(kind, T, seed, budget_s, steps=1, procs=1):
     """The float64 oracle on bounded samples of the workload, in a fresh
@@ -474,10 +591,13 @@ def run_ours(args, rank, world, local_rank):
     spec, wts = make_layer_set(kind, n_layers, device, seed=args.seed + rank)
     head = measure(args, args.workload, spec, kind, wts, T, chain, device, stream, rank, world, args.steps,
                    sample_clocks=True, want_e2e=True)
+    sweep = {}
+    if args.sweep and world == 1 and kind == "stack" and len(wts) == WORKLOADS["stack47"][2]:
+        for wname, Tn in STACK_DECODE.items():
+            sweep[wname] = measure_stack_decode(args, wname, spec, wts, Tn, device, stream)
     del wts
     torch.cuda.empty_cache()
 
-    sweep = {}
     if args.sweep and world == 1:
         sets = {}
         for wname in SWEEP:
@@ -496,6 +616,9 @@ def run_ours(args, rank, world, local_rank):
             r.pop("value", None)
             sweep[wname] = r
         sets.clear()
+        torch.cuda.empty_cache()
+        for wname, Tn in HEAD.items():
+            sweep[wname] = measure_head(args, wname, Tn, device, stream)
         torch.cuda.empty_cache()
 
     cpu = None

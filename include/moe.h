@@ -252,6 +252,97 @@ moe_status moe_profile_enable(moe_handle h, int32_t enable, int32_t max_launches
  */
 moe_status moe_profile_read(moe_handle h, float* ms, int32_t* launches);
 
+/* ------------------------------------------------------------------ stacks */
+
+typedef struct moe_stack* moe_stack_handle;    /* opaque, owned by the library */
+
+/*
+ * A stack of MoE layers joined by residual adds, x_{l+1} = bf16(x_l +
+ * moe_l(x_l)): the 47 MoE layers of the Flint decoder (swarmz.net, section
+ * "The architecture, in plain terms"; the rounding of the residual stream to
+ * the activation type between layers is this library's reading).
+ *
+ * cfg: the shape shared by every layer; add_residual must be nonzero.
+ * layers: n_layers (1..4096) weight sets as in moe_create, borrowed for the
+ * handle's lifetime.  Creates one moe_create handle per layer (the per-layer
+ * path) and, when the shapes allow it, sets up the persistent decode kernel:
+ * bf16 weights and activations, at most 256 routed experts, d, F and F_s
+ * multiples of 256, a device of compute capability 10.x that launches
+ * cooperative grids.  That kernel runs every layer of the stack for T <= 8
+ * tokens in one launch -- the counterpart of the decode megakernel the pages
+ * describe (evermx.com review, Feature Overview, "Kernels and inference").
+ * Errors: those of moe_create; MOE_ERR_INVALID_ARG for a NULL argument,
+ * n_layers out of range or add_residual == 0; MOE_ERR_OOM if the stack's own
+ * workspace cannot be allocated.  On failure *out is NULL and nothing is held.
+ */
+moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, int32_t n_layers,
+                            cudaStream_t stream, moe_stack_handle* out);
+
+/* Free the stack, its layer handles and workspace (synchronises the device). NULL is a no-op. */
+moe_status moe_stack_destroy(moe_stack_handle h);
+
+/* 1 if moe_stack_forward with T tokens runs the persistent kernel, else 0 (per-layer path). */
+int32_t moe_stack_uses_persistent(moe_stack_handle h, int32_t T);
+
+/*
+ * Run the whole stack: y = layer_{L-1}( ... layer_0(x)), each layer with its
+ * residual add.  x [T][d] and y [T][d] in act_dtype, device memory, 16-byte
+ * aligned, not overlapping; T <= max_tokens.  Optional traces (NULL to skip):
+ * x_trace [L + 1][T][d] receives x and every layer's output (16-byte aligned);
+ * idx_trace [L][T][k] int32 and gate_trace [L][T][k] fp32 (both or neither)
+ * receive every layer's routing.  Enqueued on `stream`, no host
+ * synchronisation.  Errors: MOE_ERR_INVALID_ARG for bad arguments (checked
+ * before any launch), MOE_ERR_CUDA if a launch fails (the persistent kernel
+ * needs all of its CTAs resident at once: one per SM).  Device-side timeouts
+ * show up in moe_stack_check.
+ */
+moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void* y, void* x_trace,
+                             int32_t* idx_trace, float* gate_trace, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then report and clear the error words of the
+ * persistent kernel and of every layer handle (as moe_check).
+ */
+moe_status moe_stack_check(moe_stack_handle h, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ 4-bit output layer */
+
+typedef struct moe_head* moe_head_handle;      /* opaque, owned by the library */
+
+/*
+ * The output layer (lm_head) quantised to 4 bits: the pages say it was, since
+ * it is a large share of the weights read per token, and that the shipped
+ * low-bit model is NVFP4 (evermx.com review, Feature Overview,
+ * "Quantization").  logits[t][v] = sum_i x[t][i] W[v][i], W = e2m1 code x
+ * e4m3 block scale (one per 16 values along d) x fp32 matrix scale.
+ *
+ * codes [vocab][d / 2] bytes (element 2i in the low nibble), scales
+ * [vocab][d / 16] e4m3 codes, tscale [1] fp32: device memory, borrowed for
+ * the handle's lifetime, codes and scales 16-byte aligned.  d a multiple of
+ * 512, vocab a multiple of 16.  wait_timeout_ms limits every device-side wait
+ * (0 = 2000 ms).  Errors: MOE_ERR_INVALID_ARG (NULL, non-positive sizes,
+ * misalignment), MOE_ERR_UNSUPPORTED (shape), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+moe_status moe_head_create(int32_t d, int32_t vocab, int32_t max_tokens, const uint8_t* codes,
+                           const uint8_t* scales, const float* tscale, int32_t wait_timeout_ms,
+                           moe_head_handle* out);
+
+/*
+ * logits [T][vocab] fp32 (device, 16-byte aligned) from x [T][d] bf16 (device,
+ * 16-byte aligned), T <= max_tokens; one launch per 8 tokens, enqueued on
+ * `stream`.  The weights are decoded exactly to f16 in registers and x is
+ * carried in f16 with an exact power-of-two scale per token; products are
+ * accumulated in fp32.  Errors: MOE_ERR_INVALID_ARG (checked before any
+ * launch), MOE_ERR_CUDA (launch); timeouts show up in moe_head_check.
+ */
+moe_status moe_head_forward(moe_head_handle h, const void* x, int32_t T, float* logits, cudaStream_t stream);
+
+/* Synchronise `stream`, then report and clear the head's error word (MOE_ERR_TIMEOUT or MOE_OK). */
+moe_status moe_head_check(moe_head_handle h, cudaStream_t stream);
+
+/* Free the handle (synchronises the device). NULL is a no-op. */
+moe_status moe_head_destroy(moe_head_handle h);
+
 /*
  * Routing without any device allocation (no counterpart on the pages).
  *

@@ -20,7 +20,9 @@ MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_TC = 0, 1, 2
 
 EXPORTED = ["moe_status_string", "moe_create", "moe_destroy", "moe_route", "moe_forward",
             "moe_forward_host", "moe_get_grouping", "moe_check", "moe_debug_expire_wait",
-            "moe_profile_enable", "moe_profile_read", "moe_route_noalloc", "moe_debug_fail_alloc"]
+            "moe_profile_enable", "moe_profile_read", "moe_route_noalloc", "moe_debug_fail_alloc",
+            "moe_stack_create", "moe_stack_destroy", "moe_stack_uses_persistent", "moe_stack_forward",
+            "moe_stack_check", "moe_head_create", "moe_head_forward", "moe_head_check", "moe_head_destroy"]
 KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize"]
 
 
@@ -78,8 +80,27 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_enable.argtypes = [vp, i32, i32]
         L.moe_profile_read.restype = ctypes.c_int
         L.moe_profile_read.argtypes = [vp, vp, vp]
+        L.moe_stack_create.restype = ctypes.c_int
+        L.moe_stack_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights), i32, vp,
+                                       ctypes.POINTER(vp)]
+        L.moe_stack_destroy.restype = ctypes.c_int
+        L.moe_stack_destroy.argtypes = [vp]
+        L.moe_stack_uses_persistent.restype = ctypes.c_int32
+        L.moe_stack_uses_persistent.argtypes = [vp, i32]
+        L.moe_stack_forward.restype = ctypes.c_int
+        L.moe_stack_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
+        L.moe_stack_check.restype = ctypes.c_int
+        L.moe_stack_check.argtypes = [vp, vp]
         L.moe_debug_fail_alloc.restype = ctypes.c_int
         L.moe_debug_fail_alloc.argtypes = [i32]
+        L.moe_head_create.restype = ctypes.c_int
+        L.moe_head_create.argtypes = [i32, i32, i32, vp, vp, vp, i32, ctypes.POINTER(vp)]
+        L.moe_head_forward.restype = ctypes.c_int
+        L.moe_head_forward.argtypes = [vp, vp, i32, vp, vp]
+        L.moe_head_check.restype = ctypes.c_int
+        L.moe_head_check.argtypes = [vp, vp]
+        L.moe_head_destroy.restype = ctypes.c_int
+        L.moe_head_destroy.argtypes = [vp]
         L.moe_route_noalloc.restype = ctypes.c_int
         L.moe_route_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
@@ -152,6 +173,52 @@ def moe_route_noalloc(x: int, T: int, d: int, num_experts: int, top_k: int, act_
     """Routing with no device allocation (scratch in a fixed static array; see include/moe.h)."""
     return lib().moe_route_noalloc(x, T, d, num_experts, top_k, act_dtype, router_w, router_b or None, idx, gate,
                                    counts or None, stream)
+
+
+def moe_stack_create(cfg: moe_config, layers, stream: int = 0):
+    """layers: a sequence of moe_weights.  Returns (status, handle)."""
+    arr = (moe_weights * len(layers))(*layers)
+    h = ctypes.c_void_p()
+    st = lib().moe_stack_create(ctypes.byref(cfg), arr, len(layers), ctypes.c_void_p(stream), ctypes.byref(h))
+    return st, h.value
+
+
+def moe_stack_destroy(h) -> int:
+    return lib().moe_stack_destroy(h)
+
+
+def moe_stack_uses_persistent(h, T: int) -> int:
+    return lib().moe_stack_uses_persistent(h, T)
+
+
+def moe_stack_forward(h, x: int, T: int, y: int, x_trace: int = 0, idx_trace: int = 0, gate_trace: int = 0,
+                      stream: int = 0) -> int:
+    return lib().moe_stack_forward(h, x, T, y, x_trace or None, idx_trace or None, gate_trace or None, stream)
+
+
+def moe_stack_check(h, stream: int = 0) -> int:
+    return lib().moe_stack_check(h, stream)
+
+
+def moe_head_create(d: int, vocab: int, max_tokens: int, codes: int, scales: int, tscale: int,
+                    wait_timeout_ms: int = 0):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    st = lib().moe_head_create(d, vocab, max_tokens, codes or None, scales or None, tscale or None,
+                               wait_timeout_ms, ctypes.byref(h))
+    return st, h.value
+
+
+def moe_head_forward(h, x: int, T: int, logits: int, stream: int = 0) -> int:
+    return lib().moe_head_forward(h, x, T, logits, stream)
+
+
+def moe_head_check(h, stream: int = 0) -> int:
+    return lib().moe_head_check(h, stream)
+
+
+def moe_head_destroy(h) -> int:
+    return lib().moe_head_destroy(h)
 
 
 def _ok(st: int, what: str):
@@ -233,6 +300,105 @@ class MoeLayer:
     def close(self):
         if getattr(self, "h", None):
             moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def weights_struct(weights: dict) -> moe_weights:
+    """moe_weights with the data pointers of a dict of device tensors (missing keys -> NULL)."""
+    w = moe_weights()
+    for name, _ in moe_weights._fields_:
+        t = weights.get(name)
+        setattr(w, name, t.data_ptr() if t is not None else None)
+    return w
+
+
+class MoeStack:
+    """A stack handle plus the device tensors of every layer it borrows."""
+
+    def __init__(self, spec, layers: list, max_tokens: int, stream=None, **kw):
+        import torch
+        self.torch = torch
+        self.tensors = [dict(w) for w in layers]
+        self.cfg = moe_config(d=spec.d, ffn=spec.ffn, shared_ffn=spec.shared_ffn, num_experts=spec.num_experts,
+                              top_k=spec.top_k, max_tokens=max_tokens, act_dtype=_DT[spec.act],
+                              weight_dtype=_DT[spec.weight], add_residual=1, path=kw.get("path", MOE_PATH_AUTO),
+                              gemv_max_tokens=0, wait_timeout_ms=kw.get("wait_timeout_ms", 0))
+        s = stream if stream is not None else torch.cuda.current_stream()
+        st, self.h = moe_stack_create(self.cfg, [weights_struct(w) for w in self.tensors], s.cuda_stream)
+        _ok(st, "moe_stack_create")
+        self.L, self.d, self.k = len(layers), spec.d, spec.top_k
+
+    def _stream(self, stream):
+        return (stream if stream is not None else self.torch.cuda.current_stream()).cuda_stream
+
+    def persistent(self, T: int) -> bool:
+        return bool(moe_stack_uses_persistent(self.h, T))
+
+    def forward(self, x, y=None, trace=False, stream=None):
+        """Returns y, or (y, x_trace [L+1][T][d], idx [L][T][k], gate [L][T][k]) with trace=True."""
+        torch = self.torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        xt = it = gt = None
+        if trace:
+            xt = torch.empty((self.L + 1, T, self.d), dtype=x.dtype, device=x.device)
+            it = torch.empty((self.L, T, self.k), dtype=torch.int32, device=x.device)
+            gt = torch.empty((self.L, T, self.k), dtype=torch.float32, device=x.device)
+        st = moe_stack_forward(self.h, x.data_ptr(), T, y.data_ptr(), xt.data_ptr() if trace else 0,
+                               it.data_ptr() if trace else 0, gt.data_ptr() if trace else 0, self._stream(stream))
+        _ok(st, "moe_stack_forward")
+        return (y, xt, it, gt) if trace else y
+
+    def check(self, stream=None) -> int:
+        return moe_stack_check(self.h, self._stream(stream))
+
+    def close(self):
+        if getattr(self, "h", None):
+            moe_stack_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class LmHead:
+    """A 4-bit output-layer handle plus the device tensors it borrows
+    (codes uint8 [V][d/2], scales uint8 [V][d/16], tscale float32 [1])."""
+
+    def __init__(self, codes, scales, tscale, max_tokens: int, wait_timeout_ms: int = 0):
+        import torch
+        self.torch = torch
+        self.codes, self.scales, self.tscale = codes, scales, tscale
+        self.V, self.d = codes.shape[0], codes.shape[1] * 2
+        st, self.h = moe_head_create(self.d, self.V, max_tokens, codes.data_ptr(), scales.data_ptr(),
+                                     tscale.data_ptr(), wait_timeout_ms)
+        _ok(st, "moe_head_create")
+
+    def forward(self, x, logits=None, stream=None):
+        torch = self.torch
+        if logits is None:
+            logits = torch.empty((x.shape[0], self.V), dtype=torch.float32, device=x.device)
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        _ok(moe_head_forward(self.h, x.data_ptr(), x.shape[0], logits.data_ptr(), s), "moe_head_forward")
+        return logits
+
+    def check(self, stream=None) -> int:
+        s = (stream if stream is not None else self.torch.cuda.current_stream()).cuda_stream
+        return moe_head_check(self.h, s)
+
+    def close(self):
+        if getattr(self, "h", None):
+            moe_head_destroy(self.h)
             self.h = None
 
     def __del__(self):

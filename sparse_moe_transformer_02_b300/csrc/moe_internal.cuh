@@ -236,4 +236,56 @@ struct Tc4Args {
 };
 cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof);
 
+// ---------------------------------------------------------------- persistent stack decode
+constexpr int kSdMaxT = 8;          // tokens per call of the persistent stack kernel
+constexpr int kSdConsumers = 8;     // consumer warps per CTA
+
+// Weights of one layer of a stack (device pointers, bf16 experts, fp32 router).
+struct StackLayerPtrs {
+  const float* wr;
+  const float* br;                  // nullptr = zeros
+  const __nv_bfloat16* wg;          // [E][F][d]
+  const __nv_bfloat16* wu;
+  const __nv_bfloat16* wd;          // [E][d][F]
+  const __nv_bfloat16* sg;          // [Fs][d]
+  const __nv_bfloat16* su;
+  const __nv_bfloat16* sd;          // [d][Fs]
+};
+
+struct StackArgs {
+  const StackLayerPtrs* layers;     // [L], device memory
+  int L;
+  const __nv_bfloat16* x_in;        // [T][d]
+  __nv_bfloat16* y_out;             // [T][d]
+  __nv_bfloat16* xbuf;              // [2][kSdMaxT][d] residual stream between layers
+  float* logits;                    // [kSdMaxT][E]
+  __nv_bfloat16* h;                 // [kSdMaxT * (k + 1)][Fmax]
+  __nv_bfloat16* x_trace;           // [L + 1][T][d] or nullptr
+  int32_t* idx_trace;               // [L][T][k] or nullptr
+  float* gate_trace;                // [L][T][k] (with idx_trace)
+  unsigned* bar;                    // grid barrier counter, zero at launch
+  unsigned* err;                    // device error word
+  int T, d, F, Fs, E, k;
+  uint64_t wait_ns;
+};
+size_t stack_decode_smem_bytes(int d, int F, int Fs, int k);
+
+// ---------------------------------------------------------------- 4-bit output layer
+constexpr int kHdMaxT = 8;          // tokens per launch of the output-layer kernel
+constexpr int kHdConsumers = 8;
+
+struct HeadArgs {
+  const uint8_t* codes;             // [V][d / 2] e2m1 pairs, element 2i in the low nibble
+  const uint8_t* scales;            // [V][d / 16] e4m3 block scales
+  const float* tscale;              // [1] matrix scale
+  const __nv_bfloat16* x;           // [T][d]
+  float* logits;                    // [T][V]
+  int T, d, V;
+  unsigned* err;
+  uint64_t wait_ns;
+};
+size_t lm_head_smem_bytes(int d);
+cudaError_t launch_lm_head(const HeadArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_stack_decode(const StackArgs& a, int num_sms, cudaStream_t s);
+
 }  // namespace moe

@@ -1,0 +1,223 @@
+// Host side of the stack entry points (moe_stack_* in include/moe.h): a stack
+// of MoE layers joined by residual adds, run either by the persistent decode
+// kernel (one launch for all layers, small batches) or layer by layer through
+// moe_forward.
+#include <new>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_stack {
+  moe_config cfg;
+  int L = 0;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<moe_handle> layers;    // one handle per layer (per-layer path)
+  bool persistent = false;           // the persistent kernel serves T <= kSdMaxT
+  StackLayerPtrs* d_layers = nullptr;
+  void* block = nullptr;             // xbuf, logits, h, barrier counter, error word, chain buffers
+  __nv_bfloat16* xbuf = nullptr;
+  float* logits = nullptr;
+  __nv_bfloat16* h = nullptr;
+  unsigned* bar = nullptr;
+  unsigned* err = nullptr;
+  void* chain[2] = {nullptr, nullptr};
+  uint64_t wait_ns = 0;
+};
+
+namespace {
+
+inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+void free_stack(moe_stack* s) {
+  for (moe_handle h : s->layers) moe_destroy(h);
+  if (s->block) cudaFree(s->block);
+  if (s->d_layers) cudaFree(s->d_layers);
+  delete s;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, int32_t n_layers, cudaStream_t stream,
+                            moe_stack_handle* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !layers || n_layers < 1 || n_layers > 4096) return MOE_ERR_INVALID_ARG;
+  if (!cfg->add_residual) return MOE_ERR_INVALID_ARG;
+  moe_stack* s = new (std::nothrow) moe_stack();
+  if (!s) return MOE_ERR_OOM;
+  s->cfg = *cfg;
+  s->L = n_layers;
+  const moe_config& c = s->cfg;
+  for (int l = 0; l < n_layers; ++l) {
+    moe_handle h = nullptr;
+    const moe_status st = moe_create(cfg, &layers[l], stream, &h);
+    if (st != MOE_OK) {
+      free_stack(s);
+      return st;
+    }
+    s->layers.push_back(h);
+  }
+  int coop = 0, cc_major = 0, smem_optin = 0;
+  if (cudaGetDevice(&s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, s->device) != cudaSuccess) {
+    cudaGetLastError();
+    free_stack(s);
+    return MOE_ERR_CUDA;
+  }
+  s->wait_ns = (uint64_t)(c.wait_timeout_ms > 0 ? c.wait_timeout_ms : 2000) * 1000000ull;
+  const int Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
+  // The persistent kernel: bf16 weights and activations, at most 256 experts
+  // (one warp's top-k), widths in whole 256-value segments, its shared-memory
+  // plan within the device's limit, and a device that launches cooperative grids.
+  s->persistent = c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.num_experts <= 256 &&
+                  c.d % 256 == 0 && c.ffn % 256 == 0 && c.shared_ffn % 256 == 0 && cc_major == 10 && coop &&
+                  stack_decode_smem_bytes(c.d, c.ffn, c.shared_ffn, c.top_k) <= (size_t)smem_optin;
+  const size_t es = c.act_dtype == MOE_F32 ? 4 : 2;
+  const size_t nx = (size_t)kSdMaxT * c.d * 2, nlog = (size_t)kSdMaxT * c.num_experts * 4;
+  const size_t nh = (size_t)kSdMaxT * (c.top_k + 1) * Fmax * 2, nchain = (size_t)c.max_tokens * c.d * es;
+  const size_t total = up256(2 * nx) + up256(nlog) + up256(nh) + 256 + 256 + 2 * up256(nchain);
+  if (dev_malloc(&s->block, total) != cudaSuccess) {
+    cudaGetLastError();
+    s->block = nullptr;
+    free_stack(s);
+    return MOE_ERR_OOM;
+  }
+  uint8_t* p = static_cast<uint8_t*>(s->block);
+  s->xbuf = reinterpret_cast<__nv_bfloat16*>(p); p += up256(2 * nx);
+  s->logits = reinterpret_cast<float*>(p); p += up256(nlog);
+  s->h = reinterpret_cast<__nv_bfloat16*>(p); p += up256(nh);
+  s->bar = reinterpret_cast<unsigned*>(p); p += 256;
+  s->err = reinterpret_cast<unsigned*>(p); p += 256;
+  s->chain[0] = p; p += up256(nchain);
+  s->chain[1] = p;
+  if (s->persistent) {
+    std::vector<StackLayerPtrs> hp(n_layers);
+    for (int l = 0; l < n_layers; ++l) {
+      const moe_weights& w = layers[l];
+      hp[l] = StackLayerPtrs{w.router_w, w.router_b,
+                             static_cast<const __nv_bfloat16*>(w.w_gate), static_cast<const __nv_bfloat16*>(w.w_up),
+                             static_cast<const __nv_bfloat16*>(w.w_down), static_cast<const __nv_bfloat16*>(w.ws_gate),
+                             static_cast<const __nv_bfloat16*>(w.ws_up), static_cast<const __nv_bfloat16*>(w.ws_down)};
+    }
+    void* dl = nullptr;
+    if (dev_malloc(&dl, sizeof(StackLayerPtrs) * n_layers) != cudaSuccess) {
+      cudaGetLastError();
+      free_stack(s);
+      return MOE_ERR_OOM;
+    }
+    s->d_layers = static_cast<StackLayerPtrs*>(dl);
+    if (cudaMemcpyAsync(s->d_layers, hp.data(), sizeof(StackLayerPtrs) * n_layers, cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess) {
+      cudaGetLastError();
+      free_stack(s);
+      return MOE_ERR_CUDA;
+    }
+  }
+  if (cudaMemsetAsync(s->err, 0, 256, stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    free_stack(s);
+    return MOE_ERR_CUDA;
+  }
+  *out = s;
+  return MOE_OK;
+}
+
+moe_status moe_stack_destroy(moe_stack_handle h) {
+  if (!h) return MOE_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  free_stack(h);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int32_t moe_stack_uses_persistent(moe_stack_handle h, int32_t T) {
+  return (h && h->persistent && T >= 1 && T <= kSdMaxT && T <= h->cfg.max_tokens) ? 1 : 0;
+}
+
+moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void* y, void* x_trace, int32_t* idx_trace,
+                             float* gate_trace, cudaStream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = h->cfg;
+  if (T < 0 || T > c.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  auto mis = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (!x || !y || mis(x) || mis(y) || mis(x_trace)) return MOE_ERR_INVALID_ARG;
+  if ((idx_trace == nullptr) != (gate_trace == nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx_trace) & 3u) || (reinterpret_cast<uintptr_t>(gate_trace) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  const size_t es = c.act_dtype == MOE_F32 ? 4 : 2;
+  const size_t nb = (size_t)T * c.d * es;
+  {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(y);
+    if (a < b + nb && b < a + nb) return MOE_ERR_INVALID_ARG;
+  }
+  if (moe_stack_uses_persistent(h, T)) {
+    if (cudaMemsetAsync(h->bar, 0, 4, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    StackArgs a;
+    a.layers = h->d_layers;
+    a.L = h->L;
+    a.x_in = static_cast<const __nv_bfloat16*>(x);
+    a.y_out = static_cast<__nv_bfloat16*>(y);
+    a.xbuf = h->xbuf;
+    a.logits = h->logits;
+    a.h = h->h;
+    a.x_trace = static_cast<__nv_bfloat16*>(x_trace);
+    a.idx_trace = idx_trace;
+    a.gate_trace = gate_trace;
+    a.bar = h->bar;
+    a.err = h->err;
+    a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+    a.wait_ns = h->wait_ns;
+    if (launch_stack_decode(a, h->num_sms, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  // layer by layer: layer l reads the previous output, writes the next buffer
+  uint8_t* tr = static_cast<uint8_t*>(x_trace);
+  if (tr && cudaMemcpyAsync(tr, x, nb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  const void* cur = x;
+  for (int l = 0; l < h->L; ++l) {
+    void* dst = tr ? static_cast<void*>(tr + (size_t)(l + 1) * nb) : (l == h->L - 1 ? y : h->chain[l & 1]);
+    int32_t* it = idx_trace ? idx_trace + (size_t)l * T * c.top_k : nullptr;
+    float* gt = gate_trace ? gate_trace + (size_t)l * T * c.top_k : nullptr;
+    const moe_status st = moe_forward(h->layers[l], cur, T, dst, it, gt, stream);
+    if (st != MOE_OK) return st;
+    cur = dst;
+  }
+  if (tr && cudaMemcpyAsync(y, cur, nb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_stack_check(moe_stack_handle h, cudaStream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, h->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word && cudaMemset(h->err, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status worst = (word & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+  for (moe_handle l : h->layers) {
+    const moe_status st = moe_check(l, stream);
+    if (worst == MOE_OK) worst = st;
+  }
+  return worst;
+}
+
+}  // extern "C"

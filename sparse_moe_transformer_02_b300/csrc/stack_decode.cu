@@ -1,0 +1,690 @@
+// Persistent decode kernel over a whole stack of MoE layers: one launch runs
+// every layer for a small batch of tokens.
+//
+// The pages describe a decode "megakernel" that fuses the whole decode
+// forward pass into one kernel (evermx.com review, Feature Overview, "Kernels
+// and inference"); for the MoE layers of a stack (47 of them in Flint, joined
+// by residual adds: swarmz.net, section "The architecture, in plain terms")
+// this is its counterpart on B300.  Per layer and token batch (T <= 8) the
+// work is a few tens of MB of weights, a few microseconds of HBM time, so a
+// launch per kernel per layer would cost as much as the weight stream; here
+// the layers follow each other inside one cooperative grid (one CTA per SM)
+// separated by grid-wide barriers.
+//
+// Per layer three phases, each ending in a grid barrier:
+//   A  router logits (fp32, one warp per expert row, plain loads) and the
+//      shared expert's gate/up row groups (need no routing);
+//   B  top-k, gates and grouping, computed by every CTA for itself from the
+//      logits (identical inputs and instructions, so every CTA holds the same
+//      routing), then the routed experts' gate/up row groups, split evenly
+//      over the CTAs;
+//   C  down projection: CTA b owns output rows [16 rb, 16 rb + 16) for
+//      rb = b, b + G, ...; its consumer warps take the shared expert and the
+//      active experts in turn, weight their rows by the gates and the CTA sums
+//      the warps in a fixed order (deterministic), adds the residual x and
+//      rounds the new residual stream to bf16.
+//
+// Inside a CTA one producer warp streams weights with 1-D bulk copies into a
+// 16-stage shared-memory ring (two stages per consumer warp, each stage 16
+// rows x 256 values padded to 528 bytes per row so ldmatrix rows hit distinct
+// banks); eight consumer warps multiply on the tensor pipe (mma.sync
+// m16n8k16, bf16 in, fp32 accumulate) with the activations (x or h, staged
+// once per phase in shared memory) as the 8-column B operand.  A gate/up row
+// group is 8 gate rows + 8 up rows of one expert, its K segments spread over
+// the consumer warps and summed through shared memory in warp order; the
+// thread holding gate row f and up row f of a token applies SwiGLU.  The
+// producer does not wait for barriers: it runs ahead into the next phase's
+// weights as far as the ring allows (phase A needs no routing; phases B and C
+// wait only for this CTA's routing), so the weights of the next phase are in
+// flight while the grid synchronises.
+//
+// Every wait is bounded: the ring, the routing hand-off and the grid barrier
+// give up after the limit, set the device error word (timeout bit) and the
+// CTA unwinds, draining its bulk copies first.
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kSdThreads = 32 * (1 + kSdConsumers);
+constexpr int kSdStages = 2 * kSdConsumers;         // two per consumer warp
+constexpr int kSdSeg = 256;                         // values per row segment
+constexpr int kSdRowPitch = kSdSeg * 2 + 16;        // 528 bytes
+constexpr int kSdStageBytes = 16 * kSdRowPitch;     // 8448 bytes
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Named barrier that also ORs a flag over the participating threads: every
+// thread gets the same answer, so a decision taken on it is uniform even if
+// the abort flag changes meanwhile (the producer warp may set it at any time).
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Shared-memory layout (byte offsets), computed identically on host and device.
+struct SdLayout {
+  uint32_t stages, bars, route_bar, abort, xs, red, yw, rt, total;
+  uint32_t x_pitch, h_pitch;
+};
+__host__ __device__ inline SdLayout sd_layout(int d, int Fmax, int k) {
+  SdLayout L;
+  L.x_pitch = (uint32_t)d * 2 + 16;
+  L.h_pitch = (uint32_t)Fmax * 2 + 16;
+  uint32_t o = 0;
+  L.stages = o; o += kSdStages * kSdStageBytes;
+  L.bars = o;   o += 2 * kSdStages * 8;
+  L.route_bar = o; o += 8;
+  L.abort = o;  o += 8;
+  L.xs = o;                                          // x rows (phases A, B) or h rows (phase C)
+  const uint32_t xsz = kSdMaxT * L.x_pitch, hsz = (uint32_t)kSdMaxT * (k + 1) * L.h_pitch;
+  o += (xsz > hsz ? xsz : hsz);
+  o = (o + 15) & ~15u;
+  L.red = o;    o += 2 * kSdConsumers * 32 * 4 * 4;   // double-buffered partial sums of a row group
+  L.yw = o;     o += kSdConsumers * 16 * kSdMaxT * 4; // per-warp down-projection sums of a row block
+  L.rt = o;     o += 4096;                            // routing tables (below)
+  L.total = o;
+  return L;
+}
+// Routing tables inside L.rt (ints / floats):
+//   sel_e[64], sel_g[64]  top-k of each token, slot s = t k + j
+//   slot_tok[64], slot_gate[64]  grouped slots (experts ascending, tokens ascending)
+//   act_e[65], act_off[65], n_act  active experts, first grouped slot of each
+//   cnt[256], off[256]  per-expert counts / offsets (grouping scratch)
+struct Rt {
+  int* sel_e; float* sel_g; int* slot_tok; float* slot_gate; int* act_e; int* act_off; int* n_act;
+  int* cnt; int* off;
+};
+__device__ __forceinline__ Rt rt_of(uint8_t* base) {
+  int* p = reinterpret_cast<int*>(base);
+  Rt r;
+  r.sel_e = p; p += 64;
+  r.sel_g = reinterpret_cast<float*>(p); p += 64;
+  r.slot_tok = p; p += 64;
+  r.slot_gate = reinterpret_cast<float*>(p); p += 64;
+  r.act_e = p; p += 65;
+  r.act_off = p; p += 65;
+  r.n_act = p; p += 2;
+  r.cnt = p; p += 256;
+  r.off = p;
+  return r;
+}
+
+// Grid barrier: every consumer thread of every CTA calls it; one thread per
+// CTA arrives on the counter (release) and waits for the target (acquire).
+__device__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, volatile int* abort_flag) {
+  named_sync(1, 32 * kSdConsumers);
+  bool bad = false;
+  if (threadIdx.x == 32) {
+    if (!*abort_flag) {
+      __threadfence();
+      atomicAdd(ctr, 1u);
+      if (!counter_wait(ctr, target, wc)) {
+        *abort_flag = 1;
+        bad = true;
+      }
+    }
+  }
+  return !named_sync_or(1, 32 * kSdConsumers, bad || *abort_flag != 0);
+}
+
+// The producer's view of the ring: consumer c owns stages 2c, 2c + 1 and
+// takes them alternately; its m-th stage has phase parity (m >> 1) & 1.
+struct SdOwner {
+  int m[kSdConsumers];
+  uint32_t last_par[kSdStages];
+  uint32_t used;
+};
+
+// One CTA's walk over the stack: the producer (prod = true) issues every
+// stage, the consumers process them, both in the same order.
+struct SdCtx {
+  StackArgs a;
+  SdLayout L;
+  uint8_t* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* route_bar;
+  volatile int* abort_flag;
+  Rt rt;
+  WaitCtl wc;
+  int G, b, warp, lane;
+};
+
+// ---------------------------------------------------------------- producer
+struct Producer {
+  SdCtx& c;
+  SdOwner own;
+  uint64_t pol;
+  __device__ explicit Producer(SdCtx& ctx) : c(ctx) {
+    for (int i = 0; i < kSdConsumers; ++i) own.m[i] = 0;
+    own.used = 0;
+    pol = policy_evict_first();
+  }
+  // Next stage of consumer w (bounded wait for it to be free); -1 on abort.
+  __device__ int next(int w) {
+    int s = -1;
+    if (c.lane == 0) {
+      const int m = own.m[w];
+      s = w * 2 + (m & 1);
+      if (!mbar_wait(&c.empty[s], ((m >> 1) & 1) ^ 1, c.wc)) s = -1;
+      else {
+        own.last_par[s] = (m >> 1) & 1;
+        own.used |= 1u << s;
+      }
+    }
+    own.m[w]++;
+    return __shfl_sync(kFull, s, 0);
+  }
+  // 16 rows of 256 bf16 values: rows 0-7 from p0 + r * pitch, rows 8-15 from p1 + r * pitch.
+  __device__ bool issue16(int w, const __nv_bfloat16* p0, const __nv_bfloat16* p1, size_t pitch) {
+    const int s = next(w);
+    if (s < 0) return false;
+    if (c.lane == 0) mbar_arrive_expect_tx(&c.full[s], 16 * kSdSeg * 2);
+    __syncwarp();
+    if (c.lane < 16) {
+      const __nv_bfloat16* src = c.lane < 8 ? p0 + (size_t)c.lane * pitch : p1 + (size_t)(c.lane - 8) * pitch;
+      bulk_g2s_hint(c.smem + c.L.stages + s * kSdStageBytes + c.lane * kSdRowPitch, src, kSdSeg * 2, &c.full[s], pol);
+    }
+    return true;
+  }
+  __device__ void drain() {
+    if (c.lane != 0) return;
+    for (int s = 0; s < kSdStages; ++s)
+      if (own.used & (1u << s)) drain_wait(&c.full[s], own.last_par[s], c.wc.limit_ns);
+  }
+};
+
+// Gate/up row group g of an expert: gate rows 8g..8g+7 and up rows 8g..8g+7,
+// K segments spread over the consumers (segment s -> consumer s % 8).
+__device__ bool produce_gu(Producer& P, const __nv_bfloat16* wg, const __nv_bfloat16* wu, int g, int d) {
+  const int KC = d / kSdSeg;
+  for (int s = 0; s < KC; ++s)
+    if (!P.issue16(s % kSdConsumers, wg + (size_t)g * 8 * d + s * kSdSeg, wu + (size_t)g * 8 * d + s * kSdSeg, d))
+      return false;
+  return true;
+}
+
+__device__ void run_producer(SdCtx& c) {
+  const StackArgs& a = c.a;
+  Producer P(c);
+  const int nsh = a.Fs / 8;
+  bool ok = true;
+  for (int l = 0; l < a.L && ok; ++l) {
+    const StackLayerPtrs& W = a.layers[l];
+    // phase A: the shared expert's row groups of this CTA
+    for (int g = c.b; g < nsh && ok; g += c.G) ok = produce_gu(P, W.sg, W.su, g, a.d);
+    if (!ok) break;
+    // this CTA's routing for layer l
+    int rdy = 1;
+    if (c.lane == 0) rdy = mbar_wait(c.route_bar, l & 1, c.wc) ? 1 : 0;
+    rdy = __shfl_sync(kFull, rdy, 0);
+    if (!rdy) { ok = false; break; }
+    const int U = *c.rt.n_act;
+    // phase B: routed row groups, an even share per CTA
+    const int ngrp = a.F / 8, n = U * ngrp;
+    const int lo = (int)(((long long)n * c.b) / c.G), hi = (int)(((long long)n * (c.b + 1)) / c.G);
+    for (int u = lo; u < hi && ok; ++u) {
+      const int e = c.rt.act_e[u / ngrp];
+      ok = produce_gu(P, W.wg + (size_t)e * a.F * a.d, W.wu + (size_t)e * a.F * a.d, u % ngrp, a.d);
+    }
+    // phase C: the down rows of this CTA's row blocks, unit j -> consumer j % 8
+    const int has_sh = a.Fs > 0 ? 1 : 0;
+    for (int rb = c.b; rb < a.d / 16 && ok; rb += c.G) {
+      for (int j = 0; j < U + has_sh && ok; ++j) {
+        const bool sh = has_sh && j == 0;
+        const int Fe = sh ? a.Fs : a.F;
+        const __nv_bfloat16* wd = sh ? W.sd : W.wd + (size_t)c.rt.act_e[j - has_sh] * a.d * a.F;
+        for (int s = 0; s < Fe / kSdSeg && ok; ++s) {
+          const __nv_bfloat16* p = wd + (size_t)rb * 16 * Fe + s * kSdSeg;
+          ok = P.issue16(j % kSdConsumers, p, p + (size_t)8 * Fe, Fe);
+        }
+      }
+    }
+  }
+  if (!ok) P.drain();
+}
+
+// ---------------------------------------------------------------- consumers
+// Wait for this consumer's next stage; returns its shared address or 0 on abort.
+struct Cons {
+  SdCtx& c;
+  int m = 0;
+  __device__ explicit Cons(SdCtx& ctx) : c(ctx) {}
+  __device__ uint32_t wait() {
+    const int s = c.warp - 1;
+    const int st = s * 2 + (m & 1);
+    int ok = 1;
+    if (c.lane == 0) ok = mbar_wait(&c.full[st], (m >> 1) & 1, c.wc) ? 1 : 0;
+    ok = __shfl_sync(kFull, ok, 0);
+    if (!ok) return 0;
+    while (!mbar_try_wait(&c.full[st], (m >> 1) & 1)) {
+    }
+    cur = st;
+    return smem_u32(c.smem + c.L.stages + st * kSdStageBytes);
+  }
+  __device__ void release() {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(&c.empty[cur]);
+    ++m;
+  }
+  int cur = 0;
+};
+
+// acc += stage (16 rows x 256 values) x B, B row n = brow(n) (k offset k0, 8 columns).
+__device__ __forceinline__ void mma_stage(uint32_t st, uint32_t bbase, uint32_t bpitch, const int (&bidx)[1],
+                                          int k0, int lane, float (&acc)[4]) {
+  const uint32_t lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
+  const uint32_t a0 = st + lrow * kSdRowPitch + lcol * 2;
+  const uint32_t b0a = bbase + (uint32_t)bidx[0] * bpitch + (uint32_t)(k0 + (lane & 3) * 2) * 2;
+#pragma unroll 4
+  for (int kk = 0; kk < kSdSeg / 16; ++kk) {
+    uint32_t af[4];
+    ldsm_x4(a0 + kk * 32, af);
+    const uint32_t b0 = lds32(b0a + kk * 32), b1 = lds32(b0a + kk * 32 + 16);
+    mma_bf16(acc, af, b0, b1);
+  }
+}
+
+// One gate/up row group: the consumer's K segments, the cross-warp sum in
+// warp order, SwiGLU, h rows of the group's tokens.  rows_tok(n) = x row of
+// column n (n < cnt), hslot(n) = h row to write.  rg counts row groups (for
+// the double-buffered partials and the finalising warp).
+template <typename Tok, typename Slot>
+__device__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int cnt, int rg, Tok&& rows_tok, Slot&& hslot,
+                           __nv_bfloat16* h, int Fmax) {
+  const int w = c.warp - 1, lane = c.lane, KC = d / kSdSeg;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int n = lane >> 2;
+  int bidx[1] = {rows_tok(n < cnt ? n : 0)};
+  const uint32_t xs = smem_u32(c.smem + c.L.xs);
+  // A failed wait has set the CTA's abort flag; this warp then skips its work
+  // but still reaches the barrier, after which every warp leaves together
+  // (a warp that left early would strand the others in bar.sync).
+  for (int s = w; s < KC; s += kSdConsumers) {
+    const uint32_t st = C.wait();
+    if (!st) break;
+    mma_stage(st, xs, c.L.x_pitch, bidx, s * kSdSeg, lane, acc);
+    C.release();
+  }
+  float* red = reinterpret_cast<float*>(c.smem + c.L.red) + (size_t)(rg & 1) * kSdConsumers * 128;
+  reinterpret_cast<float4*>(red)[w * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  if (named_sync_or(2, 32 * kSdConsumers, *c.abort_flag != 0)) return false;
+  if (w == (rg % kSdConsumers)) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const int nw = KC < kSdConsumers ? KC : kSdConsumers;
+    for (int ww = 0; ww < nw; ++ww) {
+      const float4 p = reinterpret_cast<const float4*>(red)[ww * 32 + lane];
+      v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+    }
+    const int f = g * 8 + (lane >> 2);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col = (lane & 3) * 2 + q;
+      if (col < cnt) {
+        const float hv = silu_f(v[q]) * v[2 + q];
+        __stcg(reinterpret_cast<unsigned short*>(h) + (size_t)hslot(col) * Fmax + f,
+               __bfloat16_as_ushort(__float2bfloat16_rn(hv)));
+      }
+    }
+  }
+  return true;
+}
+
+// Top-k of token t (one warp): larger logit first, lower expert index first on
+// equal logits; gates = softmax of the selected logits.
+__device__ void topk_token(const float* logits, int E, int k, int t, Rt& rt, int lane) {
+  uint64_t key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0;
+    if (e < E) {
+      const uint32_t u = __float_as_uint(__ldcg(logits + (size_t)t * E + e));
+      const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      key[i] = ((uint64_t)o << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+    }
+  }
+  float l0 = 0.f, sum = 0.f;
+  float lsel[kMaxTopK];
+  int esel[kMaxTopK];
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (key[i] > best) { best = key[i]; bi = i; }
+    uint64_t wbest = best;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(kFull, wbest, o);
+      wbest = other > wbest ? other : wbest;
+    }
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)(wbest & 0xFFFFFFFFu));
+    if (bi >= 0 && best == wbest) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i == bi) key[i] = 0;
+    }
+    const uint32_t o = (uint32_t)(wbest >> 32);
+    const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    const float lv = __uint_as_float(u);
+    if (j == 0) l0 = lv;
+    lsel[j] = lv;
+    esel[j] = e;
+    sum += expf(lv - l0);
+  }
+  if (lane == 0)
+    for (int j = 0; j < k; ++j) {
+      rt.sel_e[t * k + j] = esel[j];
+      rt.sel_g[t * k + j] = expf(lsel[j] - l0) / sum;
+    }
+}
+
+// Grouping of the T k slots by expert (one warp): active experts ascending,
+// slots of one expert in (token, j) order.
+__device__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane) {
+  const int ns = T * k;
+  for (int e = lane; e < 256; e += 32) rt.cnt[e] = 0;
+  __syncwarp();
+  const int s0 = lane, s1 = lane + 32;
+  const bool v0 = s0 < ns, v1 = s1 < ns;
+  const int e0 = v0 ? rt.sel_e[s0] : -1 - lane, e1 = v1 ? rt.sel_e[s1] : -100 - lane;
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned m0 = __match_any_sync(kFull, e0);
+  const int r0 = __popc(m0 & lt);
+  if (v0 && r0 == 0) rt.cnt[e0] = __popc(m0);
+  __syncwarp();
+  const unsigned m1 = __match_any_sync(kFull, e1);
+  const int r1 = (v1 ? rt.cnt[e1] : 0) + __popc(m1 & lt);
+  __syncwarp();
+  if (v1 && __popc(m1 & lt) == 0) rt.cnt[e1] += __popc(m1);
+  __syncwarp();
+  // exclusive scans over the experts (8 per lane): slot offsets and active ranks
+  int c[8], tot = 0, act = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    c[i] = e < E ? rt.cnt[e] : 0;
+    tot += c[i];
+    act += c[i] > 0;
+  }
+  int it = tot, ia = act;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(kFull, it, o), y = __shfl_up_sync(kFull, ia, o);
+    if (lane >= o) { it += x; ia += y; }
+  }
+  int off = it - tot, rank = ia - act;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    if (e < E) {
+      rt.off[e] = off;
+      if (c[i] > 0) {
+        rt.act_e[rank] = e;
+        rt.act_off[rank] = off;
+        ++rank;
+      }
+    }
+    off += c[i];
+  }
+  if (lane == 31) {
+    rt.act_off[ia] = ns;
+    *rt.n_act = ia;
+  }
+  __syncwarp();
+  if (v0) {
+    const int p = rt.off[e0] + r0;
+    rt.slot_tok[p] = s0 / k;
+    rt.slot_gate[p] = rt.sel_g[s0];
+  }
+  if (v1) {
+    const int p = rt.off[e1] + r1;
+    rt.slot_tok[p] = s1 / k;
+    rt.slot_gate[p] = rt.sel_g[s1];
+  }
+  __syncwarp();
+}
+
+__device__ void run_consumers(SdCtx& c) {
+  const StackArgs& a = c.a;
+  Cons C(c);
+  const int w = c.warp - 1, lane = c.lane, tid = threadIdx.x - 32, NT = 32 * kSdConsumers;
+  const int T = a.T, d = a.d, F = a.F, Fs = a.Fs, E = a.E, k = a.k;
+  const int Fmax = F > Fs ? F : Fs;
+  const int has_sh = Fs > 0 ? 1 : 0;
+  const int nsh = Fs / 8;
+  unsigned nbar = 0;
+  int rg = 0;                                  // row groups processed (partials buffer / finaliser)
+  for (int l = 0; l < a.L; ++l) {
+    const StackLayerPtrs& W = a.layers[l];
+    const __nv_bfloat16* xcur = l == 0 ? a.x_in : a.xbuf + (size_t)((l - 1) & 1) * kSdMaxT * d;
+    __nv_bfloat16* xnext = l == a.L - 1 ? a.y_out : a.xbuf + (size_t)(l & 1) * kSdMaxT * d;
+    // stage x (T rows) in shared memory
+    {
+      uint8_t* xs = c.smem + c.L.xs;
+      const int chunks = d / 8;
+      for (int i = tid; i < T * chunks; i += NT) {
+        const int t = i / chunks, q = i % chunks;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(xcur + (size_t)t * d) + q);
+        *reinterpret_cast<uint4*>(xs + t * c.L.x_pitch + q * 16) = v;
+      }
+      if (l == 0 && a.x_trace && c.b == 0)
+        for (int i = tid; i < T * chunks; i += NT)
+          __stcg(reinterpret_cast<uint4*>(a.x_trace) + i, __ldcg(reinterpret_cast<const uint4*>(a.x_in) + i));
+    }
+    named_sync(1, NT);
+    // router rows: expert e on global warp G * 8 - 1 - e (the last CTAs)
+    {
+      const int gw = c.b * kSdConsumers + w, nw = c.G * kSdConsumers;
+      for (int e = nw - 1 - gw; e >= 0 && e < E; e += nw) {
+        const float* wr = W.wr + (size_t)e * d;
+        float acc[kSdMaxT];
+#pragma unroll
+        for (int t = 0; t < kSdMaxT; ++t) acc[t] = 0.f;
+        for (int i0 = lane * 4; i0 < d; i0 += 32 * 4 * 4) {
+          float4 wv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            wv[u] = i < d ? __ldg(reinterpret_cast<const float4*>(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 128;
+            if (i < d) {
+#pragma unroll
+              for (int t = 0; t < kSdMaxT; ++t)
+                if (t < T) {
+                  const uint2 xv = *reinterpret_cast<const uint2*>(c.smem + c.L.xs + t * c.L.x_pitch + i * 2);
+                  const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xFFFF0000u);
+                  const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+                  acc[t] = fmaf(wv[u].x, x0, fmaf(wv[u].y, x1, fmaf(wv[u].z, x2, fmaf(wv[u].w, x3, acc[t]))));
+                }
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kSdMaxT; ++t) {
+          float v = acc[t];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+          if (t < T && lane == 0) __stcg(a.logits + (size_t)t * E + e, v + (W.br ? __ldg(W.br + e) : 0.f));
+        }
+      }
+    }
+    // phase A: shared expert row groups (all T tokens)
+    for (int g = c.b; g < nsh; g += c.G, ++rg)
+      if (!consume_gu(c, C, d, g, T, rg, [&](int n) { return n; }, [&](int n) { return T * k + n; }, a.h, Fmax))
+        return;
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+
+    // routing (every CTA), then hand it to the producer
+    if (w < T) topk_token(a.logits, E, k, w, c.rt, lane);
+    named_sync(1, NT);
+    if (w == 0) group_slots_warp(c.rt, T, k, E, lane);
+    named_sync(1, NT);
+    if (tid == 0) mbar_arrive(c.route_bar);
+    if (c.b == 0 && a.idx_trace)
+      for (int i = tid; i < T * k; i += NT) {
+        a.idx_trace[(size_t)l * T * k + i] = c.rt.sel_e[i];
+        a.gate_trace[(size_t)l * T * k + i] = c.rt.sel_g[i];
+      }
+    const int U = *c.rt.n_act;
+    // phase B: routed row groups
+    {
+      const int ngrp = F / 8, n = U * ngrp;
+      const int lo = (int)(((long long)n * c.b) / c.G), hi = (int)(((long long)n * (c.b + 1)) / c.G);
+      for (int u = lo; u < hi; ++u, ++rg) {
+        const int ai = u / ngrp;
+        const int off = c.rt.act_off[ai], cnt = c.rt.act_off[ai + 1] - off;
+        if (!consume_gu(c, C, d, u % ngrp, cnt, rg, [&](int nn) { return c.rt.slot_tok[off + nn]; },
+                        [&](int nn) { return off + nn; }, a.h, Fmax))
+          return;
+      }
+    }
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+
+    // phase C: stage h (routed slots, then the shared expert's T rows) in shared memory
+    const int nslots = T * k + (has_sh ? T : 0);
+    {
+      uint8_t* hs = c.smem + c.L.xs;
+      const int chunks = Fmax / 8;
+      for (int i = tid; i < nslots * chunks; i += NT) {
+        const int r = i / chunks, q = i % chunks;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.h + (size_t)r * Fmax) + q);
+        *reinterpret_cast<uint4*>(hs + r * c.L.h_pitch + q * 16) = v;
+      }
+    }
+    float* yw = reinterpret_cast<float*>(c.smem + c.L.yw);
+    for (int rb = c.b; rb < d / 16; rb += c.G) {
+      for (int i = tid; i < kSdConsumers * 16 * kSdMaxT; i += NT) yw[i] = 0.f;
+      named_sync(1, NT);
+      for (int j = w; j < U + has_sh; j += kSdConsumers) {
+        const bool sh = has_sh && j == 0;
+        const int ai = j - has_sh;
+        const int off = sh ? T * k : c.rt.act_off[ai];
+        const int cnt = sh ? T : c.rt.act_off[ai + 1] - off;
+        const int Fe = sh ? Fs : F;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int n = lane >> 2;
+        int bidx[1] = {off + (n < cnt ? n : 0)};
+        bool ok = true;
+        for (int s = 0; s < Fe / kSdSeg; ++s) {
+          const uint32_t st = C.wait();
+          if (!st) { ok = false; break; }
+          mma_stage(st, smem_u32(c.smem + c.L.xs), c.L.h_pitch, bidx, s * kSdSeg, lane, acc);
+          C.release();
+        }
+        if (!ok) break;                        // abort: fall through to the barrier below
+        const int row = lane >> 2;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int col = (lane & 3) * 2 + q;
+          if (col < cnt) {
+            const int t = sh ? col : c.rt.slot_tok[off + col];
+            const float gsc = sh ? 1.f : c.rt.slot_gate[off + col];
+            yw[(w * 16 + row) * kSdMaxT + t] += gsc * acc[q];
+            yw[(w * 16 + row + 8) * kSdMaxT + t] += gsc * acc[2 + q];
+          }
+        }
+      }
+      if (named_sync_or(1, NT, *c.abort_flag != 0)) return;
+      for (int i = tid; i < 16 * T; i += NT) {
+        const int row = i / T, t = i % T, r = rb * 16 + row;
+        float y = 0.f;
+        for (int ww = 0; ww < kSdConsumers; ++ww) y += yw[(ww * 16 + row) * kSdMaxT + t];
+        y += __bfloat162float(__ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short*>(xcur) + (size_t)t * d + r)));
+        const unsigned short ob = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+        __stcg(reinterpret_cast<unsigned short*>(xnext) + (size_t)t * d + r, ob);
+        if (a.x_trace)
+          __stcg(reinterpret_cast<unsigned short*>(a.x_trace) + ((size_t)(l + 1) * T + t) * d + r, ob);
+      }
+      named_sync(1, NT);
+    }
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+  }
+}
+
+__global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(StackArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  SdCtx c;
+  c.a = a;
+  const int Fmax = a.F > a.Fs ? a.F : a.Fs;
+  c.L = sd_layout(a.d, Fmax, a.k);
+  c.smem = dsm;
+  c.full = reinterpret_cast<uint64_t*>(dsm + c.L.bars);
+  c.empty = c.full + kSdStages;
+  c.route_bar = reinterpret_cast<uint64_t*>(dsm + c.L.route_bar);
+  c.abort_flag = reinterpret_cast<volatile int*>(dsm + c.L.abort);
+  c.rt = rt_of(dsm + c.L.rt);
+  c.G = gridDim.x;
+  c.b = blockIdx.x;
+  c.warp = threadIdx.x >> 5;
+  c.lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSdStages; ++i) {
+      mbar_init(&c.full[i], 1);
+      mbar_init(&c.empty[i], 1);
+    }
+    mbar_init(c.route_bar, 1);
+    *c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  c.wc = WaitCtl{a.wait_ns, a.err, const_cast<int*>(reinterpret_cast<volatile int*>(c.abort_flag))};
+  if (c.warp == 0) run_producer(c);
+  else run_consumers(c);
+}
+
+}  // namespace
+
+size_t stack_decode_smem_bytes(int d, int F, int Fs, int k) {
+  return sd_layout(d, F > Fs ? F : Fs, k).total;
+}
+
+cudaError_t launch_stack_decode(const StackArgs& a, int num_sms, cudaStream_t s) {
+  const size_t smem = stack_decode_smem_bytes(a.d, a.F, a.Fs, a.k);
+  cudaError_t e = ensure_smem_limit(stack_decode_kernel, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kSdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stack_decode_kernel, a);
+}
+
+}  // namespace moe

@@ -114,8 +114,9 @@ def check_routing(l: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, k: i
 
 
 def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tensor, gate_gpu: torch.Tensor,
-                k: int, fmt: str, residual: bool = False, tokens=None):
-    """Full-layer parity on `tokens` (all when None). Returns a dict of error figures."""
+                k: int, fmt: str, residual: bool = False, tokens=None, enforce: bool = True):
+    """Full-layer parity on `tokens` (all when None). Returns a dict of error figures.
+    With enforce=False the output bounds are measured, not asserted (routing still is)."""
     W = LayerWeights(L)
     xf = _widen(x)
     sel = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
@@ -132,6 +133,13 @@ def check_layer(L: dict, x: np.ndarray, y_gpu: torch.Tensor, idx_gpu: torch.Tens
     rel = float(np.linalg.norm(err) / max(np.linalg.norm(y_ref), 1e-30))
     assert np.all(np.isfinite(yg))
     bound = MAX_ABS + (bf16_ulp(y_ref) if residual and y_gpu.dtype == torch.bfloat16 else 0.0)
-    assert np.all(np.abs(err) <= bound), (max_abs, rel)
-    assert rel <= REL_L2[fmt], (max_abs, rel)
-    return {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near, "gate_err": stats["gate_err"]}
+    over = float(np.max(np.abs(err) / bound))
+    moe_ref = y_ref - xs if residual else y_ref
+    out = {"max_abs": max_abs, "rel_l2": rel, "near_ties": n_near, "gate_err": stats["gate_err"],
+           "err_over_bound": over, "x_rms": float(np.sqrt(np.mean(xs ** 2))),
+           "moe_rms": float(np.sqrt(np.mean(moe_ref ** 2))), "moe_max": float(np.max(np.abs(moe_ref))),
+           "y_max": float(np.max(np.abs(y_ref)))}
+    if enforce:
+        assert np.all(np.abs(err) <= bound), (max_abs, rel)
+        assert rel <= REL_L2[fmt], (max_abs, rel)
+    return out

@@ -45,6 +45,7 @@ def test_stack47_zipf_layers_teacher_forced():
     sample[-1] = T - 1
     x_ref = None                           # the oracle's own chain on the sampled tokens
     worst = {"max_abs": 0.0, "rel_l2": 0.0, "gate_err": 0.0, "near_ties": 0}
+    per_layer = []
     for l in range(N_LAYERS):
         dev = I.make_layer_torch(spec, seed=seed, layer=l, device="cuda")
         layer = B.layer_from_spec(spec, dev, T)
@@ -55,7 +56,9 @@ def test_stack47_zipf_layers_teacher_forced():
         assert layer.check() == B.MOE_OK, l
         L = host_layer(dev)
         x_np = gpu_bits(x)
-        r = check_layer(L, x_np, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=sample)
+        r = check_layer(L, x_np, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=sample, enforce=False)
+        print("layer", l, {kk: (round(v, 6) if isinstance(v, float) else v) for kk, v in r.items()}, flush=True)
+        per_layer.append(r)
         for key in ("max_abs", "rel_l2", "gate_err"):
             worst[key] = max(worst[key], r[key])
         worst["near_ties"] += r["near_ties"]
@@ -70,3 +73,5 @@ def test_stack47_zipf_layers_teacher_forced():
     rel = float(np.linalg.norm(yg - x_ref) / np.linalg.norm(x_ref))
     print("stack47 per-layer worst", worst, "| chained rel-L2 after 47 layers", rel)
     assert np.all(np.isfinite(yg))
+    for l, r in enumerate(per_layer):
+        assert r["err_over_bound"] <= 1.0 and r["rel_l2"] <= 1e-2, (l, r)
