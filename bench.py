@@ -647,6 +647,26 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
+def run_only(args):
+    """One sweep entry alone (for profiling): prints its result as a JSON line."""
+    import torch
+    from sparse_moe_transformer_02_b300 import build
+    build.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    if args.only in STACK_DECODE:
+        spec, wts = make_layer_set("stack", args.layers or WORKLOADS["stack47"][2], device, seed=args.seed)
+        r = measure_stack_decode(args, args.only, spec, wts, STACK_DECODE[args.only], device, stream)
+    elif args.only in HEAD:
+        r = measure_head(args, args.only, HEAD[args.only], device, stream)
+    else:
+        kind, T, n, chain = WORKLOADS[args.only]
+        spec, wts = make_layer_set(kind, args.layers or n, device, seed=args.seed)
+        r = measure(args, args.only, spec, kind, wts, T, chain, device, stream, 0, 1, 0, True, False)
+    print(json.dumps(r), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm (the CPU oracle)
 def run_reference(args, rank):
     if rank != 0:
@@ -699,6 +719,8 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--only", default=None, choices=sorted(list(WORKLOADS) + list(STACK_DECODE) + list(HEAD)),
+                    help="run one sweep entry alone and print its result (profiling)")
     ap.add_argument("--rank-selftest", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -711,6 +733,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.only:
+        run_only(args)
         return
     import torch.distributed as dist
     if args.rank_selftest:

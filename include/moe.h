@@ -319,7 +319,7 @@ typedef struct moe_head* moe_head_handle;      /* opaque, owned by the library *
  * codes [vocab][d / 2] bytes (element 2i in the low nibble), scales
  * [vocab][d / 16] e4m3 codes, tscale [1] fp32: device memory, borrowed for
  * the handle's lifetime, codes and scales 16-byte aligned.  d a multiple of
- * 512, vocab a multiple of 16.  wait_timeout_ms limits every device-side wait
+ * 256, vocab a multiple of 64.  wait_timeout_ms limits every device-side wait
  * (0 = 2000 ms).  Errors: MOE_ERR_INVALID_ARG (NULL, non-positive sizes,
  * misalignment), MOE_ERR_UNSUPPORTED (shape), MOE_ERR_OOM, MOE_ERR_CUDA.
  */

@@ -8,21 +8,23 @@
 // stream: every code is read once per call and used for at most 8 tokens, so
 // the kernel is built to stream at the HBM rate.
 //
-// One CTA per SM takes a contiguous range of 16-row blocks of W.  A producer
-// warp copies each block in segments of 512 values (16 rows x 256 code bytes
-// and 16 x 32 scale bytes, one bulk copy per row and lane, rows padded so the
-// consumers' loads hit distinct banks) into a ring where every consumer warp
-// owns four stages; eight consumer warps each take whole row blocks.  A
-// consumer decodes codes exactly into f16 in registers (cvt e2m1x2 -> f16x2,
-// times the block scale as f16x2: code x scale has at most 5 significant bits
-// and lies in [2^-10, 2688], so the product is exact) and multiplies them on
-// the tensor pipe (mma.sync m16n8k16, f16 in, fp32 accumulate) against the
-// activations, which every CTA converts once to f16 with an exact power-of-two
-// scale per token (largest |x| into [1, 2)).  The reduction order is permuted
-// the same way in A and B so that a lane decodes one 32-bit word of 8 codes
-// per row (one block, one scale) and loads its 8 activations with one 16-byte
-// load; the sum over the block is unchanged.  The fp32 result is multiplied
-// by the matrix scale and the token's power of two.
+// One CTA per SM takes a contiguous range of 64-row blocks of W.  A producer
+// thread copies each block in segments of 256 values with two TMA tile loads
+// per stage (64 rows x 128 code bytes, 128-byte swizzle; 64 rows x 16 scale
+// bytes) into a ring where every consumer warp owns two stages; eight
+// consumer warps each take whole row blocks (four 16-row tiles).  A consumer
+// decodes codes exactly into f16 in registers (cvt e2m1x2 -> f16x2, times the
+// block scale as f16x2: code x scale has at most 5 significant bits and lies
+// in [2^-10, 2688], so the product is exact) and multiplies them on the tensor
+// pipe (mma.sync m16n8k16, f16 in, fp32 accumulate) against the activations,
+// which every CTA converts once to f16 with an exact power-of-two scale per
+// token (largest |x| into [1, 2)).  The reduction order is permuted the same
+// way in A and B so that a lane decodes one 32-bit word of 8 codes per row
+// (one block, one scale) and loads its 8 activations with one 16-byte load,
+// shared by the four tiles; the sum over the block is unchanged.  The fp32
+// result is multiplied by the matrix scale and the token's power of two.
+// (Copying the rows with many small 1-D bulk copies instead left the copy
+// engine, not HBM, as the limit: about 40 ns per copy whatever its size.)
 //
 // Every wait is bounded: on expiry the kernel records the timeout in the error
 // word, drains its copies and returns.
@@ -35,13 +37,14 @@ namespace moe {
 namespace {
 
 constexpr int kHdThreads = 32 * (1 + kHdConsumers);
-constexpr int kHdPer = 4;                                // stages per consumer
+constexpr int kHdPer = 2;                                // stages per consumer
 constexpr int kHdStages = kHdConsumers * kHdPer;
-constexpr int kHdKs = 512;                               // values per segment
-constexpr int kHdCodePitch = kHdKs / 2 + 16;             // 272 bytes per row
-constexpr int kHdScalePitch = kHdKs / 16 + 16;           // 48 bytes per row
-constexpr int kHdStageBytes = 16 * (kHdCodePitch + kHdScalePitch);   // 5120
+constexpr int kHdRows = 64;                              // rows per block
+constexpr int kHdKs = 256;                               // values per segment
+constexpr int kHdCodeBytes = kHdRows * kHdKs / 2;        // 8192: 64 rows x 128 bytes, 128-byte swizzle
+constexpr int kHdStageBytes = kHdCodeBytes + kHdRows * kHdKs / 16;   // + 64 rows x 16 scale bytes = 9216
 constexpr uint32_t kAll = 0xFFFFFFFFu;
+static_assert(kHdStageBytes % 1024 == 0, "stages keep the 1024-byte alignment the swizzle needs");
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -61,6 +64,7 @@ __device__ __forceinline__ uint32_t e4m3_dup_f16x2(uint32_t byte) {
 struct HdLayout {
   uint32_t stages, bars, abort, xs, xscale, total, x_pitch;
 };
+// Offsets from the 1024-aligned base (the allocation has 1024 bytes of slack).
 __host__ __device__ inline HdLayout hd_layout(int d) {
   HdLayout L;
   L.x_pitch = (uint32_t)d * 2 + 64;   // 16-byte loads of 8 rows x 4 lanes hit distinct bank groups
@@ -70,12 +74,13 @@ __host__ __device__ inline HdLayout hd_layout(int d) {
   L.abort = o;  o += 16;
   L.xs = o;     o += kHdMaxT * L.x_pitch;
   L.xscale = o; o += kHdMaxT * 4;
-  L.total = (o + 15) & ~15u;
+  L.total = ((o + 15) & ~15u) + 1024;
   return L;
 }
 
-__global__ void __launch_bounds__(kHdThreads, 1) lm_head_kernel(HeadArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];
+__global__ void __launch_bounds__(kHdThreads, 1) lm_head_kernel(const __grid_constant__ HeadArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm_raw[];
+  uint8_t* dsm = dsm_raw + ((1024 - (smem_u32(dsm_raw) & 1023)) & 1023);
   const HdLayout L = hd_layout(a.d);
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm + L.bars);
   uint64_t* empty = full + kHdStages;
@@ -92,44 +97,41 @@ __global__ void __launch_bounds__(kHdThreads, 1) lm_head_kernel(HeadArgs a) {
   __syncthreads();
   const WaitCtl wc{a.wait_ns, a.err, abort_flag};
   const int G = gridDim.x, b = blockIdx.x, d = a.d, KS = d / kHdKs;
-  const int nblk = a.V / 16;
+  const int nblk = a.V / kHdRows;
   const int lo = (int)(((long long)nblk * b) / G), hi = (int)(((long long)nblk * (b + 1)) / G);
 
   if (warp == 0) {
-    // producer: block lo + i goes to consumer i % 8, its segments in order
+    // producer (one thread): block lo + i goes to consumer i % 8
+    if (lane != 0) return;
+    tma_prefetch_desc(&a.tm_codes);
+    tma_prefetch_desc(&a.tm_scales);
     const uint64_t pol = policy_evict_first();
     int m[kHdConsumers];
     for (int i = 0; i < kHdConsumers; ++i) m[i] = 0;
     uint32_t used = 0, last_par[kHdStages];
     bool ok = true;
-    for (int rb = lo; rb < hi && ok; ++rb) {
-      const int w = (rb - lo) % kHdConsumers;
-      for (int s = 0; s < KS && ok; ++s) {
-        const int mm = m[w]++;
-        const int st = w * kHdPer + (mm % kHdPer);
-        const uint32_t par = (mm / kHdPer) & 1;
-        int good = 1;
-        if (lane == 0) {
-          good = mbar_wait(&empty[st], par ^ 1, wc) ? 1 : 0;
-          if (good) {
-            last_par[st] = par;
-            used |= 1u << st;
-            mbar_arrive_expect_tx(&full[st], 16 * (kHdKs / 2 + kHdKs / 16));
-          }
+    // Rounds of up to 8 blocks, one per consumer; within a round the segments
+    // go out segment by segment across the consumers, so every consumer's two
+    // stages stay filled (issuing a whole block before the next would stall
+    // on the first consumer's ring while the others sit empty).
+    for (int r0 = lo; r0 < hi && ok; r0 += kHdConsumers) {
+      const int nb = hi - r0 < kHdConsumers ? hi - r0 : kHdConsumers;
+      for (int s = 0; s < KS && ok; ++s)
+        for (int w = 0; w < nb; ++w) {
+          const int rb = r0 + w;
+          const int mm = m[w]++;
+          const int st = w * kHdPer + (mm % kHdPer);
+          const uint32_t par = (mm / kHdPer) & 1;
+          if (!mbar_wait(&empty[st], par ^ 1, wc)) { ok = false; break; }
+          last_par[st] = par;
+          used |= 1u << st;
+          uint8_t* sp = dsm + L.stages + st * kHdStageBytes;
+          mbar_arrive_expect_tx(&full[st], kHdStageBytes);
+          tma_load_2d_hint(sp, &a.tm_codes, s * (kHdKs / 2), rb * kHdRows, &full[st], pol);
+          tma_load_2d_hint(sp + kHdCodeBytes, &a.tm_scales, s * (kHdKs / 16), rb * kHdRows, &full[st], pol);
         }
-        good = __shfl_sync(kAll, good, 0);
-        if (!good) { ok = false; break; }
-        uint8_t* sp = dsm + L.stages + st * kHdStageBytes;
-        const size_t row = (size_t)rb * 16 + (lane & 15);
-        if (lane < 16)
-          bulk_g2s_hint(sp + lane * kHdCodePitch, a.codes + row * (d / 2) + (size_t)s * (kHdKs / 2), kHdKs / 2,
-                        &full[st], pol);
-        else
-          bulk_g2s_hint(sp + 16 * kHdCodePitch + (lane - 16) * kHdScalePitch,
-                        a.scales + row * (d / 16) + (size_t)s * (kHdKs / 16), kHdKs / 16, &full[st], pol);
-      }
     }
-    if (!ok && lane == 0)
+    if (!ok)
       for (int st = 0; st < kHdStages; ++st)
         if (used & (1u << st)) drain_wait(&full[st], last_par[st], a.wait_ns);
     return;
@@ -161,7 +163,9 @@ __global__ void __launch_bounds__(kHdThreads, 1) lm_head_kernel(HeadArgs a) {
   const uint32_t xrow = smem_u32(xs) + (uint32_t)(g < T ? g : 0) * L.x_pitch + (uint32_t)t * 16;
   int mm = 0;
   for (int rb = lo + w; rb < hi; rb += kHdConsumers) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     bool ok = true;
     for (int s = 0; s < KS; ++s, ++mm) {
       const int st = w * kHdPer + (mm % kHdPer);
@@ -173,46 +177,53 @@ __global__ void __launch_bounds__(kHdThreads, 1) lm_head_kernel(HeadArgs a) {
       while (!mbar_try_wait(&full[st], par)) {
       }
       const uint32_t sp = smem_u32(dsm + L.stages + st * kHdStageBytes);
-      const uint32_t cg = sp + g * kHdCodePitch + t * 4, cg8 = cg + 8 * kHdCodePitch;
-      const uint32_t sg = sp + 16 * kHdCodePitch + g * kHdScalePitch + (t >> 1);
-      const uint32_t sg8 = sg + 8 * kHdScalePitch;
+      // row 16 j + g (and + 8) of the block: codes line r * 128 with 16-byte
+      // chunk q stored at q ^ (r & 7) = q ^ g; scales 16 bytes per row
+      const uint32_t cbase = sp + g * 128 + t * 4, sbase = sp + kHdCodeBytes + g * 16 + (t >> 1);
       const uint32_t xk = xrow + (uint32_t)s * kHdKs * 2;
-#pragma unroll 4
+#pragma unroll 2
       for (int q = 0; q < kHdKs / 32; ++q) {
-        uint32_t w0, w8, s0, s8;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(cg + q * 16));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w8) : "r"(cg8 + q * 16));
-        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(s0) : "r"(sg + q * 2));
-        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(s8) : "r"(sg8 + q * 2));
         uint4 xv;
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
                      : "r"(xk + q * 64));
-        uint32_t d0[4], d8[4];
-        e2m1x8_f16x2(w0, d0);
-        e2m1x8_f16x2(w8, d8);
-        const uint32_t sc0 = e4m3_dup_f16x2(s0), sc8 = e4m3_dup_f16x2(s8);
+        const uint32_t coff = (uint32_t)((q ^ g) << 4);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          d0[i] = hmul2(d0[i], sc0);
-          d8[i] = hmul2(d8[i], sc8);
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w0, w8, s0, s8;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(cbase + j * 2048 + coff));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w8) : "r"(cbase + j * 2048 + 1024 + coff));
+          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(s0) : "r"(sbase + j * 256 + q * 2));
+          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(s8) : "r"(sbase + j * 256 + 128 + q * 2));
+          uint32_t d0[4], d8[4];
+          e2m1x8_f16x2(w0, d0);
+          e2m1x8_f16x2(w8, d8);
+          const uint32_t sc0 = e4m3_dup_f16x2(s0), sc8 = e4m3_dup_f16x2(s8);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            d0[i] = hmul2(d0[i], sc0);
+            d8[i] = hmul2(d8[i], sc8);
+          }
+          mma_f16(acc[j], d0[0], d8[0], d0[1], d8[1], xv.x, xv.y);
+          mma_f16(acc[j], d0[2], d8[2], d0[3], d8[3], xv.z, xv.w);
         }
-        mma_f16(acc, d0[0], d8[0], d0[1], d8[1], xv.x, xv.y);
-        mma_f16(acc, d0[2], d8[2], d0[3], d8[3], xv.z, xv.w);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if (!ok) return;
     const float ts = __ldg(a.tscale);
-    const int row = rb * 16 + g;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int n = t * 2 + q;
-      if (n < T) {
-        const float f = ts * xscale[n];
-        a.logits[(size_t)n * a.V + row] = acc[q] * f;
-        a.logits[(size_t)n * a.V + row + 8] = acc[2 + q] * f;
+    for (int j = 0; j < 4; ++j) {
+      const int row = rb * kHdRows + j * 16 + g;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = t * 2 + q;
+        if (n < T) {
+          const float f = ts * xscale[n];
+          a.logits[(size_t)n * a.V + row] = acc[j][q] * f;
+          a.logits[(size_t)n * a.V + row + 8] = acc[j][2 + q] * f;
+        }
       }
     }
   }
@@ -240,6 +251,7 @@ cudaError_t launch_lm_head(const HeadArgs& a, int num_sms, cudaStream_t s) {
 using namespace moe;
 
 struct moe_head {
+  CUtensorMap tm_codes, tm_scales;
   int d = 0, V = 0, max_tokens = 0, num_sms = 0;
   const uint8_t* codes = nullptr;
   const uint8_t* scales = nullptr;
@@ -258,7 +270,7 @@ moe_status moe_head_create(int32_t d, int32_t vocab, int32_t max_tokens, const u
   if (d <= 0 || vocab <= 0 || max_tokens <= 0 || wait_timeout_ms < 0) return MOE_ERR_INVALID_ARG;
   if (!codes || !scales || !tscale || mis(codes) || mis(scales) || (reinterpret_cast<uintptr_t>(tscale) & 3u))
     return MOE_ERR_INVALID_ARG;
-  if (d % kHdKs != 0 || vocab % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d % kHdKs != 0 || vocab % kHdRows != 0) return MOE_ERR_UNSUPPORTED;
   moe_head* h = new (std::nothrow) moe_head();
   if (!h) return MOE_ERR_OOM;
   int dev = 0, optin = 0;
@@ -285,6 +297,18 @@ moe_status moe_head_create(int32_t d, int32_t vocab, int32_t max_tokens, const u
     delete h;
     return MOE_ERR_CUDA;
   }
+  {
+    const uint64_t cd[2] = {(uint64_t)d / 2, (uint64_t)vocab}, cs[1] = {(uint64_t)d / 2};
+    const uint32_t cb[2] = {kHdKs / 2, kHdRows};
+    const uint64_t sd[2] = {(uint64_t)d / 16, (uint64_t)vocab}, ss[1] = {(uint64_t)d / 16};
+    const uint32_t sb[2] = {kHdKs / 16, kHdRows};
+    if (!encode_tiled(&h->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, codes, cd, cs, cb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&h->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, scales, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      cudaFree(e);
+      delete h;
+      return MOE_ERR_CUDA;
+    }
+  }
   h->err = static_cast<unsigned*>(e);
   h->d = d;
   h->V = vocab;
@@ -305,6 +329,8 @@ moe_status moe_head_forward(moe_head_handle h, const void* x, int32_t T, float* 
     return MOE_ERR_INVALID_ARG;
   for (int t0 = 0; t0 < T; t0 += kHdMaxT) {
     HeadArgs a;
+    a.tm_codes = h->tm_codes;
+    a.tm_scales = h->tm_scales;
     a.codes = h->codes;
     a.scales = h->scales;
     a.tscale = h->tscale;

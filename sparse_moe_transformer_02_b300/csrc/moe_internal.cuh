@@ -143,6 +143,12 @@ inline cudaError_t ensure_smem_limit(Kernel* func, int bytes) {
   return ensure_smem_limit(reinterpret_cast<const void*>(func), bytes);
 }
 
+// cuTensorMapEncodeTiled (through the runtime's driver entry point): a rank-D
+// tensor with dims[0] contiguous, strides_bytes[i] = byte stride of dimension
+// i + 1, box extents box[], no interleave, L2 256-byte promotion, zero fill.
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
 // Every device allocation of the library goes through here, so that
 // moe_debug_fail_alloc can make the nth one fail.
 cudaError_t dev_malloc(void** p, size_t bytes);
@@ -252,8 +258,14 @@ struct StackLayerPtrs {
   const __nv_bfloat16* sd;          // [d][Fs]
 };
 
+// Tensor maps of one layer for the persistent kernel (device memory, [L][kSdMaps]):
+// 3-D views {64 values, rows, K / 64 chunks} of the bf16 weight stacks, box
+// {64, 8, 4} for gate / up and {64, 16, 4} for down, 128-byte swizzle.
+constexpr int kMapWg = 0, kMapWu = 1, kMapWd = 2, kMapSg = 3, kMapSu = 4, kMapSd = 5, kSdMaps = 6;
+
 struct StackArgs {
   const StackLayerPtrs* layers;     // [L], device memory
+  const CUtensorMap* maps;          // [L][kSdMaps], device memory
   int L;
   const __nv_bfloat16* x_in;        // [T][d]
   __nv_bfloat16* y_out;             // [T][d]
@@ -275,6 +287,8 @@ constexpr int kHdMaxT = 8;          // tokens per launch of the output-layer ker
 constexpr int kHdConsumers = 8;
 
 struct HeadArgs {
+  CUtensorMap tm_codes;             // codes, box 128 bytes x 64 rows, 128-byte swizzle
+  CUtensorMap tm_scales;            // scales, box 16 bytes x 64 rows
   const uint8_t* codes;             // [V][d / 2] e2m1 pairs, element 2i in the low nibble
   const uint8_t* scales;            // [V][d / 16] e4m3 block scales
   const float* tscale;              // [1] matrix scale

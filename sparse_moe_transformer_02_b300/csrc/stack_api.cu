@@ -17,6 +17,7 @@ struct moe_stack {
   std::vector<moe_handle> layers;    // one handle per layer (per-layer path)
   bool persistent = false;           // the persistent kernel serves T <= kSdMaxT
   StackLayerPtrs* d_layers = nullptr;
+  CUtensorMap* d_maps = nullptr;
   void* block = nullptr;             // xbuf, logits, h, barrier counter, error word, chain buffers
   __nv_bfloat16* xbuf = nullptr;
   float* logits = nullptr;
@@ -35,6 +36,7 @@ void free_stack(moe_stack* s) {
   for (moe_handle h : s->layers) moe_destroy(h);
   if (s->block) cudaFree(s->block);
   if (s->d_layers) cudaFree(s->d_layers);
+  if (s->d_maps) cudaFree(s->d_maps);
   delete s;
 }
 
@@ -107,18 +109,46 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
                              static_cast<const __nv_bfloat16*>(w.w_down), static_cast<const __nv_bfloat16*>(w.ws_gate),
                              static_cast<const __nv_bfloat16*>(w.ws_up), static_cast<const __nv_bfloat16*>(w.ws_down)};
     }
+    // 3-D tile views of every weight stack: {64 values, rows, K / 64 chunks}
+    std::vector<CUtensorMap> maps((size_t)n_layers * kSdMaps);
+    auto view = [](CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+      const uint64_t dims[3] = {64, rows, K / 64}, strides[2] = {K * 2, 128};
+      const uint32_t box[3] = {64, box_rows, 4};
+      return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    };
+    const uint64_t E = c.num_experts, d = c.d, F = c.ffn, Fs = c.shared_ffn;
+    bool ok = true;
+    for (int l = 0; l < n_layers && ok; ++l) {
+      const moe_weights& w = layers[l];
+      CUtensorMap* m = &maps[(size_t)l * kSdMaps];
+      ok = view(m + kMapWg, w.w_gate, E * F, d, 8) && view(m + kMapWu, w.w_up, E * F, d, 8) &&
+           view(m + kMapWd, w.w_down, E * d, F, 16);
+      if (ok && Fs > 0)
+        ok = view(m + kMapSg, w.ws_gate, Fs, d, 8) && view(m + kMapSu, w.ws_up, Fs, d, 8) &&
+             view(m + kMapSd, w.ws_down, d, Fs, 16);
+    }
     void* dl = nullptr;
-    if (dev_malloc(&dl, sizeof(StackLayerPtrs) * n_layers) != cudaSuccess) {
+    void* dm = nullptr;
+    if (ok && (dev_malloc(&dl, sizeof(StackLayerPtrs) * n_layers) != cudaSuccess ||
+               dev_malloc(&dm, sizeof(CUtensorMap) * maps.size()) != cudaSuccess)) {
       cudaGetLastError();
+      if (dl) cudaFree(dl);
       free_stack(s);
       return MOE_ERR_OOM;
     }
-    s->d_layers = static_cast<StackLayerPtrs*>(dl);
-    if (cudaMemcpyAsync(s->d_layers, hp.data(), sizeof(StackLayerPtrs) * n_layers, cudaMemcpyHostToDevice,
-                        stream) != cudaSuccess) {
-      cudaGetLastError();
-      free_stack(s);
-      return MOE_ERR_CUDA;
+    if (!ok) {
+      s->persistent = false;                 // the per-layer path serves every T
+    } else {
+      s->d_layers = static_cast<StackLayerPtrs*>(dl);
+      s->d_maps = static_cast<CUtensorMap*>(dm);
+      if (cudaMemcpy(s->d_layers, hp.data(), sizeof(StackLayerPtrs) * n_layers, cudaMemcpyHostToDevice) !=
+              cudaSuccess ||
+          cudaMemcpy(s->d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) !=
+              cudaSuccess) {
+        cudaGetLastError();
+        free_stack(s);
+        return MOE_ERR_CUDA;
+      }
     }
   }
   if (cudaMemsetAsync(s->err, 0, 256, stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) {
@@ -165,6 +195,7 @@ moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void*
     }
     StackArgs a;
     a.layers = h->d_layers;
+    a.maps = h->d_maps;
     a.L = h->L;
     a.x_in = static_cast<const __nv_bfloat16*>(x);
     a.y_out = static_cast<__nv_bfloat16*>(y);

@@ -24,10 +24,13 @@
 //      the warps in a fixed order (deterministic), adds the residual x and
 //      rounds the new residual stream to bf16.
 //
-// Inside a CTA one producer warp streams weights with 1-D bulk copies into a
+// Inside a CTA one producer thread streams weights with TMA tile loads into a
 // 16-stage shared-memory ring (two stages per consumer warp, each stage 16
-// rows x 256 values padded to 528 bytes per row so ldmatrix rows hit distinct
-// banks); eight consumer warps multiply on the tensor pipe (mma.sync
+// rows x 256 values = 8 KB in one or two loads of a 3-D box {64 values, rows,
+// 4 chunks of 64} with the 128-byte swizzle; the chunk dimension is outermost
+// in shared memory, so the swizzle's XOR follows the weight row and ldmatrix
+// rows hit distinct banks; many small 1-D bulk copies instead left the copy
+// engine, not HBM, as the limit); eight consumer warps multiply on the tensor pipe (mma.sync
 // m16n8k16, bf16 in, fp32 accumulate) with the activations (x or h, staged
 // once per phase in shared memory) as the 8-column B operand.  A gate/up row
 // group is 8 gate rows + 8 up rows of one expert, its K segments spread over
@@ -50,8 +53,7 @@ namespace {
 constexpr int kSdThreads = 32 * (1 + kSdConsumers);
 constexpr int kSdStages = 2 * kSdConsumers;         // two per consumer warp
 constexpr int kSdSeg = 256;                         // values per row segment
-constexpr int kSdRowPitch = kSdSeg * 2 + 16;        // 528 bytes
-constexpr int kSdStageBytes = 16 * kSdRowPitch;     // 8448 bytes
+constexpr int kSdStageBytes = 16 * kSdSeg * 2;      // 8192 bytes: 16 rows x 4 chunks x 128 bytes
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -109,7 +111,7 @@ __host__ __device__ inline SdLayout sd_layout(int d, int Fmax, int k) {
   L.red = o;    o += 2 * kSdConsumers * 32 * 4 * 4;   // double-buffered partial sums of a row group
   L.yw = o;     o += kSdConsumers * 16 * kSdMaxT * 4; // per-warp down-projection sums of a row block
   L.rt = o;     o += 4096;                            // routing tables (below)
-  L.total = o;
+  L.total = o + 1024;                                 // slack to align the base to 1024 bytes
   return L;
 }
 // Routing tables inside L.rt (ints / floats):
@@ -143,9 +145,18 @@ __device__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, vol
   bool bad = false;
   if (threadIdx.x == 32) {
     if (!*abort_flag) {
-      __threadfence();
-      atomicAdd(ctr, 1u);
-      if (!counter_wait(ctr, target, wc)) {
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+      // poll without sleeping (the barrier is on the critical path), bounded in time
+      bool ok = ld_acquire_gpu(ctr) >= target;
+      if (!ok) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t it = 1; !ok; ++it) {
+          ok = ld_acquire_gpu(ctr) >= target;
+          if (!ok && (it & 255u) == 0 && global_ns() - t0 > wc.limit_ns) break;
+        }
+      }
+      if (!ok) {
+        atomicOr(wc.err, kErrTimeout);
         *abort_flag = 1;
         bad = true;
       }
@@ -202,15 +213,27 @@ struct Producer {
     own.m[w]++;
     return __shfl_sync(kFull, s, 0);
   }
-  // 16 rows of 256 bf16 values: rows 0-7 from p0 + r * pitch, rows 8-15 from p1 + r * pitch.
-  __device__ bool issue16(int w, const __nv_bfloat16* p0, const __nv_bfloat16* p1, size_t pitch) {
-    const int s = next(w);
-    if (s < 0) return false;
-    if (c.lane == 0) mbar_arrive_expect_tx(&c.full[s], 16 * kSdSeg * 2);
-    __syncwarp();
-    if (c.lane < 16) {
-      const __nv_bfloat16* src = c.lane < 8 ? p0 + (size_t)c.lane * pitch : p1 + (size_t)(c.lane - 8) * pitch;
-      bulk_g2s_hint(c.smem + c.L.stages + s * kSdStageBytes + c.lane * kSdRowPitch, src, kSdSeg * 2, &c.full[s], pol);
+  // Gate/up stage: gate rows [row0, row0 + 8) and up rows [row0, row0 + 8),
+  // values [256 s, 256 s + 256): two 4 KB boxes.
+  __device__ bool issue_gu(int w, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int s) {
+    const int st = next(w);
+    if (st < 0) return false;
+    if (c.lane == 0) {
+      uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
+      mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
+      tma_load_3d_hint(dst, mg, 0, row0, 4 * s, &c.full[st], pol);
+      tma_load_3d_hint(dst + kSdStageBytes / 2, mu, 0, row0, 4 * s, &c.full[st], pol);
+    }
+    return true;
+  }
+  // Down stage: rows [row0, row0 + 16), values [256 s, 256 s + 256): one 8 KB box.
+  __device__ bool issue_dn(int w, const CUtensorMap* md, int row0, int s) {
+    const int st = next(w);
+    if (st < 0) return false;
+    if (c.lane == 0) {
+      uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
+      mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
+      tma_load_3d_hint(dst, md, 0, row0, 4 * s, &c.full[st], pol);
     }
     return true;
   }
@@ -221,13 +244,13 @@ struct Producer {
   }
 };
 
-// Gate/up row group g of an expert: gate rows 8g..8g+7 and up rows 8g..8g+7,
-// K segments spread over the consumers (segment s -> consumer s % 8).
-__device__ bool produce_gu(Producer& P, const __nv_bfloat16* wg, const __nv_bfloat16* wu, int g, int d) {
+// Gate/up row group g of an expert (first row row0 = e F + 8 g, or 8 g for
+// the shared expert): K segments spread over the consumers (segment s ->
+// consumer s % 8).
+__device__ bool produce_gu(Producer& P, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int d) {
   const int KC = d / kSdSeg;
   for (int s = 0; s < KC; ++s)
-    if (!P.issue16(s % kSdConsumers, wg + (size_t)g * 8 * d + s * kSdSeg, wu + (size_t)g * 8 * d + s * kSdSeg, d))
-      return false;
+    if (!P.issue_gu(s % kSdConsumers, mg, mu, row0, s)) return false;
   return true;
 }
 
@@ -237,9 +260,11 @@ __device__ void run_producer(SdCtx& c) {
   const int nsh = a.Fs / 8;
   bool ok = true;
   for (int l = 0; l < a.L && ok; ++l) {
-    const StackLayerPtrs& W = a.layers[l];
+    const CUtensorMap* M = a.maps + (size_t)l * kSdMaps;
+    if (c.lane == 0 && l + 1 < a.L)
+      for (int i = 0; i < kSdMaps; ++i) tma_prefetch_desc(M + kSdMaps + i);
     // phase A: the shared expert's row groups of this CTA
-    for (int g = c.b; g < nsh && ok; g += c.G) ok = produce_gu(P, W.sg, W.su, g, a.d);
+    for (int g = c.b; g < nsh && ok; g += c.G) ok = produce_gu(P, M + kMapSg, M + kMapSu, g * 8, a.d);
     if (!ok) break;
     // this CTA's routing for layer l
     int rdy = 1;
@@ -252,7 +277,7 @@ __device__ void run_producer(SdCtx& c) {
     const int lo = (int)(((long long)n * c.b) / c.G), hi = (int)(((long long)n * (c.b + 1)) / c.G);
     for (int u = lo; u < hi && ok; ++u) {
       const int e = c.rt.act_e[u / ngrp];
-      ok = produce_gu(P, W.wg + (size_t)e * a.F * a.d, W.wu + (size_t)e * a.F * a.d, u % ngrp, a.d);
+      ok = produce_gu(P, M + kMapWg, M + kMapWu, e * a.F + (u % ngrp) * 8, a.d);
     }
     // phase C: the down rows of this CTA's row blocks, unit j -> consumer j % 8
     const int has_sh = a.Fs > 0 ? 1 : 0;
@@ -260,11 +285,8 @@ __device__ void run_producer(SdCtx& c) {
       for (int j = 0; j < U + has_sh && ok; ++j) {
         const bool sh = has_sh && j == 0;
         const int Fe = sh ? a.Fs : a.F;
-        const __nv_bfloat16* wd = sh ? W.sd : W.wd + (size_t)c.rt.act_e[j - has_sh] * a.d * a.F;
-        for (int s = 0; s < Fe / kSdSeg && ok; ++s) {
-          const __nv_bfloat16* p = wd + (size_t)rb * 16 * Fe + s * kSdSeg;
-          ok = P.issue16(j % kSdConsumers, p, p + (size_t)8 * Fe, Fe);
-        }
+        const int row0 = sh ? rb * 16 : c.rt.act_e[j - has_sh] * a.d + rb * 16;
+        for (int s = 0; s < Fe / kSdSeg && ok; ++s) ok = P.issue_dn(j % kSdConsumers, M + (sh ? kMapSd : kMapWd), row0, s);
       }
     }
   }
@@ -297,16 +319,23 @@ struct Cons {
   int cur = 0;
 };
 
-// acc += stage (16 rows x 256 values) x B, B row n = brow(n) (k offset k0, 8 columns).
-__device__ __forceinline__ void mma_stage(uint32_t st, uint32_t bbase, uint32_t bpitch, const int (&bidx)[1],
+// acc += stage (16 rows x 256 values) x B, B row n = bidx (k offset k0, 8
+// columns).  The stage holds 4 chunks of 64 values; row r of chunk c is a
+// 128-byte line whose 16-byte pieces are XOR-swizzled by r & 7.  Gate/up
+// stages (gu) keep rows 0-7 (gate) and 8-15 (up) in two 4 KB boxes
+// [chunk][8 rows]; down stages are one 8 KB box [chunk][16 rows].
+__device__ __forceinline__ void mma_stage(uint32_t st, bool gu, uint32_t bbase, uint32_t bpitch, const int (&bidx)[1],
                                           int k0, int lane, float (&acc)[4]) {
-  const uint32_t lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
-  const uint32_t a0 = st + lrow * kSdRowPitch + lcol * 2;
+  const uint32_t lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lhi = lane >> 4;   // ldmatrix row, 8-value half
+  const uint32_t rr = gu ? (lrow & 7) : lrow;
+  const uint32_t rbase = st + (gu ? (lrow >> 3) * (kSdStageBytes / 2) : 0) + rr * 128;
+  const uint32_t cstride = gu ? 1024 : 2048, sw = lrow & 7;
   const uint32_t b0a = bbase + (uint32_t)bidx[0] * bpitch + (uint32_t)(k0 + (lane & 3) * 2) * 2;
 #pragma unroll 4
   for (int kk = 0; kk < kSdSeg / 16; ++kk) {
     uint32_t af[4];
-    ldsm_x4(a0 + kk * 32, af);
+    const uint32_t piece = ((((uint32_t)kk & 3) << 1) | lhi) ^ sw;
+    ldsm_x4(rbase + (kk >> 2) * cstride + (piece << 4), af);
     const uint32_t b0 = lds32(b0a + kk * 32), b1 = lds32(b0a + kk * 32 + 16);
     mma_bf16(acc, af, b0, b1);
   }
@@ -330,7 +359,7 @@ __device__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int cnt, int rg, Tok
   for (int s = w; s < KC; s += kSdConsumers) {
     const uint32_t st = C.wait();
     if (!st) break;
-    mma_stage(st, xs, c.L.x_pitch, bidx, s * kSdSeg, lane, acc);
+    mma_stage(st, true, xs, c.L.x_pitch, bidx, s * kSdSeg, lane, acc);
     C.release();
   }
   float* red = reinterpret_cast<float*>(c.smem + c.L.red) + (size_t)(rg & 1) * kSdConsumers * 128;
@@ -509,15 +538,16 @@ __device__ void run_consumers(SdCtx& c) {
         float acc[kSdMaxT];
 #pragma unroll
         for (int t = 0; t < kSdMaxT; ++t) acc[t] = 0.f;
-        for (int i0 = lane * 4; i0 < d; i0 += 32 * 4 * 4) {
-          float4 wv[4];
+        // 2048 values per pass: all 16 loads of a lane in flight at once
+        for (int i0 = lane * 4; i0 < d; i0 += 32 * 4 * 16) {
+          float4 wv[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 16; ++u) {
             const int i = i0 + u * 128;
             wv[u] = i < d ? __ldg(reinterpret_cast<const float4*>(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 16; ++u) {
             const int i = i0 + u * 128;
             if (i < d) {
 #pragma unroll
@@ -583,6 +613,18 @@ __device__ void run_consumers(SdCtx& c) {
         *reinterpret_cast<uint4*>(hs + r * c.L.h_pitch + q * 16) = v;
       }
     }
+    // CTAs that own no output rows pull the next layer's router rows into L2
+    // meanwhile, so its logits do not wait on HBM latency
+    if (c.b >= d / 16 && l + 1 < a.L && c.G > d / 16) {
+      const size_t bytes = (size_t)E * d * 4, nidle = (size_t)(c.G - d / 16);
+      const size_t per = ((bytes + nidle - 1) / nidle + 4095) & ~(size_t)4095;
+      const size_t lo = per * (size_t)(c.b - d / 16), hi = lo + per < bytes ? lo + per : bytes;
+      const char* base = reinterpret_cast<const char*>(a.layers[l + 1].wr);
+      for (size_t o = lo + (size_t)tid * 4096; o < hi; o += (size_t)NT * 4096) {
+        const uint32_t n = (uint32_t)(hi - o < 4096 ? hi - o : 4096);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n) : "memory");
+      }
+    }
     float* yw = reinterpret_cast<float*>(c.smem + c.L.yw);
     for (int rb = c.b; rb < d / 16; rb += c.G) {
       for (int i = tid; i < kSdConsumers * 16 * kSdMaxT; i += NT) yw[i] = 0.f;
@@ -600,7 +642,7 @@ __device__ void run_consumers(SdCtx& c) {
         for (int s = 0; s < Fe / kSdSeg; ++s) {
           const uint32_t st = C.wait();
           if (!st) { ok = false; break; }
-          mma_stage(st, smem_u32(c.smem + c.L.xs), c.L.h_pitch, bidx, s * kSdSeg, lane, acc);
+          mma_stage(st, false, smem_u32(c.smem + c.L.xs), c.L.h_pitch, bidx, s * kSdSeg, lane, acc);
           C.release();
         }
         if (!ok) break;                        // abort: fall through to the barrier below
@@ -634,7 +676,8 @@ __device__ void run_consumers(SdCtx& c) {
 }
 
 __global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(StackArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];
+  extern __shared__ __align__(128) uint8_t dsm_raw[];
+  uint8_t* dsm = dsm_raw + ((1024 - (smem_u32(dsm_raw) & 1023)) & 1023);   // the swizzle wants 1024-byte stages
   SdCtx c;
   c.a = a;
   const int Fmax = a.F > a.Fs ? a.F : a.Fs;

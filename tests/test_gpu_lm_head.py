@@ -87,5 +87,5 @@ def test_small_head_and_argument_checks():
     head.close()
     assert B.moe_head_create(500, 64, 8, codes.data_ptr(), scales.data_ptr(), ts.data_ptr())[0] == \
         B.MOE_ERR_UNSUPPORTED
-    assert B.moe_head_create(512, 60, 8, codes.data_ptr(), scales.data_ptr(), ts.data_ptr())[0] == \
+    assert B.moe_head_create(512, 48, 8, codes.data_ptr(), scales.data_ptr(), ts.data_ptr())[0] == \
         B.MOE_ERR_UNSUPPORTED
