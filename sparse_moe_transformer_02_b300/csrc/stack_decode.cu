@@ -140,7 +140,7 @@ __device__ __forceinline__ Rt rt_of(uint8_t* base) {
 
 // Grid barrier: every consumer thread of every CTA calls it; one thread per
 // CTA arrives on the counter (release) and waits for the target (acquire).
-__device__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, volatile int* abort_flag) {
+__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, volatile int* abort_flag) {
   named_sync(1, 32 * kSdConsumers);
   bool bad = false;
   if (threadIdx.x == 32) {
@@ -166,17 +166,15 @@ __device__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, vol
 }
 
 // The producer's view of the ring: consumer c owns stages 2c, 2c + 1 and
-// takes them alternately; its m-th stage has phase parity (m >> 1) & 1.
-struct SdOwner {
-  int m[kSdConsumers];
-  uint32_t last_par[kSdStages];
-  uint32_t used;
-};
+// takes them alternately; its m-th stage has phase parity (m >> 1) & 1.  The
+// counters live in shared memory (a local array indexed by consumer would sit
+// in local memory, which this kernel's shared-memory footprint leaves
+// uncached in L1).
 
 // One CTA's walk over the stack: the producer (prod = true) issues every
 // stage, the consumers process them, both in the same order.
 struct SdCtx {
-  StackArgs a;
+  const StackArgs& a;               // the kernel's __grid_constant__ parameter (no copy)
   SdLayout L;
   uint8_t* smem;
   uint64_t* full;
@@ -186,91 +184,79 @@ struct SdCtx {
   Rt rt;
   WaitCtl wc;
   int G, b, warp, lane;
+  int* prod_m;                      // producer: stages taken per consumer [kSdConsumers]
+  uint32_t* prod_par;               // producer: phase parity last used per stage [kSdStages]
 };
 
 // ---------------------------------------------------------------- producer
+// One thread issues every stage of the CTA.
 struct Producer {
   SdCtx& c;
-  SdOwner own;
   uint64_t pol;
-  __device__ explicit Producer(SdCtx& ctx) : c(ctx) {
-    for (int i = 0; i < kSdConsumers; ++i) own.m[i] = 0;
-    own.used = 0;
+  uint32_t used = 0;
+  __device__ __forceinline__ explicit Producer(SdCtx& ctx) : c(ctx) {
+    for (int i = 0; i < kSdConsumers; ++i) c.prod_m[i] = 0;
     pol = policy_evict_first();
   }
   // Next stage of consumer w (bounded wait for it to be free); -1 on abort.
-  __device__ int next(int w) {
-    int s = -1;
-    if (c.lane == 0) {
-      const int m = own.m[w];
-      s = w * 2 + (m & 1);
-      if (!mbar_wait(&c.empty[s], ((m >> 1) & 1) ^ 1, c.wc)) s = -1;
-      else {
-        own.last_par[s] = (m >> 1) & 1;
-        own.used |= 1u << s;
-      }
-    }
-    own.m[w]++;
-    return __shfl_sync(kFull, s, 0);
+  __device__ __forceinline__ int next(int w) {
+    const int m = c.prod_m[w]++;
+    const int s = w * 2 + (m & 1);
+    if (!mbar_wait(&c.empty[s], ((m >> 1) & 1) ^ 1, c.wc)) return -1;
+    c.prod_par[s] = (m >> 1) & 1;
+    used |= 1u << s;
+    return s;
   }
   // Gate/up stage: gate rows [row0, row0 + 8) and up rows [row0, row0 + 8),
   // values [256 s, 256 s + 256): two 4 KB boxes.
-  __device__ bool issue_gu(int w, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int s) {
+  __device__ __forceinline__ bool issue_gu(int w, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int s) {
     const int st = next(w);
     if (st < 0) return false;
-    if (c.lane == 0) {
-      uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
-      mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
-      tma_load_3d_hint(dst, mg, 0, row0, 4 * s, &c.full[st], pol);
-      tma_load_3d_hint(dst + kSdStageBytes / 2, mu, 0, row0, 4 * s, &c.full[st], pol);
-    }
+    uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
+    mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
+    tma_load_3d_hint(dst, mg, 0, row0, 4 * s, &c.full[st], pol);
+    tma_load_3d_hint(dst + kSdStageBytes / 2, mu, 0, row0, 4 * s, &c.full[st], pol);
     return true;
   }
   // Down stage: rows [row0, row0 + 16), values [256 s, 256 s + 256): one 8 KB box.
-  __device__ bool issue_dn(int w, const CUtensorMap* md, int row0, int s) {
+  __device__ __forceinline__ bool issue_dn(int w, const CUtensorMap* md, int row0, int s) {
     const int st = next(w);
     if (st < 0) return false;
-    if (c.lane == 0) {
-      uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
-      mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
-      tma_load_3d_hint(dst, md, 0, row0, 4 * s, &c.full[st], pol);
-    }
+    uint8_t* dst = c.smem + c.L.stages + st * kSdStageBytes;
+    mbar_arrive_expect_tx(&c.full[st], kSdStageBytes);
+    tma_load_3d_hint(dst, md, 0, row0, 4 * s, &c.full[st], pol);
     return true;
   }
-  __device__ void drain() {
-    if (c.lane != 0) return;
+  __device__ __forceinline__ void drain() {
     for (int s = 0; s < kSdStages; ++s)
-      if (own.used & (1u << s)) drain_wait(&c.full[s], own.last_par[s], c.wc.limit_ns);
+      if (used & (1u << s)) drain_wait(&c.full[s], c.prod_par[s], c.wc.limit_ns);
   }
 };
 
 // Gate/up row group g of an expert (first row row0 = e F + 8 g, or 8 g for
 // the shared expert): K segments spread over the consumers (segment s ->
 // consumer s % 8).
-__device__ bool produce_gu(Producer& P, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int d) {
+__device__ __forceinline__ bool produce_gu(Producer& P, const CUtensorMap* mg, const CUtensorMap* mu, int row0, int d) {
   const int KC = d / kSdSeg;
   for (int s = 0; s < KC; ++s)
     if (!P.issue_gu(s % kSdConsumers, mg, mu, row0, s)) return false;
   return true;
 }
 
-__device__ void run_producer(SdCtx& c) {
+__device__ __forceinline__ void run_producer(SdCtx& c) {
   const StackArgs& a = c.a;
   Producer P(c);
   const int nsh = a.Fs / 8;
   bool ok = true;
   for (int l = 0; l < a.L && ok; ++l) {
     const CUtensorMap* M = a.maps + (size_t)l * kSdMaps;
-    if (c.lane == 0 && l + 1 < a.L)
+    if (l + 1 < a.L)
       for (int i = 0; i < kSdMaps; ++i) tma_prefetch_desc(M + kSdMaps + i);
     // phase A: the shared expert's row groups of this CTA
     for (int g = c.b; g < nsh && ok; g += c.G) ok = produce_gu(P, M + kMapSg, M + kMapSu, g * 8, a.d);
     if (!ok) break;
     // this CTA's routing for layer l
-    int rdy = 1;
-    if (c.lane == 0) rdy = mbar_wait(c.route_bar, l & 1, c.wc) ? 1 : 0;
-    rdy = __shfl_sync(kFull, rdy, 0);
-    if (!rdy) { ok = false; break; }
+    if (!mbar_wait(c.route_bar, l & 1, c.wc)) { ok = false; break; }
     const int U = *c.rt.n_act;
     // phase B: routed row groups, an even share per CTA
     const int ngrp = a.F / 8, n = U * ngrp;
@@ -298,8 +284,8 @@ __device__ void run_producer(SdCtx& c) {
 struct Cons {
   SdCtx& c;
   int m = 0;
-  __device__ explicit Cons(SdCtx& ctx) : c(ctx) {}
-  __device__ uint32_t wait() {
+  __device__ __forceinline__ explicit Cons(SdCtx& ctx) : c(ctx) {}
+  __device__ __forceinline__ uint32_t wait() {
     const int s = c.warp - 1;
     const int st = s * 2 + (m & 1);
     int ok = 1;
@@ -311,7 +297,7 @@ struct Cons {
     cur = st;
     return smem_u32(c.smem + c.L.stages + st * kSdStageBytes);
   }
-  __device__ void release() {
+  __device__ __forceinline__ void release() {
     __syncwarp();
     if (c.lane == 0) mbar_arrive(&c.empty[cur]);
     ++m;
@@ -346,7 +332,7 @@ __device__ __forceinline__ void mma_stage(uint32_t st, bool gu, uint32_t bbase, 
 // column n (n < cnt), hslot(n) = h row to write.  rg counts row groups (for
 // the double-buffered partials and the finalising warp).
 template <typename Tok, typename Slot>
-__device__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int cnt, int rg, Tok&& rows_tok, Slot&& hslot,
+__device__ __forceinline__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int cnt, int rg, Tok&& rows_tok, Slot&& hslot,
                            __nv_bfloat16* h, int Fmax) {
   const int w = c.warp - 1, lane = c.lane, KC = d / kSdSeg;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -388,7 +374,7 @@ __device__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int cnt, int rg, Tok
 
 // Top-k of token t (one warp): larger logit first, lower expert index first on
 // equal logits; gates = softmax of the selected logits.
-__device__ void topk_token(const float* logits, int E, int k, int t, Rt& rt, int lane) {
+__device__ __forceinline__ void topk_token(const float* logits, int E, int k, int t, Rt& rt, int lane) {
   uint64_t key[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -400,45 +386,43 @@ __device__ void topk_token(const float* logits, int E, int k, int t, Rt& rt, int
       key[i] = ((uint64_t)o << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
     }
   }
-  float l0 = 0.f, sum = 0.f;
-  float lsel[kMaxTopK];
-  int esel[kMaxTopK];
+  // k rounds of a warp-wide maximum; round j's winner (expert, logit) goes
+  // straight to shared memory (the logit parked in sel_g until the gates)
   for (int j = 0; j < k; ++j) {
     uint64_t best = 0;
-    int bi = -1;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (key[i] > best) { best = key[i]; bi = i; }
+    for (int i = 0; i < 8; ++i) best = key[i] > best ? key[i] : best;
     uint64_t wbest = best;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       const uint64_t other = __shfl_xor_sync(kFull, wbest, o);
       wbest = other > wbest ? other : wbest;
     }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(wbest & 0xFFFFFFFFu));
-    if (bi >= 0 && best == wbest) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i == bi) key[i] = 0;
+    for (int i = 0; i < 8; ++i)
+      if (key[i] == wbest) key[i] = 0;            // keys are unique (the index is part of them)
+    if (lane == 0) {
+      const uint32_t o = (uint32_t)(wbest >> 32);
+      const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+      rt.sel_e[t * k + j] = (int)(0xFFFFFFFFu - (uint32_t)(wbest & 0xFFFFFFFFu));
+      rt.sel_g[t * k + j] = __uint_as_float(u);
     }
-    const uint32_t o = (uint32_t)(wbest >> 32);
-    const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
-    const float lv = __uint_as_float(u);
-    if (j == 0) l0 = lv;
-    lsel[j] = lv;
-    esel[j] = e;
-    sum += expf(lv - l0);
   }
-  if (lane == 0)
-    for (int j = 0; j < k; ++j) {
-      rt.sel_e[t * k + j] = esel[j];
-      rt.sel_g[t * k + j] = expf(lsel[j] - l0) / sum;
-    }
+  __syncwarp();
+  // gates: softmax of the k selected logits (lane j holds selection j)
+  const float l0 = rt.sel_g[t * k];
+  const float lj = lane < k ? rt.sel_g[t * k + lane] : l0;
+  const float ej = lane < k ? expf(lj - l0) : 0.f;
+  float sum = ej;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  __syncwarp();
+  if (lane < k) rt.sel_g[t * k + lane] = ej / sum;
 }
 
 // Grouping of the T k slots by expert (one warp): active experts ascending,
 // slots of one expert in (token, j) order.
-__device__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane) {
+__device__ __forceinline__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane) {
   const int ns = T * k;
   for (int e = lane; e < 256; e += 32) rt.cnt[e] = 0;
   __syncwarp();
@@ -502,7 +486,7 @@ __device__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane) {
   __syncwarp();
 }
 
-__device__ void run_consumers(SdCtx& c) {
+__device__ __forceinline__ void run_consumers(SdCtx& c) {
   const StackArgs& a = c.a;
   Cons C(c);
   const int w = c.warp - 1, lane = c.lane, tid = threadIdx.x - 32, NT = 32 * kSdConsumers;
@@ -675,12 +659,11 @@ __device__ void run_consumers(SdCtx& c) {
   }
 }
 
-__global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(StackArgs a) {
+__global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(const __grid_constant__ StackArgs a) {
   extern __shared__ __align__(128) uint8_t dsm_raw[];
   uint8_t* dsm = dsm_raw + ((1024 - (smem_u32(dsm_raw) & 1023)) & 1023);   // the swizzle wants 1024-byte stages
-  SdCtx c;
-  c.a = a;
   const int Fmax = a.F > a.Fs ? a.F : a.Fs;
+  SdCtx c{a};
   c.L = sd_layout(a.d, Fmax, a.k);
   c.smem = dsm;
   c.full = reinterpret_cast<uint64_t*>(dsm + c.L.bars);
@@ -688,6 +671,8 @@ __global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(StackArgs a
   c.route_bar = reinterpret_cast<uint64_t*>(dsm + c.L.route_bar);
   c.abort_flag = reinterpret_cast<volatile int*>(dsm + c.L.abort);
   c.rt = rt_of(dsm + c.L.rt);
+  c.prod_m = reinterpret_cast<int*>(dsm + c.L.rt + 3840);
+  c.prod_par = reinterpret_cast<uint32_t*>(dsm + c.L.rt + 3840 + 4 * kSdConsumers);
   c.G = gridDim.x;
   c.b = blockIdx.x;
   c.warp = threadIdx.x >> 5;
@@ -702,9 +687,12 @@ __global__ void __launch_bounds__(kSdThreads, 1) stack_decode_kernel(StackArgs a
     fence_mbar_init();
   }
   __syncthreads();
-  c.wc = WaitCtl{a.wait_ns, a.err, const_cast<int*>(reinterpret_cast<volatile int*>(c.abort_flag))};
-  if (c.warp == 0) run_producer(c);
-  else run_consumers(c);
+  c.wc = WaitCtl{a.wait_ns, a.err, c.abort_flag};
+  if (c.warp == 0) {
+    if (c.lane == 0) run_producer(c);      // one thread issues every copy
+  } else {
+    run_consumers(c);
+  }
 }
 
 }  // namespace
