@@ -270,7 +270,7 @@ struct StackArgs {
   const __nv_bfloat16* x_in;        // [T][d]
   __nv_bfloat16* y_out;             // [T][d]
   __nv_bfloat16* xbuf;              // [2][kSdMaxT][d] residual stream between layers
-  float* logits;                    // [kSdMaxT][E]
+  float* logits;                    // [4][kSdMaxT][E] partial router logits (quarter rows)
   __nv_bfloat16* h;                 // [kSdMaxT * (k + 1)][Fmax]
   __nv_bfloat16* x_trace;           // [L + 1][T][d] or nullptr
   int32_t* idx_trace;               // [L][T][k] or nullptr

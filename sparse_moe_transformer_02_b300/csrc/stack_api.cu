@@ -83,7 +83,7 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
                   c.d % 256 == 0 && c.ffn % 256 == 0 && c.shared_ffn % 256 == 0 && cc_major == 10 && coop &&
                   stack_decode_smem_bytes(c.d, c.ffn, c.shared_ffn, c.top_k) <= (size_t)smem_optin;
   const size_t es = c.act_dtype == MOE_F32 ? 4 : 2;
-  const size_t nx = (size_t)kSdMaxT * c.d * 2, nlog = (size_t)kSdMaxT * c.num_experts * 4;
+  const size_t nx = (size_t)kSdMaxT * c.d * 2, nlog = (size_t)4 * kSdMaxT * c.num_experts * 4;
   const size_t nh = (size_t)kSdMaxT * (c.top_k + 1) * Fmax * 2, nchain = (size_t)c.max_tokens * c.d * es;
   const size_t total = up256(2 * nx) + up256(nlog) + up256(nh) + 256 + 256 + 2 * up256(nchain);
   if (dev_malloc(&s->block, total) != cudaSuccess) {

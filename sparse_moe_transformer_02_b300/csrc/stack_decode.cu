@@ -12,8 +12,9 @@
 // separated by grid-wide barriers.
 //
 // Per layer three phases, each ending in a grid barrier:
-//   A  router logits (fp32, one warp per expert row, plain loads) and the
-//      shared expert's gate/up row groups (need no routing);
+//   A  router logits (fp32; each expert row split over 4 warps across the
+//      grid, plain loads, partial sums added in a fixed order by the top-k)
+//      and the shared expert's gate/up row groups (need no routing);
 //   B  top-k, gates and grouping, computed by every CTA for itself from the
 //      logits (identical inputs and instructions, so every CTA holds the same
 //      routing), then the routed experts' gate/up row groups, split evenly
@@ -53,6 +54,7 @@ namespace {
 constexpr int kSdThreads = 32 * (1 + kSdConsumers);
 constexpr int kSdStages = 2 * kSdConsumers;         // two per consumer warp
 constexpr int kSdSeg = 256;                         // values per row segment
+constexpr int kSdRq = 4;                            // warps per router row
 constexpr int kSdStageBytes = 16 * kSdSeg * 2;      // 8192 bytes: 16 rows x 4 chunks x 128 bytes
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -374,37 +376,43 @@ __device__ __forceinline__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int 
 
 // Top-k of token t (one warp): larger logit first, lower expert index first on
 // equal logits; gates = softmax of the selected logits.
-__device__ __forceinline__ void topk_token(const float* logits, int E, int k, int t, Rt& rt, int lane) {
-  uint64_t key[8];
+__device__ __forceinline__ void topk_token(const float* part, int E, int k, int t, Rt& rt, int lane) {
+  float lg[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    key[i] = 0;
+    lg[i] = 0.f;
     if (e < E) {
-      const uint32_t u = __float_as_uint(__ldcg(logits + (size_t)t * E + e));
-      const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-      key[i] = ((uint64_t)o << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+#pragma unroll
+      for (int q = 0; q < kSdRq; ++q) lg[i] += __ldcg(part + ((size_t)q * kSdMaxT + t) * E + e);
     }
   }
-  // k rounds of a warp-wide maximum; round j's winner (expert, logit) goes
-  // straight to shared memory (the logit parked in sel_g until the gates)
+  // order-preserving 32-bit keys of the logits (0 = taken or absent)
+  uint32_t key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = __float_as_uint(lg[i]);
+    key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+  }
+  // k rounds: the warp's largest key (redux max), then the lowest expert
+  // index holding it (redux min); the winner goes straight to shared memory
+  // (its logit parked in sel_g until the gates)
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
+    uint32_t lm = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) best = key[i] > best ? key[i] : best;
-    uint64_t wbest = best;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(kFull, wbest, o);
-      wbest = other > wbest ? other : wbest;
-    }
+    for (int i = 0; i < 8; ++i) lm = key[i] > lm ? key[i] : lm;
+    const uint32_t wm = __reduce_max_sync(kFull, lm);
+    uint32_t cand = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (key[i] == wbest) key[i] = 0;            // keys are unique (the index is part of them)
+      if (key[i] == wm) cand = min(cand, (uint32_t)(lane + 32 * i));
+    const uint32_t win = __reduce_min_sync(kFull, cand);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((uint32_t)(lane + 32 * i) == win) key[i] = 0;
     if (lane == 0) {
-      const uint32_t o = (uint32_t)(wbest >> 32);
-      const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
-      rt.sel_e[t * k + j] = (int)(0xFFFFFFFFu - (uint32_t)(wbest & 0xFFFFFFFFu));
+      const uint32_t u = (wm & 0x80000000u) ? (wm & 0x7FFFFFFFu) : ~wm;
+      rt.sel_e[t * k + j] = (int)win;
       rt.sel_g[t * k + j] = __uint_as_float(u);
     }
   }
@@ -514,30 +522,34 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
           __stcg(reinterpret_cast<uint4*>(a.x_trace) + i, __ldcg(reinterpret_cast<const uint4*>(a.x_in) + i));
     }
     named_sync(1, NT);
-    // router rows: expert e on global warp G * 8 - 1 - e (the last CTAs)
+    // router: row e split into kSdRq quarter rows, task e * kSdRq + q on global
+    // warp G * 8 - 1 - task (the last CTAs first); partial logits
+    // part[q][t][e] are summed in q order by the top-k
     {
-      const int gw = c.b * kSdConsumers + w, nw = c.G * kSdConsumers;
-      for (int e = nw - 1 - gw; e >= 0 && e < E; e += nw) {
-        const float* wr = W.wr + (size_t)e * d;
+      const int gw = c.b * kSdConsumers + w, nw = c.G * kSdConsumers, dq = d / kSdRq;
+      for (int task = nw - 1 - gw; task >= 0 && task < E * kSdRq; task += nw) {
+        const int e = task / kSdRq, q = task % kSdRq;
+        const float* wr = W.wr + (size_t)e * d + (size_t)q * dq;
+        const float bias = (q == 0 && W.br) ? __ldg(W.br + e) : 0.f;   // quarter 0 carries the bias
         float acc[kSdMaxT];
 #pragma unroll
         for (int t = 0; t < kSdMaxT; ++t) acc[t] = 0.f;
-        // 2048 values per pass: all 16 loads of a lane in flight at once
-        for (int i0 = lane * 4; i0 < d; i0 += 32 * 4 * 16) {
-          float4 wv[16];
+        for (int i0 = lane * 4; i0 < dq; i0 += 32 * 4 * 4) {
+          float4 wv[4];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * 128;
-            wv[u] = i < d ? __ldg(reinterpret_cast<const float4*>(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            wv[u] = i < dq ? __ldg(reinterpret_cast<const float4*>(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * 128;
-            if (i < d) {
+            if (i < dq) {
 #pragma unroll
               for (int t = 0; t < kSdMaxT; ++t)
                 if (t < T) {
-                  const uint2 xv = *reinterpret_cast<const uint2*>(c.smem + c.L.xs + t * c.L.x_pitch + i * 2);
+                  const uint2 xv =
+                      *reinterpret_cast<const uint2*>(c.smem + c.L.xs + t * c.L.x_pitch + (q * dq + i) * 2);
                   const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xFFFF0000u);
                   const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xFFFF0000u);
                   acc[t] = fmaf(wv[u].x, x0, fmaf(wv[u].y, x1, fmaf(wv[u].z, x2, fmaf(wv[u].w, x3, acc[t]))));
@@ -550,7 +562,7 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
           float v = acc[t];
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-          if (t < T && lane == 0) __stcg(a.logits + (size_t)t * E + e, v + (W.br ? __ldg(W.br + e) : 0.f));
+          if (t < T && lane == 0) __stcg(a.logits + ((size_t)q * kSdMaxT + t) * E + e, v + bias);
         }
       }
     }
