@@ -52,8 +52,9 @@ typedef enum {
   MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch error, no device, ...) */
   MOE_ERR_OOM = 4,           /* workspace allocation failed in moe_create */
   MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out (reported by moe_check) */
-  MOE_ERR_RANGE = 6          /* NVFP4 weights on the tensor-core path: an intermediate h / xs^2 exceeded
-                                the f16 range and was saturated (reported by moe_check) */
+  MOE_ERR_RANGE = 6          /* a value out of its range, reported by the check calls: NVFP4 weights on the
+                                tensor-core path, an intermediate h / xs^2 saturated f16 (moe_check); a
+                                negative decode position (moe_attn_check) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
@@ -304,6 +305,77 @@ moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void*
  * persistent kernel and of every layer handle (as moe_check).
  */
 moe_status moe_stack_check(moe_stack_handle h, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ sliding-window attention */
+
+typedef struct moe_attn* moe_attn_handle;      /* opaque, owned by the library */
+
+typedef struct {
+  int32_t d;              /* hidden width, a multiple of 256 */
+  int32_t n_q;            /* query heads */
+  int32_t n_kv;           /* key/value heads; n_q / n_kv <= 8 query heads share one */
+  int32_t head_dim;       /* 128 */
+  int32_t window;         /* positions attended: the current one and window - 1 before it */
+  int32_t max_batch;      /* largest B (sequences per call), 1..8 */
+  int32_t use_rope;       /* nonzero: rotate queries and keys (the sliding-window layers) */
+  int32_t add_residual;   /* nonzero: y = x + attn(x) */
+  int32_t wait_timeout_ms;/* limit of every device-side wait; 0 = 2000 ms */
+  float rope_base;        /* RoPE base (10,000 in this library's reading) */
+  float eps;              /* RMSNorm epsilon */
+} moe_attn_config;
+
+/* Borrowed device pointers: wq [n_q 128][d], wk and wv [n_kv 128][d], wo
+   [d][n_q 128] bf16 (16-byte aligned); q_norm and k_norm [128] fp32 (the
+   per-head RMSNorm scales); sinks [n_q] fp32 (one learned logit per head). */
+typedef struct {
+  const void* wq;
+  const void* wk;
+  const void* wv;
+  const void* wo;
+  const float* q_norm;
+  const float* k_norm;
+  const float* sinks;
+} moe_attn_weights;
+
+/*
+ * Sliding-window grouped-query attention for decode: 35 of Flint's 49 layers
+ * attend over the current token and the 512 before it, with 32 query heads
+ * over 4 key/value heads of dimension 128, a per-head QK RMSNorm, learned
+ * per-head sinks and RoPE (swarmz.net, section "The architecture, in plain
+ * terms"; futurpulse.com, section "How does Flint use 39.8B parameters
+ * efficiently?").  Per sequence b at position p: q = Wq x, k = Wk x, v = Wv
+ * x; q and k RMS-normalised per head (times q_norm / k_norm) and rotated by
+ * RoPE (pairs i, i + 64, angle p base^(-i / 64)); the new k, v written to the
+ * cache slot p % window as bf16; o_h = softmax over the window's keys of
+ * q_h . k / sqrt(128), with sink_h as one more logit in the denominator, times
+ * the values; y = Wo o (+ x).  The readings the pages leave open are listed
+ * at the top of this library's design notes.
+ *
+ * Errors: MOE_ERR_INVALID_ARG (NULL, non-positive sizes, misalignment),
+ * MOE_ERR_UNSUPPORTED (head_dim != 128, n_q / n_kv > 8, d not a multiple of
+ * 256, max_batch > 8, no cooperative launch), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* w, moe_attn_handle* out);
+
+/*
+ * One decode step of B sequences (B <= max_batch), one cooperative launch:
+ * x [B][d] bf16, pos [B] int32 (device memory, so a captured graph can be
+ * replayed at new positions), k_cache and v_cache [B][window][n_kv][128] bf16
+ * (caller-owned ring buffers; slot p % window holds position p; this call
+ * writes slot pos[b] % window), y [B][d] bf16.  All device pointers, 16-byte
+ * aligned (pos 4-byte), x and y not overlapping.  Enqueued on `stream`.
+ * Errors: MOE_ERR_INVALID_ARG (checked before any launch), MOE_ERR_CUDA;
+ * timeouts show up in moe_attn_check, and so does a negative position
+ * (MOE_ERR_RANGE; that sequence is computed as if at position 0).
+ */
+moe_status moe_attn_decode(moe_attn_handle h, const void* x, int32_t B, const int32_t* pos, void* k_cache,
+                           void* v_cache, void* y, cudaStream_t stream);
+
+/* Synchronise `stream`, then report and clear the error word (MOE_ERR_TIMEOUT, MOE_ERR_RANGE or MOE_OK). */
+moe_status moe_attn_check(moe_attn_handle h, cudaStream_t stream);
+
+/* Free the handle (synchronises the device). NULL is a no-op. */
+moe_status moe_attn_destroy(moe_attn_handle h);
 
 /* ------------------------------------------------------------------ 4-bit output layer */
 

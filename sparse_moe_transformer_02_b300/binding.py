@@ -22,7 +22,8 @@ EXPORTED = ["moe_status_string", "moe_create", "moe_destroy", "moe_route", "moe_
             "moe_forward_host", "moe_get_grouping", "moe_check", "moe_debug_expire_wait",
             "moe_profile_enable", "moe_profile_read", "moe_route_noalloc", "moe_debug_fail_alloc",
             "moe_stack_create", "moe_stack_destroy", "moe_stack_uses_persistent", "moe_stack_forward",
-            "moe_stack_check", "moe_head_create", "moe_head_forward", "moe_head_check", "moe_head_destroy"]
+            "moe_stack_check", "moe_head_create", "moe_head_forward", "moe_head_check", "moe_head_destroy",
+            "moe_attn_create", "moe_attn_decode", "moe_attn_check", "moe_attn_destroy"]
 KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize"]
 
 
@@ -30,6 +31,16 @@ class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d", "ffn", "shared_ffn", "num_experts", "top_k", "max_tokens", "act_dtype", "weight_dtype",
         "add_residual", "path", "gemv_max_tokens", "wait_timeout_ms")]
+
+
+class moe_attn_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("d", "n_q", "n_kv", "head_dim", "window", "max_batch", "use_rope",
+                                              "add_residual", "wait_timeout_ms")] + \
+               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+class moe_attn_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("wq", "wk", "wv", "wo", "q_norm", "k_norm", "sinks")]
 
 
 class moe_weights(ctypes.Structure):
@@ -93,6 +104,15 @@ def lib() -> ctypes.CDLL:
         L.moe_stack_check.argtypes = [vp, vp]
         L.moe_debug_fail_alloc.restype = ctypes.c_int
         L.moe_debug_fail_alloc.argtypes = [i32]
+        L.moe_attn_create.restype = ctypes.c_int
+        L.moe_attn_create.argtypes = [ctypes.POINTER(moe_attn_config), ctypes.POINTER(moe_attn_weights),
+                                      ctypes.POINTER(vp)]
+        L.moe_attn_decode.restype = ctypes.c_int
+        L.moe_attn_decode.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp]
+        L.moe_attn_check.restype = ctypes.c_int
+        L.moe_attn_check.argtypes = [vp, vp]
+        L.moe_attn_destroy.restype = ctypes.c_int
+        L.moe_attn_destroy.argtypes = [vp]
         L.moe_head_create.restype = ctypes.c_int
         L.moe_head_create.argtypes = [i32, i32, i32, vp, vp, vp, i32, ctypes.POINTER(vp)]
         L.moe_head_forward.restype = ctypes.c_int
@@ -198,6 +218,25 @@ def moe_stack_forward(h, x: int, T: int, y: int, x_trace: int = 0, idx_trace: in
 
 def moe_stack_check(h, stream: int = 0) -> int:
     return lib().moe_stack_check(h, stream)
+
+
+def moe_attn_create(cfg: moe_attn_config, w: moe_attn_weights):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    st = lib().moe_attn_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h))
+    return st, h.value
+
+
+def moe_attn_decode(h, x: int, B: int, pos: int, k_cache: int, v_cache: int, y: int, stream: int = 0) -> int:
+    return lib().moe_attn_decode(h, x, B, pos, k_cache, v_cache, y, stream)
+
+
+def moe_attn_check(h, stream: int = 0) -> int:
+    return lib().moe_attn_check(h, stream)
+
+
+def moe_attn_destroy(h) -> int:
+    return lib().moe_attn_destroy(h)
 
 
 def moe_head_create(d: int, vocab: int, max_tokens: int, codes: int, scales: int, tscale: int,
@@ -362,6 +401,50 @@ class MoeStack:
     def close(self):
         if getattr(self, "h", None):
             moe_stack_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoeAttn:
+    """A sliding-window attention handle plus the device tensors it borrows
+    (keys as in inputs.make_attention, as device tensors)."""
+
+    def __init__(self, weights: dict, d: int, n_q: int, n_kv: int, window: int, max_batch: int = 8,
+                 use_rope: bool = True, add_residual: bool = False, rope_base: float = 10000.0, eps: float = 1e-6,
+                 wait_timeout_ms: int = 0):
+        import torch
+        self.torch = torch
+        self.tensors = dict(weights)
+        self.cfg = moe_attn_config(d=d, n_q=n_q, n_kv=n_kv, head_dim=128, window=window, max_batch=max_batch,
+                                   use_rope=int(bool(use_rope)), add_residual=int(bool(add_residual)),
+                                   wait_timeout_ms=wait_timeout_ms, rope_base=rope_base, eps=eps)
+        w = moe_attn_weights()
+        for name, _ in moe_attn_weights._fields_:
+            setattr(w, name, self.tensors[name].data_ptr())
+        st, self.h = moe_attn_create(self.cfg, w)
+        _ok(st, "moe_attn_create")
+
+    def decode(self, x, pos, k_cache, v_cache, y=None, stream=None):
+        torch = self.torch
+        if y is None:
+            y = torch.empty_like(x)
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        _ok(moe_attn_decode(self.h, x.data_ptr(), x.shape[0], pos.data_ptr(), k_cache.data_ptr(),
+                            v_cache.data_ptr(), y.data_ptr(), s), "moe_attn_decode")
+        return y
+
+    def check(self, stream=None) -> int:
+        s = (stream if stream is not None else self.torch.cuda.current_stream()).cuda_stream
+        return moe_attn_check(self.h, s)
+
+    def close(self):
+        if getattr(self, "h", None):
+            moe_attn_destroy(self.h)
             self.h = None
 
     def __del__(self):

@@ -282,6 +282,32 @@ struct StackArgs {
 };
 size_t stack_decode_smem_bytes(int d, int F, int Fs, int k);
 
+// ---------------------------------------------------------------- sliding-window attention (decode)
+constexpr int kAtMaxT = 8;          // sequences per attention launch
+
+struct AttnArgs {
+  CUtensorMap tm[4];                // Wq, Wk, Wv, Wo as 3-D views {64, rows, K / 64}, box {64, 16, 4}
+  const __nv_bfloat16* x;           // [B][d]
+  __nv_bfloat16* y;                 // [B][d]
+  const int32_t* pos;               // [B] position of each sequence's new token
+  __nv_bfloat16* k_cache;           // [B][window][n_kv][128]
+  __nv_bfloat16* v_cache;
+  const float* q_norm;              // [128]
+  const float* k_norm;              // [128]
+  const float* sinks;               // [n_q]
+  float* qkv;                       // [8][n_q 128 + 2 n_kv 128] projections
+  __nv_bfloat16* ob;                // [8][n_q 128] attention output per head
+  float* part;                      // [B n_kv splits][8][130] per-split (o, max, sum)
+  unsigned* split_cnt;              // [B n_kv] splits finished (kept at zero between calls)
+  unsigned* bar;                    // grid barrier counter, zero at launch
+  unsigned* err;
+  int B, d, n_q, n_kv, window, use_rope, add_residual, splits;
+  float eps, rope_base;
+  uint64_t wait_ns;
+};
+size_t attn_decode_smem_bytes(int d, int n_q);
+cudaError_t launch_attn_decode(const AttnArgs& a, int num_sms, cudaStream_t s);
+
 // ---------------------------------------------------------------- 4-bit output layer
 constexpr int kHdMaxT = 8;          // tokens per launch of the output-layer kernel
 constexpr int kHdConsumers = 8;

@@ -330,3 +330,34 @@ def make_tokens_torch(spec: LayerSpec, seed: int, T: int, device):
     g.manual_seed(int(seed) * 7919 + 17)
     x = torch.randn(T, spec.d, generator=g, device=device) * spec.sigma_x
     return x.to(torch.bfloat16) if spec.act == "bf16" else x
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window attention of the Flint decoder (swarmz.net, "Recursive Flint:
+# 40B Open Model, 2.5B Active", section "The architecture, in plain terms"):
+# 32 query heads over 4 key/value heads of dimension 128, a 513-token window.
+# ---------------------------------------------------------------------------
+FLINT_ATTN = {"d": 2048, "n_q": 32, "n_kv": 4, "hd": 128, "window": 513}
+TID_WQ, TID_WK, TID_WV, TID_WO, TID_QN, TID_KN, TID_SINK, TID_KC, TID_VC = 20, 21, 22, 23, 24, 25, 26, 27, 28
+
+
+def make_attention(seed: int, layer: int = 0, d: int = 2048, n_q: int = 32, n_kv: int = 4, hd: int = 128,
+                   sigma: float = 0.02) -> dict:
+    """Attention weights: wq [n_q hd][d], wk, wv [n_kv hd][d], wo [d][n_q hd] as bf16 bit patterns
+    (N(0, sigma^2)); q_norm, k_norm [hd] float32 around 1 (1 + N(0, 0.1^2)); sinks [n_q] float32 N(0, 1)."""
+    W = {}
+    for name, tid, shape in (("wq", TID_WQ, (n_q * hd, d)), ("wk", TID_WK, (n_kv * hd, d)),
+                             ("wv", TID_WV, (n_kv * hd, d)), ("wo", TID_WO, (d, n_q * hd))):
+        W[name] = bf16_bits(normal_f32(seed, layer, tid, shape, sigma))
+    W["q_norm"] = (1.0 + normal_f32(seed, layer, TID_QN, (hd,), 0.1)).astype(np.float32)
+    W["k_norm"] = (1.0 + normal_f32(seed, layer, TID_KN, (hd,), 0.1)).astype(np.float32)
+    W["sinks"] = normal_f32(seed, layer, TID_SINK, (n_q,), 1.0)
+    return W
+
+
+def make_kv_cache(seed: int, B: int, window: int, n_kv: int = 4, hd: int = 128, layer: int = 0):
+    """Key and value ring buffers [B][window][n_kv][hd] as bf16 bit patterns: keys N(0, 1) (the scale of
+    normalised keys), values N(0, 0.8^2) (the scale of Wv x for N(0, 1) activations and N(0, 0.02^2) weights)."""
+    k = bf16_bits(normal_f32(seed, layer, TID_KC, (B, window, n_kv, hd), 1.0))
+    v = bf16_bits(normal_f32(seed, layer, TID_VC, (B, window, n_kv, hd), 0.8))
+    return k, v
