@@ -54,6 +54,10 @@ STACK_DECODE = {"stack47_decode1": 1, "stack47_decode8": 8}
 # the 4-bit output layer (vocabulary 146,432 x d 2048, NVFP4), four copies in rotation
 HEAD = {"lmhead1": 1, "lmhead8": 8}
 HEAD_COPIES = 4
+# sliding-window attention at decode: B sequences at position 4096 (full 513-token window), 8 layers in rotation
+ATTN = {"attn1": 1, "attn8": 8}
+ATTN_LAYERS = 8
+ATTN_POS = 4096
 D, E_ROUTED, F_EXP, TOPK = 2048, 256, 512, 6
 B_EXP_BF16 = 3 * D * F_EXP * 2                       # bytes of one expert's three bf16 matrices
 B_EXP_NVFP4 = 3 * (D * F_EXP // 2 + D * F_EXP // 16 + 4)
@@ -495,6 +499,72 @@ def measure_head(args, name, T, device, stream):
             "roofline": roof, "clocks": clocks, "launches_per_forward": 1, "gpu_launches": n * len(heads)}
 
 
+def measure_attn(args, name, Bn, device, stream):
+    """Sliding-window GQA attention at decode, Bn sequences, ATTN_LAYERS layers' weights and caches in rotation."""
+    import numpy as np
+    import torch
+    from sparse_moe_transformer_02_b300 import binding as B
+    from sparse_moe_transformer_02_b300 import inputs as I
+    A = I.FLINT_ATTN
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+    base = {k: dev(v) for k, v in I.make_attention(seed=args.seed).items()}
+    kc0, vc0 = (dev(t) for t in I.make_kv_cache(args.seed, Bn, A["window"]))
+    layers = []
+    for _ in range(ATTN_LAYERS):
+        w = {k: t.clone() for k, t in base.items()}
+        layers.append((B.MoeAttn(w, A["d"], A["n_q"], A["n_kv"], A["window"], max_batch=8), kc0.clone(),
+                       vc0.clone()))
+    x = I.make_tokens_torch(I.FLINT_BF16, seed=args.seed + 41, T=Bn, device=device)
+    pos = torch.full((Bn,), ATTN_POS, dtype=torch.int32, device=device)
+    ys = [torch.empty_like(x) for _ in layers]
+
+    def step():
+        for (at, kc, vc), y in zip(layers, ys):
+            at.decode(x, pos, kc, vc, y, stream=stream)
+    step()
+    stream.synchronize()
+    for at, _, _ in layers:
+        if at.check(stream) != B.MOE_OK:
+            raise RuntimeError(f"{name}: device error")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 100
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    clocks = sampler.stop()
+    t = ev0.elapsed_time(ev1) / 1e3 / n / len(layers)
+    del graph
+    for at, _, _ in layers:
+        at.close()
+    pk = peaks()
+    d, qd, kvd, W = A["d"], A["n_q"] * A["hd"], A["n_kv"] * A["hd"], A["window"]
+    byt = (qd + 2 * kvd) * d * 2 + d * qd * 2 + Bn * (W * kvd * 2 * 2 + 2 * d * 2 + kvd * 2 * 2) + 4 * Bn
+    flops = 2 * Bn * ((qd + 2 * kvd) * d + d * qd + 2 * W * qd)
+    roof = binding(byt, 0, t, pk)
+    roof.update({"kernel": "attn_decode_kernel", "kernel_ms": round(t * 1e3, 5), "traffic": dram_traffic("attn", name),
+                 "algorithmic_bytes": int(byt), "flops": int(flops), "peak_source": pk["source"]})
+    return {"name": name, "tokens_per_s": round(Bn / t, 1), "B": Bn, "position": ATTN_POS,
+            "us_per_layer": round(t * 1e6, 2), "roofline": roof, "clocks": clocks, "launches_per_forward": 1,
+            "gpu_launches": n * len(layers)}
+
+
 # ------------------------------------------------------------------ the CPU oracle as a baseline
 def oracle_rates(kind, T, seed, budget_s, steps=1, procs=1):
     """The float64 oracle on bounded samples of the workload, in a fresh
@@ -619,6 +689,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         for wname, Tn in HEAD.items():
             sweep[wname] = measure_head(args, wname, Tn, device, stream)
+        for wname, Bn in ATTN.items():
+            sweep[wname] = measure_attn(args, wname, Bn, device, stream)
         torch.cuda.empty_cache()
 
     cpu = None
@@ -660,6 +732,8 @@ def run_only(args):
         r = measure_stack_decode(args, args.only, spec, wts, STACK_DECODE[args.only], device, stream)
     elif args.only in HEAD:
         r = measure_head(args, args.only, HEAD[args.only], device, stream)
+    elif args.only in ATTN:
+        r = measure_attn(args, args.only, ATTN[args.only], device, stream)
     else:
         kind, T, n, chain = WORKLOADS[args.only]
         spec, wts = make_layer_set(kind, args.layers or n, device, seed=args.seed)
@@ -719,7 +793,8 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
-    ap.add_argument("--only", default=None, choices=sorted(list(WORKLOADS) + list(STACK_DECODE) + list(HEAD)),
+    ap.add_argument("--only", default=None,
+                    choices=sorted(list(WORKLOADS) + list(STACK_DECODE) + list(HEAD) + list(ATTN)),
                     help="run one sweep entry alone and print its result (profiling)")
     ap.add_argument("--rank-selftest", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()

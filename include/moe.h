@@ -315,7 +315,7 @@ typedef struct {
   int32_t n_q;            /* query heads */
   int32_t n_kv;           /* key/value heads; n_q / n_kv <= 8 query heads share one */
   int32_t head_dim;       /* 128 */
-  int32_t window;         /* positions attended: the current one and window - 1 before it */
+  int32_t window;         /* positions attended: the current one and window - 1 before it; at most 4096 */
   int32_t max_batch;      /* largest B (sequences per call), 1..8 */
   int32_t use_rope;       /* nonzero: rotate queries and keys (the sliding-window layers) */
   int32_t add_residual;   /* nonzero: y = x + attn(x) */
@@ -352,8 +352,9 @@ typedef struct {
  * at the top of this library's design notes.
  *
  * Errors: MOE_ERR_INVALID_ARG (NULL, non-positive sizes, misalignment),
- * MOE_ERR_UNSUPPORTED (head_dim != 128, n_q / n_kv > 8, d not a multiple of
- * 256, max_batch > 8, no cooperative launch), MOE_ERR_OOM, MOE_ERR_CUDA.
+ * MOE_ERR_UNSUPPORTED (head_dim != 128, n_q / n_kv > 8, n_q > 64, d not a
+ * multiple of 256, window > 4096, max_batch > 8, no cooperative launch),
+ * MOE_ERR_OOM, MOE_ERR_CUDA.
  */
 moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* w, moe_attn_handle* out);
 

@@ -102,7 +102,7 @@ __device__ __forceinline__ float reduce8(float v0, float v1, float v2, float v3,
 }
 
 struct AtLayout {
-  uint32_t stages, bars, abort, prod, act, red, total, x_pitch, o_pitch;
+  uint32_t stages, bars, abort, prod, tab, act, red, total, x_pitch, o_pitch;
 };
 // Offsets from the 1024-aligned base (the allocation carries 1024 bytes of slack).
 __host__ __device__ inline AtLayout at_layout(int d, int qdim) {
@@ -115,9 +115,11 @@ __host__ __device__ inline AtLayout at_layout(int d, int qdim) {
   L.abort = o;  o += 16;
   L.prod = o;   o += 4 * (kAtConsumers + kAtStages);
   o = (o + 15) & ~15u;
+  L.tab = o;    o += 2 * kAtHd * 4 + (kAtHd / 2) * 8 + 64 * 4;   // q_norm, k_norm, RoPE turns, sinks (n_q <= 64)
+  o = (o + 15) & ~15u;
   L.act = o;                                        // x rows (1), attention scratch (2) or o rows (3)
   const uint32_t xs = kAtMaxT * L.x_pitch, os = kAtMaxT * L.o_pitch;
-  const uint32_t scratch = (kAtMaxGroup * kAtHd + 2 * kAtHd) * 4 + kAtConsumers * kAtMaxGroup * kAtWp * 4 + 256;
+  const uint32_t scratch = (kAtMaxGroup * kAtHd + 4 * kAtHd) * 4 + kAtConsumers * kAtMaxGroup * kAtWp * 4 + 256;
   uint32_t m = xs > os ? xs : os;
   m = m > scratch ? m : scratch;
   o += m;
@@ -266,27 +268,31 @@ __device__ __forceinline__ bool grid_sync(AtCtx& c, unsigned target) {
 }
 
 // RMSNorm with gamma, then RoPE at position pos, of one 128-value head held as
-// 4 values per lane (lane l: values 2l, 2l + 1, 64 + 2l, 65 + 2l).
+// 4 values per lane (lane l: values 2l, 2l + 1, 64 + 2l, 65 + 2l).  The angle
+// of pair i is pos * f_i turns with f_i = base^(-2 i / 128) / (2 pi) stored as
+// a 64-bit fraction (turns[i] = f_i 2^64, made on the host in fp64): the
+// product's low 64 bits are pos * f_i mod 1 exactly, so the reduced angle
+// keeps full precision at any position with integer arithmetic only.
 __device__ __forceinline__ void norm_rope(float (&v)[4], const float* gamma, float eps, int pos, bool use_rope,
-                                          double base, int lane) {
+                                          const unsigned long long* turns, int lane) {
   float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(kAll, ss, o);
   const float r = rsqrtf(ss / (float)kAtHd + eps);
   const int i0 = 2 * lane;
-  v[0] *= r * __ldg(gamma + i0);
-  v[1] *= r * __ldg(gamma + i0 + 1);
-  v[2] *= r * __ldg(gamma + 64 + i0);
-  v[3] *= r * __ldg(gamma + 64 + i0 + 1);
+  v[0] *= r * gamma[i0];
+  v[1] *= r * gamma[i0 + 1];
+  v[2] *= r * gamma[64 + i0];
+  v[3] *= r * gamma[64 + i0 + 1];
   if (!use_rope) return;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    // angle pos * base^(-2 i / 128), reduced in fp64 so large positions stay exact
-    const int i = i0 + j;
-    const double ang = (double)pos * pow(base, -2.0 * i / kAtHd);
-    const double red = ang - 6.283185307179586 * floor(ang / 6.283185307179586);
+    const unsigned long long frac = (unsigned long long)(unsigned)pos * turns[i0 + j];
+    // the turn as a signed fraction in [-1/2, 1/2): the angle lands in [-pi, pi),
+    // where the fast sine and cosine are accurate to about 2^-21
+    const float ang = (float)((long long)frac >> 40) * (6.283185307179586f / 16777216.f);
     float sn, cs;
-    sincosf((float)red, &sn, &cs);
+    __sincosf(ang, &sn, &cs);
     const float x0 = v[j], x1 = v[2 + j];
     v[j] = x0 * cs - x1 * sn;
     v[2 + j] = x0 * sn + x1 * cs;
@@ -299,6 +305,32 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
   const int B = a.B, d = a.d, qdim = a.n_q * kAtHd, kvdim = a.n_kv * kAtHd, R = qdim + 2 * kvdim;
   const int group = a.n_q / a.n_kv;
   int m = 0;
+  // tables of phase 2 in shared memory (gammas, RoPE turns, sinks), and this
+  // CTA's keys and values pulled into L2 while phase 1 runs
+  float* tq = reinterpret_cast<float*>(c.smem + c.L.tab);
+  float* tk = tq + kAtHd;
+  unsigned long long* tt = reinterpret_cast<unsigned long long*>(tk + kAtHd);
+  float* tsk = reinterpret_cast<float*>(tt + kAtHd / 2);
+  for (int i = tid; i < kAtHd; i += NT) {
+    tq[i] = __ldg(a.q_norm + i);
+    tk[i] = __ldg(a.k_norm + i);
+    if (i < kAtHd / 2) tt[i] = __ldg(a.rope_turns + i);
+    if (i < a.n_q) tsk[i] = __ldg(a.sinks + i);
+  }
+  {
+    const int S = a.splits, n_items = B * a.n_kv * S;
+    for (int item = c.b; item < n_items; item += c.G) {
+      const int bq = item / (a.n_kv * S), g = (item / S) % a.n_kv, sp = item % S;
+      const int pos = max(__ldg(a.pos + bq), 0), W = a.window;
+      const int n_keys = pos + 1 < W ? pos + 1 : W, first = pos + 1 - n_keys;
+      const int j0 = (int)(((long long)n_keys * sp) / S), j1 = (int)(((long long)n_keys * (sp + 1)) / S);
+      for (int j = j0 + tid; j < j1; j += NT) {
+        const size_t sl = (((size_t)bq * W + ((first + j) % W)) * a.n_kv + g) * kAtHd;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(a.k_cache + sl) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(a.v_cache + sl) : "memory");
+      }
+    }
+  }
   // ---------------- phase 1: q, k, v
   {
     uint8_t* xs = c.smem + c.L.act;
@@ -329,7 +361,9 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
     float* qs = reinterpret_cast<float*>(c.smem + c.L.act);            // [group][128] normalised, rotated q
     float* kn = qs + kAtMaxGroup * kAtHd;                               // [128] new key (bf16 values)
     float* vn = kn + kAtHd;                                             // [128] new value (bf16 values)
-    float* wst = vn + kAtHd;                                            // [8 warps][group][kAtWp]
+    uint16_t* knb = reinterpret_cast<uint16_t*>(vn + kAtHd);           // [128] new key, bf16 bits
+    uint16_t* vnb = knb + kAtHd;                                        // [128] new value, bf16 bits
+    float* wst = vn + 2 * kAtHd;                                        // [8 warps][group][kAtWp]
     const float scale = rsqrtf((float)kAtHd);
     for (int item = c.b; item < n_items; item += c.G) {
       const int bq = item / (a.n_kv * S), g = (item / S) % a.n_kv, sp = item % S;
@@ -349,7 +383,7 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
         const float* src = task < group ? qrow + (g * group + task) * kAtHd : qrow + qdim + g * kAtHd;
         const int i0 = 2 * lane;
         v[0] = __ldcg(src + i0); v[1] = __ldcg(src + i0 + 1); v[2] = __ldcg(src + 64 + i0); v[3] = __ldcg(src + 65 + i0);
-        norm_rope(v, task < group ? a.q_norm : a.k_norm, a.eps, pos, a.use_rope != 0, a.rope_base, lane);
+        norm_rope(v, task < group ? tq : tk, a.eps, pos, a.use_rope != 0, tt, lane);
         float* dst = task < group ? qs + task * kAtHd : kn;
         if (task == group) {                     // the cache holds bf16
 #pragma unroll
@@ -357,8 +391,16 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
         }
         dst[i0] = v[0]; dst[i0 + 1] = v[1]; dst[64 + i0] = v[2]; dst[65 + i0] = v[3];
         if (task == group) {
+          knb[i0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
+          knb[i0 + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
+          knb[64 + i0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2]));
+          knb[65 + i0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[3]));
           const float* vs = qrow + qdim + kvdim + g * kAtHd;
-          for (int i = lane; i < kAtHd; i += 32) vn[i] = __bfloat162float(__float2bfloat16_rn(__ldcg(vs + i)));
+          for (int i = lane; i < kAtHd; i += 32) {
+            const __nv_bfloat16 vb = __float2bfloat16_rn(__ldcg(vs + i));
+            vn[i] = __bfloat162float(vb);
+            vnb[i] = __bfloat16_as_ushort(vb);
+          }
         }
       }
       named_sync(NT);
@@ -383,36 +425,64 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         qv[h][0] = t4.x; qv[h][1] = t4.y; qv[h][2] = t4.z; qv[h][3] = t4.w;
       }
-      for (int j = j0 + w; j < j1; j += kAtConsumers) {
-        const int p = first + j;
-        float kk[4], vv[4];
-        if (p == pos) {
-          const float4 k4 = *reinterpret_cast<const float4*>(kn + 4 * lane);
-          const float4 v4 = *reinterpret_cast<const float4*>(vn + 4 * lane);
-          kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
-          vv[0] = v4.x; vv[1] = v4.y; vv[2] = v4.z; vv[3] = v4.w;
-        } else {
-          const size_t sl = (((size_t)bq * W + (p % W)) * a.n_kv + g) * kAtHd + 4 * lane;
-          const uint2 kb = __ldcg(reinterpret_cast<const uint2*>(a.k_cache + sl));
-          const uint2 vb = __ldcg(reinterpret_cast<const uint2*>(a.v_cache + sl));
-          kk[0] = __uint_as_float(kb.x << 16); kk[1] = __uint_as_float(kb.x & 0xFFFF0000u);
-          kk[2] = __uint_as_float(kb.y << 16); kk[3] = __uint_as_float(kb.y & 0xFFFF0000u);
-          vv[0] = __uint_as_float(vb.x << 16); vv[1] = __uint_as_float(vb.x & 0xFFFF0000u);
-          vv[2] = __uint_as_float(vb.y << 16); vv[3] = __uint_as_float(vb.y & 0xFFFF0000u);
+      // keys j0 + w, j0 + w + 8, ...: eight at a time, all their loads issued
+      // before any of them is used (the new token's entry comes from shared
+      // memory, the others from the cache)
+      for (int jb = j0 + w; jb < j1; jb += 8 * kAtConsumers) {
+        uint2 kbv[8], vbv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = jb + u * kAtConsumers;
+          kbv[u] = make_uint2(0u, 0u);
+          vbv[u] = make_uint2(0u, 0u);
+          if (j < j1) {
+            const int p = first + j;
+            if (p == pos) {                      // shared memory
+              kbv[u] = *reinterpret_cast<const uint2*>(knb + 4 * lane);
+              vbv[u] = *reinterpret_cast<const uint2*>(vnb + 4 * lane);
+            } else {                             // the cache, through L2
+              const size_t sl = (((size_t)bq * W + (p % W)) * a.n_kv + g) * kAtHd + 4 * lane;
+              kbv[u] = __ldcg(reinterpret_cast<const uint2*>(a.k_cache + sl));
+              vbv[u] = __ldcg(reinterpret_cast<const uint2*>(a.v_cache + sl));
+            }
+          }
         }
+        // all eight scores first (independent reductions), then one rescale per head for the batch
+        float zs[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float kk[4];
+          kk[0] = __uint_as_float(kbv[u].x << 16); kk[1] = __uint_as_float(kbv[u].x & 0xFFFF0000u);
+          kk[2] = __uint_as_float(kbv[u].y << 16); kk[3] = __uint_as_float(kbv[u].y & 0xFFFF0000u);
 #define AT_DOT(h) (qv[h][0] * kk[0] + qv[h][1] * kk[1] + qv[h][2] * kk[2] + qv[h][3] * kk[3])
-        const float s_lane = reduce8(AT_DOT(0), AT_DOT(1), AT_DOT(2), AT_DOT(3), AT_DOT(4), AT_DOT(5), AT_DOT(6),
-                                     AT_DOT(7), lane);
+          zs[u] = reduce8(AT_DOT(0), AT_DOT(1), AT_DOT(2), AT_DOT(3), AT_DOT(4), AT_DOT(5), AT_DOT(6), AT_DOT(7),
+                          lane);   // lane 4 h holds head h's score
 #undef AT_DOT
+        }
+        const int nu = (j1 - jb + kAtConsumers - 1) / kAtConsumers;   // keys of this batch (>= 1)
 #pragma unroll
         for (int h = 0; h < kAtMaxGroup; ++h) {
           if (h < group) {
-            const float z = __shfl_sync(kAll, s_lane, 4 * h) * scale;   // lane 4 h holds head h's score
-            const float mn = fmaxf(mx[h], z);
-            const float f = __expf(mx[h] - mn), pz = __expf(z - mn);
-            sm[h] = sm[h] * f + pz;
+            float z[8], mb = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[h][q] = o[h][q] * f + pz * vv[q];
+            for (int u = 0; u < 8; ++u) {
+              z[u] = u < nu ? __shfl_sync(kAll, zs[u], 4 * h) * scale : -INFINITY;
+              mb = fmaxf(mb, z[u]);
+            }
+            const float mn = fmaxf(mx[h], mb);
+            const float f = __expf(mx[h] - mn);
+            sm[h] *= f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[h][q] *= f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float pz = __expf(z[u] - mn);       // 0 for the batch's missing keys
+              sm[h] += pz;
+              o[h][0] += pz * __uint_as_float(vbv[u].x << 16);
+              o[h][1] += pz * __uint_as_float(vbv[u].x & 0xFFFF0000u);
+              o[h][2] += pz * __uint_as_float(vbv[u].y << 16);
+              o[h][3] += pz * __uint_as_float(vbv[u].y & 0xFFFF0000u);
+            }
             mx[h] = mn;
           }
         }
@@ -458,21 +528,48 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
       named_sync(NT);
       if (last) {
         const float* p0 = a.part + (size_t)(bq * a.n_kv + g) * S * kAtMaxGroup * (kAtHd + 2);
+        // warp h: the split weights exp(m_s - M) / L of head h (sink included) into shared memory
+        float* fw = wst;                                   // [group][kAtMaxSplit] (the warp states are done)
+        if (w < group) {
+          const float sink = tsk[g * group + w];
+          float ms[2], ls[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int s2 = lane + 32 * u;
+            ms[u] = s2 < S ? __ldcg(p0 + ((size_t)s2 * kAtMaxGroup + w) * (kAtHd + 2) + kAtHd) : -INFINITY;
+            ls[u] = s2 < S ? __ldcg(p0 + ((size_t)s2 * kAtMaxGroup + w) * (kAtHd + 2) + kAtHd + 1) : 0.f;
+          }
+          float M = fmaxf(sink, fmaxf(ms[0], ms[1]));
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
+          float f[2], L = 0.f;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            f[u] = ms[u] == -INFINITY ? 0.f : __expf(ms[u] - M);
+            L += ls[u] * f[u];
+          }
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kAll, L, o);
+          L += __expf(sink - M);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (lane + 32 * u < S) fw[w * kAtMaxSplit + lane + 32 * u] = f[u] / L;
+        }
+        named_sync(NT);
         for (int i = tid; i < group * kAtHd; i += NT) {
           const int h = i / kAtHd, e = i % kAtHd;
-          const float sink = __ldg(a.sinks + g * group + h);
-          float M = sink;
-          for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, __ldcg(p0 + ((size_t)s2 * kAtMaxGroup + h) * (kAtHd + 2) + kAtHd));
-          float L = __expf(sink - M), acc = 0.f;
-          for (int s2 = 0; s2 < S; ++s2) {
-            const float* pp = p0 + ((size_t)s2 * kAtMaxGroup + h) * (kAtHd + 2);
-            const float ms = __ldcg(pp + kAtHd);
-            if (ms == -INFINITY) continue;
-            const float f = __expf(ms - M);
-            L += __ldcg(pp + kAtHd + 1) * f;
-            acc += __ldcg(pp + e) * f;
+          float acc = 0.f;
+          // eight splits' loads in flight at a time (a loop of dependent L2 round trips would serialise them)
+          for (int s0 = 0; s0 < S; s0 += 8) {
+            float pv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              pv[u] = s0 + u < S ? __ldcg(p0 + ((size_t)(s0 + u) * kAtMaxGroup + h) * (kAtHd + 2) + e) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (s0 + u < S) acc += pv[u] * fw[h * kAtMaxSplit + s0 + u];
           }
-          a.ob[(size_t)bq * qdim + (g * group + h) * kAtHd + e] = __float2bfloat16_rn(acc / L);
+          a.ob[(size_t)bq * qdim + (g * group + h) * kAtHd + e] = __float2bfloat16_rn(acc);
         }
       }
       named_sync(NT);
@@ -571,6 +668,7 @@ struct moe_attn {
   unsigned* split_cnt = nullptr;
   unsigned* bar = nullptr;
   unsigned* err = nullptr;
+  unsigned long long* turns = nullptr;   // [64] RoPE frequencies as 64-bit fractions of a turn
   uint64_t wait_ns = 0;
 };
 
@@ -590,7 +688,7 @@ moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* w
       (reinterpret_cast<uintptr_t>(w->k_norm) & 3u) || (reinterpret_cast<uintptr_t>(w->sinks) & 3u))
     return MOE_ERR_INVALID_ARG;
   if (c.head_dim != kAtHd || c.n_q % c.n_kv != 0 || c.n_q / c.n_kv > kAtMaxGroup || c.d % kAtSeg != 0 ||
-      c.max_batch > kAtMaxT || c.n_kv * kAtMaxT > 240)
+      c.max_batch > kAtMaxT || c.n_kv * kAtMaxT > 240 || c.n_q > 64)
     return MOE_ERR_UNSUPPORTED;
   moe_attn* h = new (std::nothrow) moe_attn();
   if (!h) return MOE_ERR_OOM;
@@ -622,9 +720,13 @@ moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* w
     return MOE_ERR_CUDA;
   }
   const size_t B = kAtMaxT, R = qdim + 2 * kvdim;
+  if ((c.window + 63) / 64 > kAtMaxSplit) {
+    delete h;
+    return MOE_ERR_UNSUPPORTED;
+  }
   const size_t n_part = B * c.n_kv * kAtMaxSplit * kAtMaxGroup * (kAtHd + 2);
   const size_t bytes = ((B * R * 4 + 255) & ~(size_t)255) + ((B * qdim * 2 + 255) & ~(size_t)255) +
-                       ((n_part * 4 + 255) & ~(size_t)255) + 1024;
+                       ((n_part * 4 + 255) & ~(size_t)255) + 1024 + 512;
   if (dev_malloc(&h->block, bytes) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -637,6 +739,21 @@ moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* w
   h->split_cnt = reinterpret_cast<unsigned*>(p);       // [B * n_kv] (at most 256 words with the bar and err)
   h->bar = h->split_cnt + 240;
   h->err = h->split_cnt + 248;
+  h->turns = reinterpret_cast<unsigned long long*>(p + 1024);
+  {
+    // f_i = base^(-2 i / 128) / (2 pi) turns per position, as f_i 2^64 (f_i < 1)
+    unsigned long long t[kAtHd / 2];
+    for (int i = 0; i < kAtHd / 2; ++i) {
+      const double f = pow((double)c.rope_base, -2.0 * i / kAtHd) / 6.283185307179586476925286766559;
+      t[i] = (unsigned long long)ldexp(f, 64);
+    }
+    if (cudaMemcpy(h->turns, t, sizeof(t), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(h->block);
+      delete h;
+      return MOE_ERR_CUDA;
+    }
+  }
   if (cudaMemset(h->split_cnt, 0, 1024) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->block);
@@ -691,9 +808,10 @@ moe_status moe_attn_decode(moe_attn_handle h, const void* x, int32_t B, const in
   a.use_rope = c.use_rope;
   a.add_residual = c.add_residual;
   a.eps = c.eps;
-  a.rope_base = c.rope_base;
-  const int items = B * c.n_kv;
-  int S = (h->num_sms + items - 1) / items;
+  a.rope_turns = h->turns;
+  // window splits per (sequence, kv head): at most 64 keys each, so every
+  // warp takes a single batch of 8 keys and the combine reads few partials
+  int S = (c.window + 63) / 64;
   S = S < 1 ? 1 : (S > kAtMaxSplit ? kAtMaxSplit : S);
   a.splits = S;
   a.wait_ns = h->wait_ns;

@@ -301,8 +301,9 @@ struct AttnArgs {
   unsigned* split_cnt;              // [B n_kv] splits finished (kept at zero between calls)
   unsigned* bar;                    // grid barrier counter, zero at launch
   unsigned* err;
+  const unsigned long long* rope_turns;   // [64] base^(-2 i / 128) / (2 pi) as 64-bit fractions of a turn
   int B, d, n_q, n_kv, window, use_rope, add_residual, splits;
-  float eps, rope_base;
+  float eps;
   uint64_t wait_ns;
 };
 size_t attn_decode_smem_bytes(int d, int n_q);
