@@ -247,6 +247,25 @@ __device__ __forceinline__ bool consume_group(AtCtx& c, int& m, int KC, uint32_t
   return true;
 }
 
+// Copy rows global -> shared memory with eight 16-byte loads in flight per thread.
+__device__ __forceinline__ void stage_rows(uint8_t* dst, uint32_t dst_pitch, const uint8_t* src, size_t src_pitch,
+                                           int rows, int chunks, int tid, int nt) {
+  const int n = rows * chunks;
+  for (int i0 = tid; i0 < n; i0 += 8 * nt) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * nt;
+      if (i < n) v[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(i / chunks) * src_pitch) + i % chunks);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * nt;
+      if (i < n) *reinterpret_cast<uint4*>(dst + (i / chunks) * dst_pitch + (i % chunks) * 16) = v[u];
+    }
+  }
+}
+
 __device__ __forceinline__ bool grid_sync(AtCtx& c, unsigned target) {
   named_sync(32 * kAtConsumers);
   bool bad = false;
@@ -334,12 +353,7 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
   // ---------------- phase 1: q, k, v
   {
     uint8_t* xs = c.smem + c.L.act;
-    const int chunks = d / 8;
-    for (int i = tid; i < B * chunks; i += NT) {
-      const int t = i / chunks, q = i % chunks;
-      *reinterpret_cast<uint4*>(xs + t * c.L.x_pitch + q * 16) =
-          __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d) + q);
-    }
+    stage_rows(xs, c.L.x_pitch, reinterpret_cast<const uint8_t*>(a.x), (size_t)d * 2, B, d / 8, tid, NT);
     named_sync(NT);
     int lo, hi;
     share(R / 16, c.b, c.G, lo, hi);
@@ -580,12 +594,7 @@ __device__ __forceinline__ void run_consumers(AtCtx& c) {
   // ---------------- phase 3: output projection
   {
     uint8_t* os = c.smem + c.L.act;
-    const int chunks = qdim / 8;
-    for (int i = tid; i < B * chunks; i += NT) {
-      const int t = i / chunks, q = i % chunks;
-      *reinterpret_cast<uint4*>(os + t * c.L.o_pitch + q * 16) =
-          __ldcg(reinterpret_cast<const uint4*>(a.ob + (size_t)t * qdim) + q);
-    }
+    stage_rows(os, c.L.o_pitch, reinterpret_cast<const uint8_t*>(a.ob), (size_t)qdim * 2, B, qdim / 8, tid, NT);
     named_sync(NT);
     int lo, hi;
     share(d / 16, c.b, c.G, lo, hi);

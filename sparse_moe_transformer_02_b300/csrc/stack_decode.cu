@@ -374,6 +374,27 @@ __device__ __forceinline__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int 
   return true;
 }
 
+// Copy `rows` rows of `chunks` 16-byte pieces from global (src_pitch bytes)
+// to shared memory (dst_pitch bytes), eight loads in flight per thread before
+// any store (a load-store loop would serialise one L2 round trip per piece).
+__device__ __forceinline__ void stage_rows(uint8_t* dst, uint32_t dst_pitch, const uint8_t* src, size_t src_pitch,
+                                           int rows, int chunks, int tid, int nt) {
+  const int n = rows * chunks;
+  for (int i0 = tid; i0 < n; i0 += 8 * nt) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * nt;
+      if (i < n) v[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(i / chunks) * src_pitch) + i % chunks);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * nt;
+      if (i < n) *reinterpret_cast<uint4*>(dst + (i / chunks) * dst_pitch + (i % chunks) * 16) = v[u];
+    }
+  }
+}
+
 // Top-k of token t (one warp): larger logit first, lower expert index first on
 // equal logits; gates = softmax of the selected logits.
 __device__ __forceinline__ void topk_token(const float* part, int E, int k, int t, Rt& rt, int lane) {
@@ -512,11 +533,7 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
     {
       uint8_t* xs = c.smem + c.L.xs;
       const int chunks = d / 8;
-      for (int i = tid; i < T * chunks; i += NT) {
-        const int t = i / chunks, q = i % chunks;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(xcur + (size_t)t * d) + q);
-        *reinterpret_cast<uint4*>(xs + t * c.L.x_pitch + q * 16) = v;
-      }
+      stage_rows(xs, c.L.x_pitch, reinterpret_cast<const uint8_t*>(xcur), (size_t)d * 2, T, chunks, tid, NT);
       if (l == 0 && a.x_trace && c.b == 0)
         for (int i = tid; i < T * chunks; i += NT)
           __stcg(reinterpret_cast<uint4*>(a.x_trace) + i, __ldcg(reinterpret_cast<const uint4*>(a.x_in) + i));
@@ -602,12 +619,7 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
     const int nslots = T * k + (has_sh ? T : 0);
     {
       uint8_t* hs = c.smem + c.L.xs;
-      const int chunks = Fmax / 8;
-      for (int i = tid; i < nslots * chunks; i += NT) {
-        const int r = i / chunks, q = i % chunks;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.h + (size_t)r * Fmax) + q);
-        *reinterpret_cast<uint4*>(hs + r * c.L.h_pitch + q * 16) = v;
-      }
+      stage_rows(hs, c.L.h_pitch, reinterpret_cast<const uint8_t*>(a.h), (size_t)Fmax * 2, nslots, Fmax / 8, tid, NT);
     }
     // CTAs that own no output rows pull the next layer's router rows into L2
     // meanwhile, so its logits do not wait on HBM latency
