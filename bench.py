@@ -184,6 +184,8 @@ def layer_bytes_flops(kind, T, U_mean):
 
 def kernel_bytes_flops(kname, kind, T, U_mean):
     """Algorithmic bytes and tensor flops of one launch of a kernel of the layer."""
+    if kname == "fused":                       # the persistent kernel does the whole layer
+        return layer_bytes_flops(kind, T, U_mean)
     b_exp = B_EXP_NVFP4 if kind == "nvfp4" else B_EXP_BF16
     byt = {"route": 4 * D * E_ROUTED + 4 * E_ROUTED + T * D * 2,
            "gemv_gateup": (U_mean + 1) * b_exp * 2 / 3 + T * D * 2,

@@ -61,7 +61,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_NVFP4 = 2 } moe_dtype;
 
 /* Which expert-FFN kernels moe_forward uses. */
 typedef enum {
-  MOE_PATH_AUTO = 0,   /* tcgen05 grouped GEMM when the weights allow it, else the GEMV kernels */
+  MOE_PATH_AUTO = 0,   /* T <= 8 with bf16 weights and activations, E <= 256 and d, F, F_s multiples of
+                          256: one persistent cooperative launch (routing, gate/up, down with grid-wide
+                          barriers between them); otherwise the tcgen05 grouped GEMM when the weights
+                          allow it, else the GEMV kernels */
   MOE_PATH_GEMV = 1,   /* always the weight-streaming GEMV kernels */
   MOE_PATH_TC = 2      /* always the tcgen05 grouped GEMM: bf16 activations with bf16 weights (d, F, F_s
                           multiples of 128) or NVFP4 weights (multiples of 256; the codes are decoded into
@@ -232,7 +235,8 @@ typedef enum {
   MOE_K_TC_GATEUP = 4,     /* tcgen05 gate/up + SwiGLU */
   MOE_K_TC_DOWN = 5,       /* tcgen05 down + gated accumulate */
   MOE_K_TC_FINALIZE = 6,   /* fp32 accumulator -> output */
-  MOE_K_COUNT = 7
+  MOE_K_FUSED = 7,         /* the persistent kernel: routing, gate/up and down in one launch (T <= 8) */
+  MOE_K_COUNT = 8
 } moe_kernel_id;
 
 /*

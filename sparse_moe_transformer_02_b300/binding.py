@@ -24,7 +24,8 @@ EXPORTED = ["moe_status_string", "moe_create", "moe_destroy", "moe_route", "moe_
             "moe_stack_create", "moe_stack_destroy", "moe_stack_uses_persistent", "moe_stack_forward",
             "moe_stack_check", "moe_head_create", "moe_head_forward", "moe_head_check", "moe_head_destroy",
             "moe_attn_create", "moe_attn_decode", "moe_attn_check", "moe_attn_destroy"]
-KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize"]
+KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "tc_down", "tc_finalize",
+                "fused"]
 
 
 class moe_config(ctypes.Structure):

@@ -29,6 +29,14 @@ struct moe_layer {
   bool fp4 = false;            // NVFP4 weights (tcgen05 path decodes them into tensor memory)
   CUtensorMap q4[3], sc4[3], sq4[3], ssc4[3];   // NVFP4 codes / block scales: gate, up, down (routed, shared)
   void* block = nullptr;
+  // The persistent decode kernel run as a stack of one layer (T <= kSdMaxT)
+  bool sd_capable = false;
+  void* sd_block = nullptr;          // layer pointers, tensor maps, partial logits, h, barrier counter
+  StackLayerPtrs* sd_layer = nullptr;
+  CUtensorMap* sd_maps = nullptr;
+  float* sd_logits = nullptr;
+  __nv_bfloat16* sd_h = nullptr;
+  unsigned* sd_bar = nullptr;
   Prof prof;
 };
 
@@ -307,9 +315,86 @@ moe_status do_route(moe_layer* h, const void* x, int32_t T, int32_t* idx, float*
   return cuda_status(launch_route(ra, h->num_sms, s, &h->prof));
 }
 
+// The persistent decode kernel as a stack of one layer: its layer pointers and
+// tensor maps in device memory, its scratch (partial logits, h, the grid
+// barrier counter).  Leaves sd_capable false when the shapes or the device do
+// not allow it (the other paths serve every T then).
+moe_status setup_fused(moe_layer* h, cudaStream_t stream) {
+  const moe_config& c = h->cfg;
+  bool query_ok = true;
+  if (!stack_decode_supported(c, &query_ok)) return query_ok ? MOE_OK : MOE_ERR_CUDA;
+  CUtensorMap maps[kSdMaps];
+  std::memset(maps, 0, sizeof(maps));
+  if (!stack_layer_views(c, h->w, maps)) return MOE_OK;
+  const moe_weights& w = h->w;
+  const StackLayerPtrs lp{w.router_w, w.router_b,
+                          static_cast<const __nv_bfloat16*>(w.w_gate), static_cast<const __nv_bfloat16*>(w.w_up),
+                          static_cast<const __nv_bfloat16*>(w.w_down), static_cast<const __nv_bfloat16*>(w.ws_gate),
+                          static_cast<const __nv_bfloat16*>(w.ws_up), static_cast<const __nv_bfloat16*>(w.ws_down)};
+  const size_t Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
+  const size_t nmaps = up256(sizeof(maps)), nlp = up256(sizeof(lp));
+  const size_t nlog = up256((size_t)4 * kSdMaxT * c.num_experts * 4);
+  const size_t nh = up256((size_t)kSdMaxT * (c.top_k + 1) * Fmax * 2);
+  if (dev_malloc(&h->sd_block, nmaps + nlp + nlog + nh + 256) != cudaSuccess) {
+    cudaGetLastError();
+    h->sd_block = nullptr;
+    return MOE_ERR_OOM;
+  }
+  uint8_t* p = static_cast<uint8_t*>(h->sd_block);
+  h->sd_maps = reinterpret_cast<CUtensorMap*>(p); p += nmaps;
+  h->sd_layer = reinterpret_cast<StackLayerPtrs*>(p); p += nlp;
+  h->sd_logits = reinterpret_cast<float*>(p); p += nlog;
+  h->sd_h = reinterpret_cast<__nv_bfloat16*>(p); p += nh;
+  h->sd_bar = reinterpret_cast<unsigned*>(p);
+  if (cudaMemcpyAsync(h->sd_maps, maps, sizeof(maps), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(h->sd_layer, &lp, sizeof(lp), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->sd_block);
+    h->sd_block = nullptr;
+    return MOE_ERR_CUDA;
+  }
+  h->sd_capable = true;
+  return MOE_OK;
+}
+
+moe_status run_fused(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
+                     cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  if (cudaMemsetAsync(h->sd_bar, 0, 4, s) != cudaSuccess) return cuda_status(cudaGetLastError());
+  StackArgs a;
+  a.layers = h->sd_layer;
+  a.maps = h->sd_maps;
+  a.L = 1;
+  a.x_in = static_cast<const __nv_bfloat16*>(x);
+  a.y_out = static_cast<__nv_bfloat16*>(y);
+  a.xbuf = nullptr;                  // one layer: x_in -> y_out
+  a.logits = h->sd_logits;
+  a.h = h->sd_h;
+  a.x_trace = nullptr;
+  a.idx_trace = idx_out;             // routing of the layer, each written when given
+  a.gate_trace = gate_out;
+  a.bar = h->sd_bar;
+  a.err = h->ws.err;
+  a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+  a.add_residual = c.add_residual != 0;
+  a.g_offsets = h->ws.offsets;       // kept for moe_get_grouping
+  a.g_tok_of_slot = h->ws.tok_of_slot;
+  a.g_slot_of = h->ws.slot_of;
+  a.wait_ns = h->wait_ns;
+  h->prof.begin(MOE_K_FUSED, s);
+  const cudaError_t e = launch_stack_decode(a, h->num_sms, s);
+  h->prof.end(s);
+  return cuda_status(e);
+}
+
 moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
                        cudaStream_t s) {
   const moe_config& c = h->cfg;
+  // AUTO, small batches: the persistent kernel (routing, gate/up and down in
+  // one launch with grid-wide barriers between the phases)
+  if (c.path == MOE_PATH_AUTO && h->sd_capable && T <= kSdMaxT && T > c.gemv_max_tokens)
+    return run_fused(h, x, T, y, idx_out, gate_out, s);
   int32_t* idx = idx_out ? idx_out : h->ws.idx;
   float* gate = gate_out ? gate_out : h->ws.gate;
   // AUTO: the tensor-core path whenever the weights allow it (it streams the
@@ -568,6 +653,14 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       h->tc_capable = false;
     }
   }
+  if (c.path == MOE_PATH_AUTO) {
+    moe_status sst = setup_fused(h, stream);
+    if (sst != MOE_OK) {
+      cudaFree(h->block);
+      delete h;
+      return sst;
+    }
+  }
   *out = h;
   return MOE_OK;
 }
@@ -577,6 +670,7 @@ moe_status moe_destroy(moe_handle h) {
   cudaError_t e = cudaDeviceSynchronize();
   for (cudaEvent_t ev : h->prof.ev) cudaEventDestroy(ev);
   cudaError_t f = cudaFree(h->block);
+  if (h->sd_block && cudaFree(h->sd_block) != cudaSuccess) f = cudaErrorInvalidValue;
   delete h;
   return (e == cudaSuccess && f == cudaSuccess) ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -278,9 +278,23 @@ struct StackArgs {
   unsigned* bar;                    // grid barrier counter, zero at launch
   unsigned* err;                    // device error word
   int T, d, F, Fs, E, k;
+  int add_residual;                 // y = x + moe(x) (always set for a stack)
+  int32_t* g_offsets;               // [E + 1] grouping of layer 0 (exclusive scan of the counts), or nullptr
+  int32_t* g_tok_of_slot;           // [T k] with g_offsets
+  int32_t* g_slot_of;               // [T k] with g_offsets
   uint64_t wait_ns;
 };
 size_t stack_decode_smem_bytes(int d, int F, int Fs, int k);
+// Whether the persistent kernel can serve a layer of this configuration on
+// the current device: bf16 weights and activations, at most 256 experts (one
+// warp's top-k), at most 8 per token, widths in whole 256-value segments, a
+// device of compute capability 10.x that launches cooperative grids, and its
+// shared-memory plan within the device's opt-in limit.  *query_ok = false
+// when a device query failed.
+bool stack_decode_supported(const moe_config& c, bool* query_ok);
+// The kSdMaps 3-D tile views of one layer's weights ({64 values, rows, K / 64},
+// 128-byte swizzle; 8-row boxes for gate/up, 16-row boxes for down).
+bool stack_layer_views(const moe_config& c, const moe_weights& w, CUtensorMap* maps);
 
 // ---------------------------------------------------------------- sliding-window attention (decode)
 constexpr int kAtMaxT = 8;          // sequences per attention launch

@@ -7,6 +7,41 @@
 
 #include "moe_internal.cuh"
 
+namespace moe {
+
+bool stack_decode_supported(const moe_config& c, bool* query_ok) {
+  *query_ok = true;
+  int dev = 0, coop = 0, cc_major = 0, smem_optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    *query_ok = false;
+    return false;
+  }
+  return c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.num_experts <= 256 && c.top_k <= 8 &&
+         c.d % 256 == 0 && c.ffn % 256 == 0 && c.shared_ffn % 256 == 0 && cc_major == 10 && coop &&
+         stack_decode_smem_bytes(c.d, c.ffn, c.shared_ffn, c.top_k) <= (size_t)smem_optin;
+}
+
+bool stack_layer_views(const moe_config& c, const moe_weights& w, CUtensorMap* m) {
+  auto view = [](CUtensorMap* t, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    const uint64_t dims[3] = {64, rows, K / 64}, strides[2] = {K * 2, 128};
+    const uint32_t box[3] = {64, box_rows, 4};
+    return encode_tiled(t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  const uint64_t E = c.num_experts, d = c.d, F = c.ffn, Fs = c.shared_ffn;
+  bool ok = view(m + kMapWg, w.w_gate, E * F, d, 8) && view(m + kMapWu, w.w_up, E * F, d, 8) &&
+            view(m + kMapWd, w.w_down, E * d, F, 16);
+  if (ok && Fs > 0)
+    ok = view(m + kMapSg, w.ws_gate, Fs, d, 8) && view(m + kMapSu, w.ws_up, Fs, d, 8) &&
+         view(m + kMapSd, w.ws_down, d, Fs, 16);
+  return ok;
+}
+
+}  // namespace moe
+
 using namespace moe;
 
 struct moe_stack {
@@ -64,24 +99,16 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
     }
     s->layers.push_back(h);
   }
-  int coop = 0, cc_major = 0, smem_optin = 0;
-  if (cudaGetDevice(&s->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, s->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, s->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, s->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, s->device) != cudaSuccess) {
+  bool query_ok = true;
+  s->persistent = stack_decode_supported(c, &query_ok);
+  if (!query_ok || cudaGetDevice(&s->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, s->device) != cudaSuccess) {
     cudaGetLastError();
     free_stack(s);
     return MOE_ERR_CUDA;
   }
   s->wait_ns = (uint64_t)(c.wait_timeout_ms > 0 ? c.wait_timeout_ms : 2000) * 1000000ull;
   const int Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
-  // The persistent kernel: bf16 weights and activations, at most 256 experts
-  // (one warp's top-k), widths in whole 256-value segments, its shared-memory
-  // plan within the device's limit, and a device that launches cooperative grids.
-  s->persistent = c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16 && c.num_experts <= 256 &&
-                  c.d % 256 == 0 && c.ffn % 256 == 0 && c.shared_ffn % 256 == 0 && cc_major == 10 && coop &&
-                  stack_decode_smem_bytes(c.d, c.ffn, c.shared_ffn, c.top_k) <= (size_t)smem_optin;
   const size_t es = c.act_dtype == MOE_F32 ? 4 : 2;
   const size_t nx = (size_t)kSdMaxT * c.d * 2, nlog = (size_t)4 * kSdMaxT * c.num_experts * 4;
   const size_t nh = (size_t)kSdMaxT * (c.top_k + 1) * Fmax * 2, nchain = (size_t)c.max_tokens * c.d * es;
@@ -109,24 +136,9 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
                              static_cast<const __nv_bfloat16*>(w.w_down), static_cast<const __nv_bfloat16*>(w.ws_gate),
                              static_cast<const __nv_bfloat16*>(w.ws_up), static_cast<const __nv_bfloat16*>(w.ws_down)};
     }
-    // 3-D tile views of every weight stack: {64 values, rows, K / 64 chunks}
     std::vector<CUtensorMap> maps((size_t)n_layers * kSdMaps);
-    auto view = [](CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
-      const uint64_t dims[3] = {64, rows, K / 64}, strides[2] = {K * 2, 128};
-      const uint32_t box[3] = {64, box_rows, 4};
-      return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-    };
-    const uint64_t E = c.num_experts, d = c.d, F = c.ffn, Fs = c.shared_ffn;
     bool ok = true;
-    for (int l = 0; l < n_layers && ok; ++l) {
-      const moe_weights& w = layers[l];
-      CUtensorMap* m = &maps[(size_t)l * kSdMaps];
-      ok = view(m + kMapWg, w.w_gate, E * F, d, 8) && view(m + kMapWu, w.w_up, E * F, d, 8) &&
-           view(m + kMapWd, w.w_down, E * d, F, 16);
-      if (ok && Fs > 0)
-        ok = view(m + kMapSg, w.ws_gate, Fs, d, 8) && view(m + kMapSu, w.ws_up, Fs, d, 8) &&
-             view(m + kMapSd, w.ws_down, d, Fs, 16);
-    }
+    for (int l = 0; l < n_layers && ok; ++l) ok = stack_layer_views(c, layers[l], &maps[(size_t)l * kSdMaps]);
     void* dl = nullptr;
     void* dm = nullptr;
     if (ok && (dev_malloc(&dl, sizeof(StackLayerPtrs) * n_layers) != cudaSuccess ||
@@ -208,6 +220,8 @@ moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void*
     a.bar = h->bar;
     a.err = h->err;
     a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+    a.add_residual = 1;
+    a.g_offsets = a.g_tok_of_slot = a.g_slot_of = nullptr;
     a.wait_ns = h->wait_ns;
     if (launch_stack_decode(a, h->num_sms, stream) != cudaSuccess) {
       cudaGetLastError();

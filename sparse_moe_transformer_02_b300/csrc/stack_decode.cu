@@ -11,6 +11,9 @@
 // the layers follow each other inside one cooperative grid (one CTA per SM)
 // separated by grid-wide barriers.
 //
+// A single layer (moe_forward with T <= 8) runs as a stack of one, with the
+// residual add optional.
+//
 // Per layer three phases, each ending in a grid barrier:
 //   A  router logits (fp32; each expert row split over 4 warps across the
 //      grid, plain loads, partial sums added in a fixed order by the top-k)
@@ -22,8 +25,8 @@
 //   C  down projection: CTA b owns output rows [16 rb, 16 rb + 16) for
 //      rb = b, b + G, ...; its consumer warps take the shared expert and the
 //      active experts in turn, weight their rows by the gates and the CTA sums
-//      the warps in a fixed order (deterministic), adds the residual x and
-//      rounds the new residual stream to bf16.
+//      the warps in a fixed order (deterministic), adds the residual x (in
+//      a stack; optional for a single layer) and rounds to bf16.
 //
 // Inside a CTA one producer thread streams weights with TMA tile loads into a
 // 16-stage shared-memory ring (two stages per consumer warp, each stage 16
@@ -451,7 +454,9 @@ __device__ __forceinline__ void topk_token(const float* part, int E, int k, int 
 
 // Grouping of the T k slots by expert (one warp): active experts ascending,
 // slots of one expert in (token, j) order.
-__device__ __forceinline__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane) {
+// slot_of (global memory, may be null) receives the grouped position of each
+// slot t k + j.
+__device__ __forceinline__ void group_slots_warp(Rt& rt, int T, int k, int E, int lane, int32_t* slot_of) {
   const int ns = T * k;
   for (int e = lane; e < 256; e += 32) rt.cnt[e] = 0;
   __syncwarp();
@@ -506,11 +511,13 @@ __device__ __forceinline__ void group_slots_warp(Rt& rt, int T, int k, int E, in
     const int p = rt.off[e0] + r0;
     rt.slot_tok[p] = s0 / k;
     rt.slot_gate[p] = rt.sel_g[s0];
+    if (slot_of) slot_of[s0] = p;
   }
   if (v1) {
     const int p = rt.off[e1] + r1;
     rt.slot_tok[p] = s1 / k;
     rt.slot_gate[p] = rt.sel_g[s1];
+    if (slot_of) slot_of[s1] = p;
   }
   __syncwarp();
 }
@@ -592,13 +599,17 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
     // routing (every CTA), then hand it to the producer
     if (w < T) topk_token(a.logits, E, k, w, c.rt, lane);
     named_sync(1, NT);
-    if (w == 0) group_slots_warp(c.rt, T, k, E, lane);
+    if (w == 0) group_slots_warp(c.rt, T, k, E, lane, c.b == 0 ? a.g_slot_of : nullptr);
     named_sync(1, NT);
+    if (c.b == 0 && a.g_offsets) {             // the grouping, for a caller that asks for it
+      for (int i = tid; i <= E; i += NT) a.g_offsets[i] = i < E ? c.rt.off[i] : T * k;
+      for (int i = tid; i < T * k; i += NT) a.g_tok_of_slot[i] = c.rt.slot_tok[i];
+    }
     if (tid == 0) mbar_arrive(c.route_bar);
-    if (c.b == 0 && a.idx_trace)
+    if (c.b == 0 && (a.idx_trace || a.gate_trace))
       for (int i = tid; i < T * k; i += NT) {
-        a.idx_trace[(size_t)l * T * k + i] = c.rt.sel_e[i];
-        a.gate_trace[(size_t)l * T * k + i] = c.rt.sel_g[i];
+        if (a.idx_trace) a.idx_trace[(size_t)l * T * k + i] = c.rt.sel_e[i];
+        if (a.gate_trace) a.gate_trace[(size_t)l * T * k + i] = c.rt.sel_g[i];
       }
     const int U = *c.rt.n_act;
     // phase B: routed row groups
@@ -671,7 +682,9 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
         const int row = i / T, t = i % T, r = rb * 16 + row;
         float y = 0.f;
         for (int ww = 0; ww < kSdConsumers; ++ww) y += yw[(ww * 16 + row) * kSdMaxT + t];
-        y += __bfloat162float(__ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short*>(xcur) + (size_t)t * d + r)));
+        if (a.add_residual)
+          y += __bfloat162float(
+              __ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short*>(xcur) + (size_t)t * d + r)));
         const unsigned short ob = __bfloat16_as_ushort(__float2bfloat16_rn(y));
         __stcg(reinterpret_cast<unsigned short*>(xnext) + (size_t)t * d + r, ob);
         if (a.x_trace)
