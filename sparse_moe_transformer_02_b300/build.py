@@ -14,8 +14,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["moe_api.cu", "route.cu", "gemv.cu", "gemm_tc.cu", "gemm_tc_fp4.cu", "route_noalloc.cu",
-           "stack_decode.cu", "stack_api.cu", "lm_head.cu", "attn_decode.cu"]
-HEADERS = ["moe_internal.cuh", "ptx.cuh", "units.cuh"]
+           "stack_decode.cu", "stack_decode_fp4.cu", "stack_api.cu", "lm_head.cu", "attn_decode.cu"]
+HEADERS = ["moe_internal.cuh", "ptx.cuh", "units.cuh", "persist.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -29,8 +29,18 @@ struct moe_layer {
   bool fp4 = false;            // NVFP4 weights (tcgen05 path decodes them into tensor memory)
   CUtensorMap q4[3], sc4[3], sq4[3], ssc4[3];   // NVFP4 codes / block scales: gate, up, down (routed, shared)
   void* block = nullptr;
-  // The persistent decode kernel run as a stack of one layer (T <= kSdMaxT)
+  // The persistent decode kernels run as a stack of one layer (bf16 weights:
+  // T <= kSdMaxT; NVFP4 weights: T <= kS4MaxT)
   bool sd_capable = false;
+  bool s4_capable = false;
+  CUtensorMap* s4_maps = nullptr;
+  Stack4LayerPtrs* s4_layer = nullptr;
+  __half* s4_xh = nullptr;
+  float* s4_xsc = nullptr;
+  __half* s4_h = nullptr;
+  float* s4_o = nullptr;
+  int32_t* s4_topk_e = nullptr;
+  float* s4_topk_g = nullptr;
   void* sd_block = nullptr;          // layer pointers, tensor maps, partial logits, h, barrier counter
   StackLayerPtrs* sd_layer = nullptr;
   CUtensorMap* sd_maps = nullptr;
@@ -319,8 +329,11 @@ moe_status do_route(moe_layer* h, const void* x, int32_t T, int32_t* idx, float*
 // tensor maps in device memory, its scratch (partial logits, h, the grid
 // barrier counter).  Leaves sd_capable false when the shapes or the device do
 // not allow it (the other paths serve every T then).
+moe_status setup_fused4(moe_layer* h, cudaStream_t stream);
+
 moe_status setup_fused(moe_layer* h, cudaStream_t stream) {
   const moe_config& c = h->cfg;
+  if (c.weight_dtype == MOE_NVFP4) return setup_fused4(h, stream);
   bool query_ok = true;
   if (!stack_decode_supported(c, &query_ok)) return query_ok ? MOE_OK : MOE_ERR_CUDA;
   CUtensorMap maps[kSdMaps];
@@ -356,6 +369,86 @@ moe_status setup_fused(moe_layer* h, cudaStream_t stream) {
   }
   h->sd_capable = true;
   return MOE_OK;
+}
+
+// The NVFP4 persistent kernel as a stack of one layer: tensor maps, layer
+// pointers and scratch (partial logits, the f16 copy of x and its scales, h,
+// the per-slot down outputs, the barrier counter).
+moe_status setup_fused4(moe_layer* h, cudaStream_t stream) {
+  const moe_config& c = h->cfg;
+  bool query_ok = true;
+  if (!stack_decode_fp4_supported(c, &query_ok)) return query_ok ? MOE_OK : MOE_ERR_CUDA;
+  CUtensorMap maps[kS4Maps];
+  std::memset(maps, 0, sizeof(maps));
+  if (!stack_layer_views_fp4(c, h->w, maps)) return MOE_OK;
+  const moe_weights& w = h->w;
+  const Stack4LayerPtrs lp{w.router_w, w.router_b, w.t_gate, w.t_up, w.t_down, w.ts_gate, w.ts_up, w.ts_down};
+  const size_t Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn, E = c.num_experts, d = c.d;
+  const size_t slots = (size_t)kS4MaxT * (c.top_k + 1);
+  const size_t nmaps = up256(sizeof(maps)), nlp = up256(sizeof(lp));
+  const size_t nlog = up256((d + 511) / 512 * kS4MaxT * E * 4), nxh = up256((size_t)kS4MaxT * d * 2);
+  const size_t nxs = up256((size_t)kS4MaxT * 4), nh = up256(slots * Fmax * 2), no = up256(slots * d * 4);
+  const size_t ntk = up256((size_t)kS4MaxT * kMaxTopK * 4);
+  if (dev_malloc(&h->sd_block, nmaps + nlp + nlog + nxh + nxs + nh + no + 2 * ntk + 256) != cudaSuccess) {
+    cudaGetLastError();
+    h->sd_block = nullptr;
+    return MOE_ERR_OOM;
+  }
+  uint8_t* p = static_cast<uint8_t*>(h->sd_block);
+  h->s4_maps = reinterpret_cast<CUtensorMap*>(p); p += nmaps;
+  h->s4_layer = reinterpret_cast<Stack4LayerPtrs*>(p); p += nlp;
+  h->sd_logits = reinterpret_cast<float*>(p); p += nlog;
+  h->s4_xh = reinterpret_cast<__half*>(p); p += nxh;
+  h->s4_xsc = reinterpret_cast<float*>(p); p += nxs;
+  h->s4_h = reinterpret_cast<__half*>(p); p += nh;
+  h->s4_o = reinterpret_cast<float*>(p); p += no;
+  h->s4_topk_e = reinterpret_cast<int32_t*>(p); p += ntk;
+  h->s4_topk_g = reinterpret_cast<float*>(p); p += ntk;
+  h->sd_bar = reinterpret_cast<unsigned*>(p);
+  if (cudaMemcpyAsync(h->s4_maps, maps, sizeof(maps), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(h->s4_layer, &lp, sizeof(lp), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->sd_block);
+    h->sd_block = nullptr;
+    return MOE_ERR_CUDA;
+  }
+  h->s4_capable = true;
+  return MOE_OK;
+}
+
+moe_status run_fused4(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
+                      cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  if (cudaMemsetAsync(h->sd_bar, 0, 4, s) != cudaSuccess) return cuda_status(cudaGetLastError());
+  Stack4Args a;
+  a.layers = h->s4_layer;
+  a.maps = h->s4_maps;
+  a.L = 1;
+  a.x_in = static_cast<const __nv_bfloat16*>(x);
+  a.y_out = static_cast<__nv_bfloat16*>(y);
+  a.xbuf = nullptr;                  // one layer: x_in -> y_out
+  a.logits = h->sd_logits;
+  a.xh = h->s4_xh;
+  a.xsc = h->s4_xsc;
+  a.h = h->s4_h;
+  a.o = h->s4_o;
+  a.topk_e = h->s4_topk_e;
+  a.topk_g = h->s4_topk_g;
+  a.idx_trace = idx_out;
+  a.gate_trace = gate_out;
+  a.g_offsets = h->ws.offsets;       // kept for moe_get_grouping
+  a.g_tok_of_slot = h->ws.tok_of_slot;
+  a.g_slot_of = h->ws.slot_of;
+  a.bar = h->sd_bar;
+  a.err = h->ws.err;
+  a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+  a.add_residual = c.add_residual != 0;
+  a.wait_ns = h->wait_ns;
+  h->prof.begin(MOE_K_FUSED, s);
+  const cudaError_t e = launch_stack_decode_fp4(a, h->num_sms, s);
+  h->prof.end(s);
+  return cuda_status(e);
 }
 
 moe_status run_fused(moe_layer* h, const void* x, int32_t T, void* y, int32_t* idx_out, float* gate_out,
@@ -395,6 +488,8 @@ moe_status run_forward(moe_layer* h, const void* x, int32_t T, void* y, int32_t*
   // one launch with grid-wide barriers between the phases)
   if (c.path == MOE_PATH_AUTO && h->sd_capable && T <= kSdMaxT && T > c.gemv_max_tokens)
     return run_fused(h, x, T, y, idx_out, gate_out, s);
+  if (c.path == MOE_PATH_AUTO && h->s4_capable && T <= kS4MaxT && T > c.gemv_max_tokens)
+    return run_fused4(h, x, T, y, idx_out, gate_out, s);
   int32_t* idx = idx_out ? idx_out : h->ws.idx;
   float* gate = gate_out ? gate_out : h->ws.gate;
   // AUTO: the tensor-core path whenever the weights allow it (it streams the

@@ -296,6 +296,54 @@ bool stack_decode_supported(const moe_config& c, bool* query_ok);
 // 128-byte swizzle; 8-row boxes for gate/up, 16-row boxes for down).
 bool stack_layer_views(const moe_config& c, const moe_weights& w, CUtensorMap* maps);
 
+// ---------------------------------------------------------------- persistent decode kernel, NVFP4 weights
+constexpr int kS4MaxT = 32;          // tokens per launch of the NVFP4 persistent kernel
+constexpr int kS4Consumers = 8;      // consumer warps per CTA
+// Tensor maps of one layer, [L][kS4Maps]: index 2 m (codes) and 2 m + 1
+// (block scales) for m = routed gate, up, down, shared gate, up, down.
+constexpr int kS4Maps = 12;
+struct Stack4LayerPtrs {
+  const float* wr;                  // [E][d] router (fp32)
+  const float* br;                  // [E] or nullptr
+  const float* tg; const float* tu; const float* td;      // [E] tensor scales of the routed matrices
+  const float* tsg; const float* tsu; const float* tsd;   // [1] tensor scales of the shared matrices
+};
+struct Stack4Args {
+  const Stack4LayerPtrs* layers;    // [L], device memory
+  const CUtensorMap* maps;          // [L][kS4Maps], device memory
+  int L;
+  const __nv_bfloat16* x_in;        // [T][d]
+  __nv_bfloat16* y_out;             // [T][d]
+  __nv_bfloat16* xbuf;              // [2][kS4MaxT][d] residual stream between layers (L > 1)
+  float* logits;                    // [ceil(d / 512)][kS4MaxT][E] partial router logits (512-value parts)
+  __half* xh;                       // [kS4MaxT][d] x / xs as f16
+  float* xsc;                       // [kS4MaxT] xs: a power of two per token
+  __half* h;                        // [kS4MaxT (k + 1)][Fmax] h / xs^2 as f16 (routed slots, then the shared rows)
+  float* o;                         // [kS4MaxT (k + 1)][d] gate-weighted down outputs per slot
+  int32_t* topk_e;                  // [kS4MaxT k] selections published across the grid (T > 8)
+  float* topk_g;                    // [kS4MaxT k] their gates
+  int32_t* idx_trace;               // [L][T][k] or nullptr
+  float* gate_trace;                // [L][T][k] or nullptr
+  int32_t* g_offsets;               // [E + 1] grouping of layer 0, or nullptr
+  int32_t* g_tok_of_slot;           // [T k] with g_offsets
+  int32_t* g_slot_of;               // [T k] with g_offsets
+  unsigned* bar;                    // grid barrier counter, zero at launch
+  unsigned* err;                    // device error word
+  int T, d, F, Fs, E, k, add_residual;
+  uint64_t wait_ns;
+};
+size_t stack_decode_fp4_smem_bytes();
+// Whether the NVFP4 persistent kernel can serve this configuration on the
+// current device (NVFP4 weights with bf16 activations, E <= 256, k <= 8,
+// d, F, F_s multiples of 256, compute capability 10.x, cooperative launch,
+// shared memory within the opt-in limit).  *query_ok = false when a device
+// query failed.
+bool stack_decode_fp4_supported(const moe_config& c, bool* query_ok);
+// The kS4Maps tile maps of one layer (codes: 128-byte boxes with the 128-byte
+// swizzle; block scales: 16-byte boxes; 32-row boxes for gate/up, 64 for down).
+bool stack_layer_views_fp4(const moe_config& c, const moe_weights& w, CUtensorMap* maps);
+cudaError_t launch_stack_decode_fp4(const Stack4Args& a, int num_sms, cudaStream_t s);
+
 // ---------------------------------------------------------------- sliding-window attention (decode)
 constexpr int kAtMaxT = 8;          // sequences per attention launch
 

@@ -49,17 +49,19 @@
 // give up after the limit, set the device error word (timeout bit) and the
 // CTA unwinds, draining its bulk copies first.
 #include "moe_internal.cuh"
+#include "persist.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace persist;
 
 constexpr int kSdThreads = 32 * (1 + kSdConsumers);
 constexpr int kSdStages = 2 * kSdConsumers;         // two per consumer warp
 constexpr int kSdSeg = 256;                         // values per row segment
 constexpr int kSdRq = 4;                            // warps per router row
 constexpr int kSdStageBytes = 16 * kSdSeg * 2;      // 8192 bytes: 16 rows x 4 chunks x 128 bytes
-constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -72,29 +74,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-// Named barrier that also ORs a flag over the participating threads: every
-// thread gets the same answer, so a decision taken on it is uniform even if
-// the abort flag changes meanwhile (the producer warp may set it at any time).
-__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %3, 0;\n\t"
-      "bar.red.or.pred q, %1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"(n), "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 // Shared-memory layout (byte offsets), computed identically on host and device.
 struct SdLayout {
   uint32_t stages, bars, route_bar, abort, xs, red, yw, rt, total;
@@ -141,33 +120,6 @@ __device__ __forceinline__ Rt rt_of(uint8_t* base) {
   r.cnt = p; p += 256;
   r.off = p;
   return r;
-}
-
-// Grid barrier: every consumer thread of every CTA calls it; one thread per
-// CTA arrives on the counter (release) and waits for the target (acquire).
-__device__ __forceinline__ bool grid_sync(unsigned* ctr, unsigned target, const WaitCtl& wc, volatile int* abort_flag) {
-  named_sync(1, 32 * kSdConsumers);
-  bool bad = false;
-  if (threadIdx.x == 32) {
-    if (!*abort_flag) {
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
-      // poll without sleeping (the barrier is on the critical path), bounded in time
-      bool ok = ld_acquire_gpu(ctr) >= target;
-      if (!ok) {
-        const uint64_t t0 = global_ns();
-        for (uint32_t it = 1; !ok; ++it) {
-          ok = ld_acquire_gpu(ctr) >= target;
-          if (!ok && (it & 255u) == 0 && global_ns() - t0 > wc.limit_ns) break;
-        }
-      }
-      if (!ok) {
-        atomicOr(wc.err, kErrTimeout);
-        *abort_flag = 1;
-        bad = true;
-      }
-    }
-  }
-  return !named_sync_or(1, 32 * kSdConsumers, bad || *abort_flag != 0);
 }
 
 // The producer's view of the ring: consumer c owns stages 2c, 2c + 1 and
@@ -377,81 +329,6 @@ __device__ __forceinline__ bool consume_gu(SdCtx& c, Cons& C, int d, int g, int 
   return true;
 }
 
-// Copy `rows` rows of `chunks` 16-byte pieces from global (src_pitch bytes)
-// to shared memory (dst_pitch bytes), eight loads in flight per thread before
-// any store (a load-store loop would serialise one L2 round trip per piece).
-__device__ __forceinline__ void stage_rows(uint8_t* dst, uint32_t dst_pitch, const uint8_t* src, size_t src_pitch,
-                                           int rows, int chunks, int tid, int nt) {
-  const int n = rows * chunks;
-  for (int i0 = tid; i0 < n; i0 += 8 * nt) {
-    uint4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * nt;
-      if (i < n) v[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(i / chunks) * src_pitch) + i % chunks);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * nt;
-      if (i < n) *reinterpret_cast<uint4*>(dst + (i / chunks) * dst_pitch + (i % chunks) * 16) = v[u];
-    }
-  }
-}
-
-// Top-k of token t (one warp): larger logit first, lower expert index first on
-// equal logits; gates = softmax of the selected logits.
-__device__ __forceinline__ void topk_token(const float* part, int E, int k, int t, Rt& rt, int lane) {
-  float lg[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    lg[i] = 0.f;
-    if (e < E) {
-#pragma unroll
-      for (int q = 0; q < kSdRq; ++q) lg[i] += __ldcg(part + ((size_t)q * kSdMaxT + t) * E + e);
-    }
-  }
-  // order-preserving 32-bit keys of the logits (0 = taken or absent)
-  uint32_t key[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t u = __float_as_uint(lg[i]);
-    key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-  }
-  // k rounds: the warp's largest key (redux max), then the lowest expert
-  // index holding it (redux min); the winner goes straight to shared memory
-  // (its logit parked in sel_g until the gates)
-  for (int j = 0; j < k; ++j) {
-    uint32_t lm = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lm = key[i] > lm ? key[i] : lm;
-    const uint32_t wm = __reduce_max_sync(kFull, lm);
-    uint32_t cand = 0xFFFFFFFFu;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (key[i] == wm) cand = min(cand, (uint32_t)(lane + 32 * i));
-    const uint32_t win = __reduce_min_sync(kFull, cand);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((uint32_t)(lane + 32 * i) == win) key[i] = 0;
-    if (lane == 0) {
-      const uint32_t u = (wm & 0x80000000u) ? (wm & 0x7FFFFFFFu) : ~wm;
-      rt.sel_e[t * k + j] = (int)win;
-      rt.sel_g[t * k + j] = __uint_as_float(u);
-    }
-  }
-  __syncwarp();
-  // gates: softmax of the k selected logits (lane j holds selection j)
-  const float l0 = rt.sel_g[t * k];
-  const float lj = lane < k ? rt.sel_g[t * k + lane] : l0;
-  const float ej = lane < k ? expf(lj - l0) : 0.f;
-  float sum = ej;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-  __syncwarp();
-  if (lane < k) rt.sel_g[t * k + lane] = ej / sum;
-}
-
 // Grouping of the T k slots by expert (one warp): active experts ascending,
 // slots of one expert in (token, j) order.
 // slot_of (global memory, may be null) receives the grouped position of each
@@ -594,10 +471,10 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
     for (int g = c.b; g < nsh; g += c.G, ++rg)
       if (!consume_gu(c, C, d, g, T, rg, [&](int n) { return n; }, [&](int n) { return T * k + n; }, a.h, Fmax))
         return;
-    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, 32 * kSdConsumers, 32)) return;
 
     // routing (every CTA), then hand it to the producer
-    if (w < T) topk_token(a.logits, E, k, w, c.rt, lane);
+    if (w < T) topk_token(a.logits, kSdRq, kSdMaxT, E, k, w, c.rt.sel_e, c.rt.sel_g, lane);
     named_sync(1, NT);
     if (w == 0) group_slots_warp(c.rt, T, k, E, lane, c.b == 0 ? a.g_slot_of : nullptr);
     named_sync(1, NT);
@@ -624,7 +501,7 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
           return;
       }
     }
-    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, 32 * kSdConsumers, 32)) return;
 
     // phase C: stage h (routed slots, then the shared expert's T rows) in shared memory
     const int nslots = T * k + (has_sh ? T : 0);
@@ -692,7 +569,7 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
       }
       named_sync(1, NT);
     }
-    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag)) return;
+    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, 32 * kSdConsumers, 32)) return;
   }
 }
 
