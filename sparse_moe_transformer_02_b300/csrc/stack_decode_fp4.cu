@@ -563,15 +563,10 @@ __device__ __forceinline__ void run_consumers(Ctx& c) {
                 acc[tt] = fmaf(wv[u].x, xv.x, fmaf(wv[u].y, xv.y, fmaf(wv[u].z, xv.z, fmaf(wv[u].w, xv.w, acc[tt]))));
               }
           }
-#pragma unroll
-          for (int tt = 0; tt < kTp; ++tt) {
-            if (tp + tt < T) {
-              float v = acc[tt];
-#pragma unroll
-              for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-              if (lane == 0) __stcg(a.logits + ((size_t)q * kS4MaxT + tp + tt) * E + e, v + bias);
-            }
-          }
+          // butterfly transpose-reduction: lanes 2 i and 2 i + 1 end with token tp + i's sum
+          const float v = transpose_reduce<kTp, 32>(acc, lane);
+          const int tt = lane >> 1;
+          if ((lane & 1) == 0 && tp + tt < T) __stcg(a.logits + ((size_t)q * kS4MaxT + tp + tt) * E + e, v + bias);
         }
       }
       named_sync(1, kNT);   // the slice is restaged by the next round
@@ -647,81 +642,23 @@ __device__ __forceinline__ void run_consumers(Ctx& c) {
         for (int i = tid; i < T * k; i += kNT) a.g_tok_of_slot[i] = c.rt.slot_tok[i];
       }
     }
+    // ---- phases B (gate/up units) and C (down units): one loop, one copy of
+    // the stage arithmetic; a grid barrier after each
     bool ok = true;
-    {
+#pragma unroll 1
+    for (int ph = 0; ph < 2; ++ph) {
       int lo, hi;
-      share(gu_units(c.rt, gps, gpe), c.G, c.b, lo, hi);
+      share(ph == 0 ? gu_units(c.rt, gps, gpe) : c.rt.n_ent[0] * rbn, c.G, c.b, lo, hi);
       for (int u = lo + w; u < hi && ok; u += kC) {
-        const GuUnit gu = gu_unit(c.rt, u, gps, gpe);
-        const int e = c.rt.ent_e[gu.ent], off = c.rt.ent_off[gu.ent], cnt = c.rt.ent_cnt[gu.ent];
-        const bool sh = e < 0;
-        const int ntl = (cnt + 7) >> 3;
-        const uint8_t* brow[kNt];
-#pragma unroll
-        for (int n = 0; n < kNt; ++n) {
-          const int col = n * 8 + g, cc = col < cnt ? col : 0;
-          const int tok = sh ? off - T * k + cc : c.rt.slot_tok[off + cc];
-          brow[n] = reinterpret_cast<const uint8_t*>(a.xh + (size_t)tok * d);
+        int ent, sub;                  // entry, and its row group (gate/up) or row block (down)
+        if (ph == 0) {
+          const GuUnit gu = gu_unit(c.rt, u, gps, gpe);
+          ent = gu.ent;
+          sub = gu.grp;
+        } else {
+          ent = u / rbn;
+          sub = u % rbn;
         }
-        float acc[4][kNt][4];
-        zero_acc(acc);
-        for (int s = 0; s < d / kKs; ++s) {
-          const uint32_t st = C.wait();
-          if (!st) { ok = false; break; }
-          mma_stage(st, brow, ntl, s * kKs, lane, acc);
-          C.release();
-        }
-        if (!ok) break;
-        asm volatile("" ::: "memory");   // keep the epilogue's loads after the loop (registers)
-        const float tsg = __ldg(sh ? W.tsg : W.tg + e), tsu = __ldg(sh ? W.tsu : W.tu + e);
-        // h / xs^2 = silu(a) (u / xs^2) for every held (row, column), then the stores
-#pragma unroll
-        for (int n = 0; n < kNt; ++n) {
-          if (n >= ntl) continue;
-#pragma unroll
-          for (int cix = 0; cix < 4; ++cix) {
-            const int col = n * 8 + tq * 2 + (cix & 1), cc = col < cnt ? col : 0;
-            const int tok = sh ? off - T * k + cc : c.rt.slot_tok[off + cc];
-            const float xs = __ldcg(a.xsc + tok);
-            const float ga = tsg * xs, ua = tsu / xs;
-#pragma unroll
-            for (int jt = 0; jt < 2; ++jt) {
-              const float av = acc[jt][n][cix] * ga;
-              acc[jt][n][cix] = silu_f(av) * (acc[jt + 2][n][cix] * ua);
-            }
-          }
-        }
-        bool sat = false;
-#pragma unroll
-        for (int n = 0; n < kNt; ++n) {
-          if (n >= ntl) continue;
-#pragma unroll
-          for (int cix = 0; cix < 4; ++cix) {
-            const int col = n * 8 + tq * 2 + (cix & 1);
-            if (col >= cnt) continue;
-            __half* hr = a.h + (size_t)(off + col) * Fmax + gu.grp * 32 + g + (cix >= 2 ? 8 : 0);
-#pragma unroll
-            for (int jt = 0; jt < 2; ++jt) {
-              float hv = acc[jt][n][cix];
-              if (fabsf(hv) > 65504.f) {
-                sat = true;
-                hv = copysignf(65504.f, hv);
-              }
-              hr[jt * 16] = __float2half_rn(hv);
-            }
-          }
-        }
-        if (sat) atomicOr(a.err, kErrRange);
-      }
-    }
-    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, kNT, 32)) return;
-
-    // ---- phase C: down units, gate-weighted outputs per slot
-    {
-      int lo, hi;
-      share(c.rt.n_ent[0] * rbn, c.G, c.b, lo, hi);
-      for (int u = lo + w; u < hi && ok; u += kC) {
-        const int ent = u / rbn, rb = u % rbn;
         const int e = c.rt.ent_e[ent], off = c.rt.ent_off[ent], cnt = c.rt.ent_cnt[ent];
         const bool sh = e < 0;
         const int ntl = (cnt + 7) >> 3;
@@ -729,11 +666,16 @@ __device__ __forceinline__ void run_consumers(Ctx& c) {
 #pragma unroll
         for (int n = 0; n < kNt; ++n) {
           const int col = n * 8 + g, cc = col < cnt ? col : 0;
-          brow[n] = reinterpret_cast<const uint8_t*>(a.h + (size_t)(off + cc) * Fmax);
+          if (ph == 0) {
+            const int tok = sh ? off - T * k + cc : c.rt.slot_tok[off + cc];
+            brow[n] = reinterpret_cast<const uint8_t*>(a.xh + (size_t)tok * d);
+          } else {
+            brow[n] = reinterpret_cast<const uint8_t*>(a.h + (size_t)(off + cc) * Fmax);
+          }
         }
         float acc[4][kNt][4];
         zero_acc(acc);
-        const int KS = (sh ? Fs : F) / kKs;
+        const int KS = ph == 0 ? d / kKs : (sh ? Fs : F) / kKs;
         for (int s = 0; s < KS; ++s) {
           const uint32_t st = C.wait();
           if (!st) { ok = false; break; }
@@ -741,26 +683,69 @@ __device__ __forceinline__ void run_consumers(Ctx& c) {
           C.release();
         }
         if (!ok) break;
-        asm volatile("" ::: "memory");
-        const float tsd = __ldg(sh ? W.tsd : W.td + e);
-#pragma unroll
-        for (int n = 0; n < kNt; ++n) {
-          if (n >= ntl) continue;
-#pragma unroll
-          for (int cix = 0; cix < 4; ++cix) {
-            const int col = n * 8 + tq * 2 + (cix & 1);
-            if (col >= cnt) continue;
-            const int tok = sh ? off - T * k + col : c.rt.slot_tok[off + col];
-            const float xs = __ldcg(a.xsc + tok);
-            const float sc = tsd * xs * xs * (sh ? 1.f : c.rt.slot_gate[off + col]);
-            float* orow = a.o + (size_t)(off + col) * d + rb * kRows + g + (cix >= 2 ? 8 : 0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) __stcg(orow + j * 16, acc[j][n][cix] * sc);
-          }
+        asm volatile("" ::: "memory");   // keep the epilogue's loads after the loop (registers)
+        if (ph == 0) {
+            const float tsg = __ldg(sh ? W.tsg : W.tg + e), tsu = __ldg(sh ? W.tsu : W.tu + e);
+            // h / xs^2 = silu(a) (u / xs^2) for every held (row, column), then the stores
+    #pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+              if (n >= ntl) continue;
+    #pragma unroll
+              for (int cix = 0; cix < 4; ++cix) {
+                const int col = n * 8 + tq * 2 + (cix & 1), cc = col < cnt ? col : 0;
+                const int tok = sh ? off - T * k + cc : c.rt.slot_tok[off + cc];
+                const float xs = __ldcg(a.xsc + tok);
+                const float ga = tsg * xs, ua = tsu / xs;
+    #pragma unroll
+                for (int jt = 0; jt < 2; ++jt) {
+                  const float av = acc[jt][n][cix] * ga;
+                  acc[jt][n][cix] = silu_f(av) * (acc[jt + 2][n][cix] * ua);
+                }
+              }
+            }
+            bool sat = false;
+    #pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+              if (n >= ntl) continue;
+    #pragma unroll
+              for (int cix = 0; cix < 4; ++cix) {
+                const int col = n * 8 + tq * 2 + (cix & 1);
+                if (col >= cnt) continue;
+                __half* hr = a.h + (size_t)(off + col) * Fmax + sub * 32 + g + (cix >= 2 ? 8 : 0);
+    #pragma unroll
+                for (int jt = 0; jt < 2; ++jt) {
+                  float hv = acc[jt][n][cix];
+                  if (fabsf(hv) > 65504.f) {
+                    sat = true;
+                    hv = copysignf(65504.f, hv);
+                  }
+                  hr[jt * 16] = __float2half_rn(hv);
+                }
+              }
+            }
+            if (sat) atomicOr(a.err, kErrRange);
+        } else {
+          const int rb = sub;
+            const float tsd = __ldg(sh ? W.tsd : W.td + e);
+    #pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+              if (n >= ntl) continue;
+    #pragma unroll
+              for (int cix = 0; cix < 4; ++cix) {
+                const int col = n * 8 + tq * 2 + (cix & 1);
+                if (col >= cnt) continue;
+                const int tok = sh ? off - T * k + col : c.rt.slot_tok[off + col];
+                const float xs = __ldcg(a.xsc + tok);
+                const float sc = tsd * xs * xs * (sh ? 1.f : c.rt.slot_gate[off + col]);
+                float* orow = a.o + (size_t)(off + col) * d + rb * kRows + g + (cix >= 2 ? 8 : 0);
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) __stcg(orow + j * 16, acc[j][n][cix] * sc);
+              }
+            }
         }
       }
+      if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, kNT, 32)) return;
     }
-    if (!grid_sync(a.bar, (++nbar) * c.G, c.wc, c.abort_flag, kNT, 32)) return;
 
     // ---- phase D: y = sum of the token's slots (selection order) + shared (+ x)
     {
