@@ -270,12 +270,13 @@ typedef struct moe_stack* moe_stack_handle;    /* opaque, owned by the library *
  * cfg: the shape shared by every layer; add_residual must be nonzero.
  * layers: n_layers (1..4096) weight sets as in moe_create, borrowed for the
  * handle's lifetime.  Creates one moe_create handle per layer (the per-layer
- * path) and, when the shapes allow it, sets up the persistent decode kernel:
- * bf16 weights and activations, at most 256 routed experts, d, F and F_s
- * multiples of 256, a device of compute capability 10.x that launches
- * cooperative grids.  That kernel runs every layer of the stack for T <= 8
- * tokens in one launch -- the counterpart of the decode megakernel the pages
- * describe (evermx.com review, Feature Overview, "Kernels and inference").
+ * path) and, when the shapes allow it, sets up a persistent decode kernel:
+ * bf16 activations with bf16 weights (T <= 8) or NVFP4 weights (T <= 32), at
+ * most 256 routed experts, d, F and F_s multiples of 256, a device of compute
+ * capability 10.x that launches cooperative grids.  That kernel runs every
+ * layer of the stack in one launch -- the counterpart of the decode
+ * megakernel the pages describe (evermx.com review, Feature Overview,
+ * "Kernels and inference").
  * Errors: those of moe_create; MOE_ERR_INVALID_ARG for a NULL argument,
  * n_layers out of range or add_residual == 0; MOE_ERR_OOM if the stack's own
  * workspace cannot be allocated.  On failure *out is NULL and nothing is held.
@@ -286,7 +287,8 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
 /* Free the stack, its layer handles and workspace (synchronises the device). NULL is a no-op. */
 moe_status moe_stack_destroy(moe_stack_handle h);
 
-/* 1 if moe_stack_forward with T tokens runs the persistent kernel, else 0 (per-layer path). */
+/* 1 if moe_stack_forward with T tokens runs the persistent kernel, else 0 (per-layer path).  An
+ * NVFP4 stack asked for x_trace runs the per-layer path (same kernels, one launch per layer). */
 int32_t moe_stack_uses_persistent(moe_stack_handle h, int32_t T);
 
 /*

@@ -380,8 +380,9 @@ class MoeStack:
     def persistent(self, T: int) -> bool:
         return bool(moe_stack_uses_persistent(self.h, T))
 
-    def forward(self, x, y=None, trace=False, stream=None):
-        """Returns y, or (y, x_trace [L+1][T][d], idx [L][T][k], gate [L][T][k]) with trace=True."""
+    def forward(self, x, y=None, trace=False, routing=False, stream=None):
+        """Returns y; (y, x_trace [L+1][T][d], idx [L][T][k], gate [L][T][k]) with trace=True;
+        (y, idx, gate) with routing=True (the routing only, no x_trace)."""
         torch = self.torch
         T = x.shape[0]
         if y is None:
@@ -389,12 +390,16 @@ class MoeStack:
         xt = it = gt = None
         if trace:
             xt = torch.empty((self.L + 1, T, self.d), dtype=x.dtype, device=x.device)
+        if trace or routing:
             it = torch.empty((self.L, T, self.k), dtype=torch.int32, device=x.device)
             gt = torch.empty((self.L, T, self.k), dtype=torch.float32, device=x.device)
-        st = moe_stack_forward(self.h, x.data_ptr(), T, y.data_ptr(), xt.data_ptr() if trace else 0,
-                               it.data_ptr() if trace else 0, gt.data_ptr() if trace else 0, self._stream(stream))
+        st = moe_stack_forward(self.h, x.data_ptr(), T, y.data_ptr(), xt.data_ptr() if xt is not None else 0,
+                               it.data_ptr() if it is not None else 0, gt.data_ptr() if gt is not None else 0,
+                               self._stream(stream))
         _ok(st, "moe_stack_forward")
-        return (y, xt, it, gt) if trace else y
+        if trace:
+            return y, xt, it, gt
+        return (y, it, gt) if routing else y
 
     def check(self, stream=None) -> int:
         return moe_stack_check(self.h, self._stream(stream))

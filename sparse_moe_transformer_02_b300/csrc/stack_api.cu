@@ -50,9 +50,19 @@ struct moe_stack {
   int device = 0;
   int num_sms = 0;
   std::vector<moe_handle> layers;    // one handle per layer (per-layer path)
-  bool persistent = false;           // the persistent kernel serves T <= kSdMaxT
+  bool persistent = false;           // the persistent bf16 kernel serves T <= kSdMaxT
+  bool persistent4 = false;          // the persistent NVFP4 kernel serves T <= kS4MaxT
   StackLayerPtrs* d_layers = nullptr;
   CUtensorMap* d_maps = nullptr;
+  Stack4LayerPtrs* d_layers4 = nullptr;
+  void* block4 = nullptr;            // NVFP4 kernel: maps, layer pointers, x f16 copy and scales, h, o, top-k
+  CUtensorMap* d_maps4 = nullptr;
+  __half* xh = nullptr;
+  float* xsc = nullptr;
+  __half* h4 = nullptr;
+  float* o4 = nullptr;
+  int32_t* topk_e = nullptr;
+  float* topk_g = nullptr;
   void* block = nullptr;             // xbuf, logits, h, barrier counter, error word, chain buffers
   __nv_bfloat16* xbuf = nullptr;
   float* logits = nullptr;
@@ -70,6 +80,7 @@ inline size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 void free_stack(moe_stack* s) {
   for (moe_handle h : s->layers) moe_destroy(h);
   if (s->block) cudaFree(s->block);
+  if (s->block4) cudaFree(s->block4);
   if (s->d_layers) cudaFree(s->d_layers);
   if (s->d_maps) cudaFree(s->d_maps);
   delete s;
@@ -110,7 +121,9 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
   s->wait_ns = (uint64_t)(c.wait_timeout_ms > 0 ? c.wait_timeout_ms : 2000) * 1000000ull;
   const int Fmax = c.ffn > c.shared_ffn ? c.ffn : c.shared_ffn;
   const size_t es = c.act_dtype == MOE_F32 ? 4 : 2;
-  const size_t nx = (size_t)kSdMaxT * c.d * 2, nlog = (size_t)4 * kSdMaxT * c.num_experts * 4;
+  // residual stream between layers and partial logits, sized for both persistent kernels
+  const size_t nx = (size_t)kS4MaxT * c.d * 2;
+  const size_t nlog = (size_t)((c.d + 511) / 512 > 4 ? (c.d + 511) / 512 : 4) * kS4MaxT * c.num_experts * 4;
   const size_t nh = (size_t)kSdMaxT * (c.top_k + 1) * Fmax * 2, nchain = (size_t)c.max_tokens * c.d * es;
   const size_t total = up256(2 * nx) + up256(nlog) + up256(nh) + 256 + 256 + 2 * up256(nchain);
   if (dev_malloc(&s->block, total) != cudaSuccess) {
@@ -163,6 +176,55 @@ moe_status moe_stack_create(const moe_config* cfg, const moe_weights* layers, in
       }
     }
   }
+  if (!s->persistent) {
+    bool q4 = true;
+    s->persistent4 = stack_decode_fp4_supported(c, &q4);
+    if (!q4) {
+      free_stack(s);
+      return MOE_ERR_CUDA;
+    }
+  }
+  if (s->persistent4) {
+    std::vector<Stack4LayerPtrs> hp(n_layers);
+    std::vector<CUtensorMap> maps((size_t)n_layers * kS4Maps);
+    bool ok = true;
+    for (int l = 0; l < n_layers && ok; ++l) {
+      const moe_weights& w = layers[l];
+      hp[l] = Stack4LayerPtrs{w.router_w, w.router_b, w.t_gate, w.t_up, w.t_down, w.ts_gate, w.ts_up, w.ts_down};
+      ok = stack_layer_views_fp4(c, w, &maps[(size_t)l * kS4Maps]);
+    }
+    if (!ok) {
+      s->persistent4 = false;                // the per-layer path serves every T
+    } else {
+      const size_t slots = (size_t)kS4MaxT * (c.top_k + 1);
+      const size_t nmaps = up256(sizeof(CUtensorMap) * maps.size()), nlp = up256(sizeof(Stack4LayerPtrs) * n_layers);
+      const size_t nxh = up256((size_t)kS4MaxT * c.d * 2), nxs = up256((size_t)kS4MaxT * 4);
+      const size_t nh4 = up256(slots * Fmax * 2), no4 = up256(slots * c.d * 4), ntk = up256((size_t)kS4MaxT * kMaxTopK * 4);
+      if (dev_malloc(&s->block4, nmaps + nlp + nxh + nxs + nh4 + no4 + 2 * ntk) != cudaSuccess) {
+        cudaGetLastError();
+        s->block4 = nullptr;
+        free_stack(s);
+        return MOE_ERR_OOM;
+      }
+      uint8_t* q = static_cast<uint8_t*>(s->block4);
+      s->d_maps4 = reinterpret_cast<CUtensorMap*>(q); q += nmaps;
+      s->d_layers4 = reinterpret_cast<Stack4LayerPtrs*>(q); q += nlp;
+      s->xh = reinterpret_cast<__half*>(q); q += nxh;
+      s->xsc = reinterpret_cast<float*>(q); q += nxs;
+      s->h4 = reinterpret_cast<__half*>(q); q += nh4;
+      s->o4 = reinterpret_cast<float*>(q); q += no4;
+      s->topk_e = reinterpret_cast<int32_t*>(q); q += ntk;
+      s->topk_g = reinterpret_cast<float*>(q);
+      if (cudaMemcpy(s->d_maps4, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) !=
+              cudaSuccess ||
+          cudaMemcpy(s->d_layers4, hp.data(), sizeof(Stack4LayerPtrs) * n_layers, cudaMemcpyHostToDevice) !=
+              cudaSuccess) {
+        cudaGetLastError();
+        free_stack(s);
+        return MOE_ERR_CUDA;
+      }
+    }
+  }
   if (cudaMemsetAsync(s->err, 0, 256, stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();
     free_stack(s);
@@ -180,7 +242,8 @@ moe_status moe_stack_destroy(moe_stack_handle h) {
 }
 
 int32_t moe_stack_uses_persistent(moe_stack_handle h, int32_t T) {
-  return (h && h->persistent && T >= 1 && T <= kSdMaxT && T <= h->cfg.max_tokens) ? 1 : 0;
+  if (!h || T < 1 || T > h->cfg.max_tokens) return 0;
+  return ((h->persistent && T <= kSdMaxT) || (h->persistent4 && T <= kS4MaxT)) ? 1 : 0;
 }
 
 moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void* y, void* x_trace, int32_t* idx_trace,
@@ -200,7 +263,40 @@ moe_status moe_stack_forward(moe_stack_handle h, const void* x, int32_t T, void*
     const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(y);
     if (a < b + nb && b < a + nb) return MOE_ERR_INVALID_ARG;
   }
-  if (moe_stack_uses_persistent(h, T)) {
+  if (h->persistent4 && !x_trace && moe_stack_uses_persistent(h, T)) {
+    if (cudaMemsetAsync(h->bar, 0, 4, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    Stack4Args a;
+    a.layers = h->d_layers4;
+    a.maps = h->d_maps4;
+    a.L = h->L;
+    a.x_in = static_cast<const __nv_bfloat16*>(x);
+    a.y_out = static_cast<__nv_bfloat16*>(y);
+    a.xbuf = h->xbuf;
+    a.logits = h->logits;
+    a.xh = h->xh;
+    a.xsc = h->xsc;
+    a.h = h->h4;
+    a.o = h->o4;
+    a.topk_e = h->topk_e;
+    a.topk_g = h->topk_g;
+    a.idx_trace = idx_trace;
+    a.gate_trace = gate_trace;
+    a.g_offsets = a.g_tok_of_slot = a.g_slot_of = nullptr;
+    a.bar = h->bar;
+    a.err = h->err;
+    a.T = T; a.d = c.d; a.F = c.ffn; a.Fs = c.shared_ffn; a.E = c.num_experts; a.k = c.top_k;
+    a.add_residual = 1;
+    a.wait_ns = h->wait_ns;
+    if (launch_stack_decode_fp4(a, h->num_sms, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  if (h->persistent && moe_stack_uses_persistent(h, T)) {
     if (cudaMemsetAsync(h->bar, 0, 4, stream) != cudaSuccess) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
