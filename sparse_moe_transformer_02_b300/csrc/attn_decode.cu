@@ -247,23 +247,22 @@ __device__ __forceinline__ bool consume_group(AtCtx& c, int& m, int KC, uint32_t
   return true;
 }
 
-// Copy rows global -> shared memory with eight 16-byte loads in flight per thread.
+// Copy `rows` rows of `chunks` 16-byte pieces from global (src_pitch bytes)
+// to shared memory (dst_pitch bytes) with asynchronous 16-byte copies
+// (cp.async, L2 to shared memory, no registers held): every piece of the
+// thread is in flight before it waits.  The caller synchronises the threads.
 __device__ __forceinline__ void stage_rows(uint8_t* dst, uint32_t dst_pitch, const uint8_t* src, size_t src_pitch,
                                            int rows, int chunks, int tid, int nt) {
   const int n = rows * chunks;
-  for (int i0 = tid; i0 < n; i0 += 8 * nt) {
-    uint4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * nt;
-      if (i < n) v[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(i / chunks) * src_pitch) + i % chunks);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * nt;
-      if (i < n) *reinterpret_cast<uint4*>(dst + (i / chunks) * dst_pitch + (i % chunks) * 16) = v[u];
-    }
+  const uint32_t d0 = smem_u32(dst);
+  for (int i = tid; i < n; i += nt) {
+    const uint8_t* g = src + (size_t)(i / chunks) * src_pitch + (size_t)(i % chunks) * 16;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d0 + (uint32_t)(i / chunks) * dst_pitch +
+                                                                    (uint32_t)(i % chunks) * 16),
+                 "l"(g)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ bool grid_sync(AtCtx& c, unsigned target) {

@@ -458,13 +458,10 @@ __device__ __forceinline__ void run_consumers(SdCtx& c) {
             }
           }
         }
-#pragma unroll
-        for (int t = 0; t < kSdMaxT; ++t) {
-          float v = acc[t];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-          if (t < T && lane == 0) __stcg(a.logits + ((size_t)q * kSdMaxT + t) * E + e, v + bias);
-        }
+        // butterfly transpose-reduction: lanes 4 t .. 4 t + 3 end with token t's sum
+        const float v = transpose_reduce<kSdMaxT, 32>(acc, lane);
+        const int t = lane >> 2;
+        if ((lane & 3) == 0 && t < T) __stcg(a.logits + ((size_t)q * kSdMaxT + t) * E + e, v + bias);
       }
     }
     // phase A: shared expert row groups (all T tokens)
