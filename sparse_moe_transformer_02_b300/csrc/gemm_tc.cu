@@ -52,6 +52,8 @@ constexpr int kBulkRedT = 8192;  // batches from which 16-byte red operations bo
 
 template <int MODE> struct TcStaging { static constexpr int BYTES = 0; };
 template <> struct TcStaging<3> { static constexpr int BYTES = 2 * 128 * kRedCols * 4; };   // two row buffers
+constexpr int kTpPitch = 36;     // token-major red epilogue: floats per row of a warp's 32 x 32 transpose tile
+template <> struct TcStaging<2> { static constexpr int BYTES = 4 * 32 * kTpPitch * 4; };    // one tile per warp
 
 template <> struct TcCfg<0> {     // gate/up: A_g + A_u + B per stage
   static constexpr int STAGES = 4;
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = dsm;
-  float* red_stage = reinterpret_cast<float*>(dsm + S * C::STAGE_BYTES);   // [2][128][kRedCols] (MODE 3)
+  float* red_stage = reinterpret_cast<float*>(dsm + S * C::STAGE_BYTES);   // MODE 3: [2][128][kRedCols]; MODE 2: [4][32][kTpPitch]
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + S * C::STAGE_BYTES + TcStaging<MODE>::BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -491,17 +493,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
         float* yrow = p.yacc + (size_t)t * p.d + un.m_tile * (2 * kTcBN);
         if constexpr (MODE == 2) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < 2 * kTcBN; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(acc + c0, v);
-            tmem_ld_wait();
-            if (r < un.n) {
+          // 16-byte red operations, each warp instruction on 4 rows x 128
+          // contiguous bytes: every 32 x 32 chunk of the warp's rows goes
+          // through its own shared-memory tile, after which lane l adds
+          // columns 4 (l % 8) .. + 3 of rows 4 j + l / 8 (one red instruction
+          // on one row each would touch 32 rows x 16 bytes).
+          (void)yrow;
+          float* tile = red_stage + (size_t)q * 32 * kTpPitch;
+          const int tcol = (lane & 7) * 4;
+          int tok[8];
+          unsigned valid = 0;
 #pragma unroll
-              for (int i = 0; i < 16; i += 4)
-                red_add_v4_f32(yrow + c0 + i, g * __uint_as_float(v[i]), g * __uint_as_float(v[i + 1]),
-                               g * __uint_as_float(v[i + 2]), g * __uint_as_float(v[i + 3]));
+          for (int j = 0; j < 8; ++j) {
+            const int rr = 4 * j + (lane >> 3);
+            tok[j] = __shfl_sync(0xFFFFFFFFu, t, rr);
+            if (q * 32 + rr < un.n) valid |= 1u << j;
+          }
+          float* ybase = p.yacc + (size_t)un.m_tile * (2 * kTcBN) + tcol;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 2 * kTcBN; c0 += 32) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16(acc + c0, v0);
+            tmem_ld16(acc + c0 + 16, v1);
+            tmem_ld_wait();
+            float4* trow = reinterpret_cast<float4*>(tile + lane * kTpPitch);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              trow[i] = make_float4(g * __uint_as_float(v0[4 * i]), g * __uint_as_float(v0[4 * i + 1]),
+                                    g * __uint_as_float(v0[4 * i + 2]), g * __uint_as_float(v0[4 * i + 3]));
+              trow[4 + i] = make_float4(g * __uint_as_float(v1[4 * i]), g * __uint_as_float(v1[4 * i + 1]),
+                                        g * __uint_as_float(v1[4 * i + 2]), g * __uint_as_float(v1[4 * i + 3]));
             }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (valid & (1u << j)) {
+                const float4 x = *reinterpret_cast<const float4*>(tile + (4 * j + (lane >> 3)) * kTpPitch + tcol);
+                red_add_v4_f32(ybase + (size_t)tok[j] * p.d + c0, x.x, x.y, x.z, x.w);
+              }
+            }
+            __syncwarp();
           }
         } else {
           // Accumulate into y_acc with bulk reductions (one 256-byte row segment
