@@ -19,11 +19,13 @@
 //    red.global.add (order of the adds is not fixed: the fp32 sum is
 //    deterministic up to rounding order).
 //  * pass 2 for large batches (token-major): A = h of 128 slots, B = 256 rows
-//    of Wd, D[slot][row]; each epilogue thread owns one slot, so it looks up
-//    one (token, gate) pair per tile and adds 16 consecutive outputs with four
-//    red.global.add.v4.f32; from 8192 tokens on, where the rate of those
-//    operations bounds the pass, it stages 64 gated outputs in shared memory
-//    and adds them with one bulk reduction (cp.reduce.async.bulk) instead.
+//    of Wd, D[slot][row]; each epilogue thread owns one slot (one (token,
+//    gate) lookup per tile) and the warp passes each 32 x 32 chunk of its
+//    gated outputs through a shared-memory tile, so that every
+//    red.global.add.v4.f32 instruction adds 4 token rows x 128 contiguous
+//    bytes (one instruction per row would touch 32 rows x 16 bytes; the
+//    transposed form also beat bulk reductions from shared memory
+//    (cp.reduce.async.bulk) at 16384 tokens: 404 against 491 us).
 //  * finalise: y = bf16(y_acc (+ x)).
 //
 // One persistent CTA per SM, 6 warps: warp 0 issues TMA into a ring of
@@ -47,11 +49,8 @@ constexpr int kThreadsTc = 192;
 constexpr int kRing = 8;
 
 template <int MODE> struct TcCfg;
-constexpr int kRedCols = 64;     // token-major down pass: columns per bulk reduction (256 bytes)
-constexpr int kBulkRedT = 8192;  // batches from which 16-byte red operations bound the token-major pass
 
 template <int MODE> struct TcStaging { static constexpr int BYTES = 0; };
-template <> struct TcStaging<3> { static constexpr int BYTES = 2 * 128 * kRedCols * 4; };   // two row buffers
 constexpr int kTpPitch = 36;     // token-major red epilogue: floats per row of a warp's 32 x 32 transpose tile
 template <> struct TcStaging<2> { static constexpr int BYTES = 4 * 32 * kTpPitch * 4; };    // one tile per warp
 
@@ -72,9 +71,6 @@ template <> struct TcCfg<2> {     // down, token-major: A (h of 128 slots) + B (
   static constexpr int STAGE_BYTES = kTcBM * 128 + 2 * kTcBN * 128;
   static constexpr int ACC_COLS = 2 * kTcBN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
-};
-template <> struct TcCfg<3> : TcCfg<2> {   // the same with a bulk-reduction epilogue (largest batches)
-  static constexpr int STAGES = 3;
 };
 
 struct TcParams {
@@ -147,7 +143,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = dsm;
-  float* red_stage = reinterpret_cast<float*>(dsm + S * C::STAGE_BYTES);   // MODE 3: [2][128][kRedCols]; MODE 2: [4][32][kTpPitch]
+  float* red_stage = reinterpret_cast<float*>(dsm + S * C::STAGE_BYTES);   // MODE 2: [4][32][kTpPitch]
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + S * C::STAGE_BYTES + TcStaging<MODE>::BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -424,7 +420,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
     }
     uint32_t tph[2] = {0, 0};
     int buf = 0;
-    int red_buf = 0;
     int n_total = p.n_pre;
     bool waited = MODE >= 1;
     if (MODE >= 1) n_total = __ldcg(p.n_units + LIST);
@@ -492,7 +487,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::ACC_COLS + ((uint32_t)(q * 32) << 16);
         float* yrow = p.yacc + (size_t)t * p.d + un.m_tile * (2 * kTcBN);
-        if constexpr (MODE == 2) {
+        {
           // 16-byte red operations, each warp instruction on 4 rows x 128
           // contiguous bytes: every 32 x 32 chunk of the warp's rows goes
           // through its own shared-memory tile, after which lane l adds
@@ -533,39 +528,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
               }
             }
             __syncwarp();
-          }
-        } else {
-          // Accumulate into y_acc with bulk reductions (one 256-byte row segment
-          // per operation, added at L2 by the copy engine) rather than 16-byte
-          // red operations, whose rate bounds this pass at prefill sizes.  Each
-          // thread stages its own row in one of two buffers, storing its 16-byte
-          // pieces in a rotated order so that a quarter-warp hits distinct banks.
-#pragma unroll 1
-          for (int c0 = 0; c0 < 2 * kTcBN; c0 += kRedCols) {
-            float* rs = red_stage + (size_t)(red_buf * 128 + r) * kRedCols;
-            if (r < un.n) bulk_wait_read<1>();        // this buffer's previous reduction has read it
-#pragma unroll
-            for (int h = 0; h < kRedCols; h += 16) {
-              uint32_t v[16];
-              tmem_ld16(acc + c0 + h, v);
-              tmem_ld_wait();
-              if (r < un.n) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int pc = (h / 4 + ((i + r) & 3));      // 16-byte piece, rotated within the 64-byte group
-                  const int j = (pc - h / 4) * 4;
-                  reinterpret_cast<float4*>(rs)[pc] =
-                      make_float4(g * __uint_as_float(v[j]), g * __uint_as_float(v[j + 1]),
-                                  g * __uint_as_float(v[j + 2]), g * __uint_as_float(v[j + 3]));
-                }
-              }
-            }
-            if (r < un.n) {
-              fence_proxy_async_smem();
-              bulk_red_add_f32(yrow + c0, smem_u32(rs), kRedCols * 4);
-              bulk_commit();
-            }
-            red_buf ^= 1;
           }
         }
         tc_fence_before();
@@ -692,7 +654,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
         atomicAdd(p.ready + p.E + 2, 1u);
       }
     }
-    if (MODE == 3) bulk_wait_all();          // every reduction performed before the CTA ends
   }
   tc_fence_before();
   __syncthreads();
@@ -835,7 +796,6 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
     cudaError_t e = ensure_smem_limit(tc_kernel<0>, (int)tc_smem_bytes<0>());
     if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<1>, (int)tc_smem_bytes<1>());
     if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<2>, (int)tc_smem_bytes<2>());
-    if (e == cudaSuccess) e = ensure_smem_limit(tc_kernel<3>, (int)tc_smem_bytes<3>());
     if (e != cudaSuccess) return e;
   }
   const int Fmax = a.F > a.Fs ? a.F : a.Fs;
@@ -906,8 +866,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   const int grid2 = num_sms < a.max_units_dn ? num_sms : (a.max_units_dn > 0 ? a.max_units_dn : 1);
   if (prof) prof->begin(MOE_K_TC_DOWN, s);
   if (tok_major)
-    e = a.T >= kBulkRedT ? launch_ex(tc_kernel<3>, grid2, kThreadsTc, tc_smem_bytes<3>(), s, p)
-                         : launch_ex(tc_kernel<2>, grid2, kThreadsTc, tc_smem_bytes<2>(), s, p);
+    e = launch_ex(tc_kernel<2>, grid2, kThreadsTc, tc_smem_bytes<2>(), s, p);
   else
     e = launch_ex(tc_kernel<1>, grid2, kThreadsTc, tc_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);

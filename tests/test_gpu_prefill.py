@@ -151,9 +151,9 @@ def test_token_major_no_shared_and_narrow_d(spec):
     check_layer(L, x, y, idx, gate, spec.top_k, "bf16")
 
 
-def test_token_major_bulk_reduction(small):
-    """From 8192 tokens on the token-major down pass adds its results with bulk
-    reductions from shared memory; every token against the oracle."""
+def test_token_major_large_batch(small):
+    """A large token-major batch (64 slot tiles per expert; the transposed red
+    epilogue on every tile); every token against the oracle."""
     L, dev = small
     T = 8192
     x = I.make_tokens(SMALL, seed=8192, T=T)
