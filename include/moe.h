@@ -84,6 +84,12 @@ typedef struct {
   int32_t path;          /* moe_path */
   int32_t gemv_max_tokens; /* MOE_PATH_AUTO: T <= this uses the GEMV kernels even when tcgen05 could; 0 = never */
   int32_t wait_timeout_ms; /* limit of every device-side spin wait; 0 = default (2000 ms) */
+  int32_t deterministic;   /* 1: the tcgen05 paths combine each token's expert outputs in a fixed order
+                              (gate-weighted per-slot rows, summed in selection order, then the shared
+                              expert and x), so repeated calls agree bit for bit; 0 (default): they add
+                              into an fp32 accumulator with atomics, in arrival order (equal up to fp32
+                              rounding order).  The persistent and GEMV paths are fixed-order either way.
+                              Costs a [max_tokens (k + 1)][d] fp32 buffer and its traffic. */
 } moe_config;
 
 /*

@@ -31,7 +31,7 @@ KERNEL_NAMES = ["route", "gemv_gateup", "gemv_down", "tc_gather", "tc_gateup", "
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d", "ffn", "shared_ffn", "num_experts", "top_k", "max_tokens", "act_dtype", "weight_dtype",
-        "add_residual", "path", "gemv_max_tokens", "wait_timeout_ms")]
+        "add_residual", "path", "gemv_max_tokens", "wait_timeout_ms", "deterministic")]
 
 
 class moe_attn_config(ctypes.Structure):
@@ -278,13 +278,14 @@ class MoeLayer:
 
     def __init__(self, *, d, ffn, shared_ffn, num_experts, top_k, max_tokens, act, weight,
                  weights: dict, add_residual=False, path=MOE_PATH_AUTO, gemv_max_tokens=0,
-                 wait_timeout_ms=0, stream=None):
+                 wait_timeout_ms=0, deterministic=False, stream=None):
         import torch
         self.torch = torch
         self.cfg = moe_config(d=d, ffn=ffn, shared_ffn=shared_ffn, num_experts=num_experts, top_k=top_k,
                               max_tokens=max_tokens, act_dtype=_DT[act], weight_dtype=_DT[weight],
                               add_residual=int(bool(add_residual)), path=path,
-                              gemv_max_tokens=gemv_max_tokens, wait_timeout_ms=wait_timeout_ms)
+                              gemv_max_tokens=gemv_max_tokens, wait_timeout_ms=wait_timeout_ms,
+                              deterministic=int(bool(deterministic)))
         self.tensors = dict(weights)            # keeps the borrowed memory alive
         w = moe_weights()
         for name, _ in moe_weights._fields_:

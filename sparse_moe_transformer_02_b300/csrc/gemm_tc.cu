@@ -89,6 +89,7 @@ struct TcParams {
   const int32_t* n_units;
   __nv_bfloat16* h16;
   float* yacc;
+  float* oslot;               // deterministic mode: per-slot rows [T (k + 1)][d] instead of y_acc, or null
   unsigned int* err;
   uint64_t wait_ns;
   // Gate/up progress, read by the down pass (see below): ready[e] counts the
@@ -496,15 +497,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           (void)yrow;
           float* tile = red_stage + (size_t)q * 32 * kTpPitch;
           const int tcol = (lane & 7) * 4;
+          // accumulate mode: rows of y_acc (tokens); deterministic mode: this
+          // tile's rows of the per-slot buffer, each stored once
+          const int orow = p.oslot ? (sh ? p.T * p.k : 0) + un.slot0 + r : t;
           int tok[8];
           unsigned valid = 0;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int rr = 4 * j + (lane >> 3);
-            tok[j] = __shfl_sync(0xFFFFFFFFu, t, rr);
+            tok[j] = __shfl_sync(0xFFFFFFFFu, orow, rr);
             if (q * 32 + rr < un.n) valid |= 1u << j;
           }
-          float* ybase = p.yacc + (size_t)un.m_tile * (2 * kTcBN) + tcol;
+          float* ybase = (p.oslot ? p.oslot : p.yacc) + (size_t)un.m_tile * (2 * kTcBN) + tcol;
 #pragma unroll 1
           for (int c0 = 0; c0 < 2 * kTcBN; c0 += 32) {
             uint32_t v0[16], v1[16];
@@ -524,7 +528,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
             for (int j = 0; j < 8; ++j) {
               if (valid & (1u << j)) {
                 const float4 x = *reinterpret_cast<const float4*>(tile + (4 * j + (lane >> 3)) * kTpPitch + tcol);
-                red_add_v4_f32(ybase + (size_t)tok[j] * p.d + c0, x.x, x.y, x.z, x.w);
+                float* dst = ybase + (size_t)tok[j] * p.d + c0;
+                if (p.oslot)
+                  __stcg(reinterpret_cast<float4*>(dst), x);
+                else
+                  red_add_v4_f32(dst, x.x, x.y, x.z, x.w);
               }
             }
             __syncwarp();
@@ -626,10 +634,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_kernel(const __grid_constant
           tmem_ld_wait();
           const int* ct = col_tok + q * kTcBN;
           const float* cg = col_gate + q * kTcBN;
+          if (p.oslot) {                       // fixed order: each (slot, row) stored once
+            const int s0 = sh ? p.T * p.k + un.slot0 : un.slot0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < un.n) red_add_f32(p.yacc + (size_t)ct[col] * p.d + row, cg[col] * __uint_as_float(v[i]));
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + i;
+              if (col < un.n) __stcg(p.oslot + (size_t)(s0 + col) * p.d + row, cg[col] * __uint_as_float(v[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + i;
+              if (col < un.n) red_add_f32(p.yacc + (size_t)ct[col] * p.d + row, cg[col] * __uint_as_float(v[i]));
+            }
           }
         }
       }
@@ -741,6 +758,50 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const float* __restric
   }
 }
 
+// Deterministic mode: y[t] = bf16(sum over j < k of oslot[slot_of[t k + j]] (selection
+// order) + oslot[T k + t] (the shared expert) (+ x[t])), 8 values per thread.
+__global__ void __launch_bounds__(256) tc_finalize_det_kernel(const float* __restrict__ oslot,
+                                                              const int32_t* __restrict__ slot_of,
+                                                              const __nv_bfloat16* __restrict__ x,
+                                                              __nv_bfloat16* __restrict__ y, int T, int d, int k,
+                                                              int has_shared, int residual, unsigned int* ready,
+                                                              int n_ready) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
+  const int per = d / 8;
+  const size_t n8 = (size_t)T * per;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per), c = (int)(i % per) * 8;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    auto add_row = [&](size_t r) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(oslot + r * d + c));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(oslot + r * d + c) + 1);
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    };
+    for (int j = 0; j < k; ++j) add_row((size_t)__ldcg(slot_of + (size_t)t * k + j));
+    if (has_shared) add_row((size_t)T * k + t);
+    if (residual) {
+      const uint4 xr = __ldg(reinterpret_cast<const uint4*>(x) + i);
+      const uint32_t xs[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] += __uint_as_float(xs[j] << 16);
+        v[2 * j + 1] += __uint_as_float(xs[j] & 0xFFFF0000u);
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      op[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(y)[i] = o;
+  }
+}
+
 template <int MODE>
 size_t tc_smem_bytes() {
   using C = TcCfg<MODE>;
@@ -779,14 +840,19 @@ int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n) {
   return (int)(routed + shared);
 }
 
-cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, unsigned int* ready,
-                               int n_ready, int num_sms, cudaStream_t s, Prof* prof) {
-  const size_t n8 = n / 8;
+cudaError_t launch_tc_finalize(const Workspace& ws, const void* x, void* y, int T, int d, int k, bool has_shared,
+                               bool residual, unsigned int* ready, int n_ready, int num_sms, cudaStream_t s,
+                               Prof* prof) {
+  const size_t n8 = (size_t)T * d / 8;
   const int grid = (int)((n8 + 255) / 256 < (size_t)num_sms * 4 ? (n8 + 255) / 256 : (size_t)num_sms * 4);
   if (prof) prof->begin(MOE_K_TC_FINALIZE, s);
-  const cudaError_t e = launch_ex(tc_finalize_kernel, grid > 0 ? grid : 1, 256, 0, s, yacc,
-                                  static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), n8,
-                                  (int)residual, ready, n_ready);
+  const cudaError_t e =
+      ws.oslot ? launch_ex(tc_finalize_det_kernel, grid > 0 ? grid : 1, 256, 0, s, (const float*)ws.oslot,
+                           (const int32_t*)ws.slot_of, static_cast<const __nv_bfloat16*>(x),
+                           static_cast<__nv_bfloat16*>(y), T, d, k, (int)has_shared, (int)residual, ready, n_ready)
+               : launch_ex(tc_finalize_kernel, grid > 0 ? grid : 1, 256, 0, s, (const float*)ws.yacc,
+                           static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), n8,
+                           (int)residual, ready, n_ready);
   if (prof) prof->end(s);
   return e;
 }
@@ -806,6 +872,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   p.gate = a.gate;
   p.h16 = a.ws.h16;
   p.yacc = a.ws.yacc;
+  p.oslot = a.ws.oslot;
   p.err = a.ws.err;
   p.wait_ns = a.wait_ns;
   p.n_units = a.ws.n_units;
@@ -872,7 +939,7 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof) 
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
   // finalise
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 4,
+  return launch_tc_finalize(a.ws, a.x, a.y, a.T, a.d, a.k, a.Fs > 0, a.add_residual != 0, a.ws.ready, a.E + 4,
                             num_sms, s, prof);
 }
 

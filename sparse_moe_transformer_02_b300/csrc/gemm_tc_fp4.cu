@@ -100,6 +100,7 @@ struct Tc4Params {
   const int32_t* n_units;
   __half* h16;
   float* yacc;
+  float* oslot;               // deterministic mode: per-slot rows [T (k + 1)][d] instead of y_acc, or null
   unsigned int* err;
   uint64_t wait_ns;
 };
@@ -404,10 +405,19 @@ __global__ void __launch_bounds__(kThreads4, 1) tc4_kernel(const __grid_constant
           uint32_t v[16];
           tmem_ld16(acc + c0, v);
           tmem_ld_wait();
+          if (p.oslot) {                       // fixed order: each (slot, row) stored once
+            const int s0 = sh ? p.T * p.k + un.slot0 : un.slot0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < un.n) red_add_f32(p.yacc + (size_t)ct[col] * p.d + row, cf[col] * __uint_as_float(v[i]));
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + i;
+              if (col < un.n) __stcg(p.oslot + (size_t)(s0 + col) * p.d + row, cf[col] * __uint_as_float(v[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + i;
+              if (col < un.n) red_add_f32(p.yacc + (size_t)ct[col] * p.d + row, cf[col] * __uint_as_float(v[i]));
+            }
           }
         }
       }
@@ -542,6 +552,7 @@ cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof
   p.n_units = a.ws.n_units;
   p.h16 = reinterpret_cast<__half*>(a.ws.h16);
   p.yacc = a.ws.yacc;
+  p.oslot = a.ws.oslot;
   p.err = a.ws.err;
   p.wait_ns = a.wait_ns;
   const bool has_sh = a.Fs > 0;
@@ -587,7 +598,7 @@ cudaError_t launch_tc4(const Tc4Args& a, int num_sms, cudaStream_t s, Prof* prof
   e = launch_pdl(tc4_kernel<1>, grid2, kThreads4, tc4_smem_bytes<1>(), s, p);
   if (prof) prof->end(s);
   if (e != cudaSuccess) return e;
-  return launch_tc_finalize(a.ws.yacc, a.x, a.y, (size_t)a.T * a.d, a.add_residual != 0, a.ws.ready, a.E + 3,
+  return launch_tc_finalize(a.ws, a.x, a.y, a.T, a.d, a.k, a.Fs > 0, a.add_residual != 0, a.ws.ready, a.E + 3,
                             num_sms, s, prof);
 }
 

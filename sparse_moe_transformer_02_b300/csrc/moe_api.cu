@@ -124,7 +124,8 @@ moe_status validate_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->d <= 0 || c->ffn <= 0 || c->shared_ffn < 0 || c->max_tokens <= 0) return MOE_ERR_INVALID_ARG;
   if (c->num_experts < 1 || c->top_k < 1 || c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
-  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC || c->gemv_max_tokens < 0 || c->wait_timeout_ms < 0)
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_TC || c->gemv_max_tokens < 0 || c->wait_timeout_ms < 0 ||
+      c->deterministic < 0 || c->deterministic > 1)
     return MOE_ERR_INVALID_ARG;
   if (c->d % 64 || c->ffn % 64 || c->shared_ffn % 64) return MOE_ERR_UNSUPPORTED;
   if (c->d > kMaxHidden) return MOE_ERR_UNSUPPORTED;
@@ -658,6 +659,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
       {(void**)&ws.xh16, c.weight_dtype == MOE_NVFP4 ? Tg * d * 2 : 16},
       {(void**)&ws.xsc, c.weight_dtype == MOE_NVFP4 ? Tg * 4 : 16},
       {(void**)&ws.yacc, h->tc_capable ? Tm * d * 4 : 16},
+      {(void**)&ws.oslot, h->tc_capable && c.deterministic ? Tm * (k + 1) * d * 4 : 16},
       {(void**)&ws.counters, (size_t)(64 + (Tm + 127) / 128) * 4},
       {(void**)&ws.wr_split, h->rtc_capable ? 3 * E * d * 2 : 16},
       {(void**)&ws.cand, h->rtc_capable ? Tm * (E / 64) * kMaxTopK * 8 : 16},
@@ -682,6 +684,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, cudaStream_t 
     *p.dst = static_cast<uint8_t*>(h->block) + off;
     off += up256(p.bytes);
   }
+  if (!(h->tc_capable && c.deterministic)) ws.oslot = nullptr;   // accumulate mode
   // Counters and the error word start at zero; the rest is written before it is read.
   h->n_counters = (int)(64 + (Tm + 127) / 128);
   cudaError_t e = cudaMemsetAsync(ws.counters, 0, (size_t)h->n_counters * 4, stream);

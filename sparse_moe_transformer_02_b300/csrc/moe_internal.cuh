@@ -60,6 +60,7 @@ struct Workspace {
   __half* xh16;           // [min(max_T, kGemvChunkT)][d] NVFP4 GEMV: f16 activations, scaled per token
   float* xsc;             // [min(max_T, kGemvChunkT)] their power-of-two scales
   float* yacc;            // [max_T][d] tcgen05 fp32 accumulator
+  float* oslot;           // [max_T (k + 1)][d] gate-weighted down outputs per slot (deterministic mode), or null
   uint32_t* counters;     // router tickets: [0] grid, [1 + b] per token chunk / block
   __nv_bfloat16* wr_split;  // [3][E][d] router weights as bf16 hi, mid, lo (tensor-core router)
   uint64_t* cand;         // [max_T][E / 64][kMaxTopK] tensor-core router: per-slice selection keys
@@ -213,9 +214,12 @@ cudaError_t launch_tc(const TcArgs& a, int num_sms, cudaStream_t s, Prof* prof);
 // Most unit-list entries a call can produce (token tiles of tile_n).
 int tc_max_units_gu(int T, int d, int F, int Fs, int E, int k, int tile_n);
 int tc_max_units_dn(int T, int d, int F, int Fs, int E, int k, int tile_n);
-// y = bf16(y_acc (+ x)) over T x d values; clears ready[0 .. n_ready).
-cudaError_t launch_tc_finalize(const float* yacc, const void* x, void* y, size_t n, bool residual, unsigned int* ready,
-                               int n_ready, int num_sms, cudaStream_t s, Prof* prof);
+// y = bf16(y_acc (+ x)) over T x d values, or with ws.oslot set the fixed-order
+// sum of each token's per-slot rows (selection order, then the shared expert's
+// row) (+ x); clears ready[0 .. n_ready).
+cudaError_t launch_tc_finalize(const Workspace& ws, const void* x, void* y, int T, int d, int k, bool has_shared,
+                               bool residual, unsigned int* ready, int n_ready, int num_sms, cudaStream_t s,
+                               Prof* prof);
 
 // NVFP4 weights on the tensor cores.  Tensor maps over the packed codes
 // (bytes [rows][K / 2], box 128 B x 128 rows, 128-byte swizzle) and the block

@@ -58,6 +58,8 @@ def fake_weights():
     (dict(top_k=7, num_experts=6), B.MOE_ERR_INVALID_ARG),
     (dict(max_tokens=0), B.MOE_ERR_INVALID_ARG),
     (dict(path=7), B.MOE_ERR_INVALID_ARG),
+    (dict(deterministic=2), B.MOE_ERR_INVALID_ARG),
+    (dict(deterministic=-1), B.MOE_ERR_INVALID_ARG),
     (dict(d=100), B.MOE_ERR_UNSUPPORTED),
     (dict(d=6464), B.MOE_ERR_UNSUPPORTED),           # the router's staging limit is d <= 6400
     (dict(ffn=96), B.MOE_ERR_UNSUPPORTED),
