@@ -245,7 +245,8 @@ def measure(args, name, spec, kind, wts, T, chain, device, stream, rank, world, 
     with torch.cuda.stream(stream):
         for w in wts:
             handles.append(B.layer_from_spec(spec, w, max_tokens=max(T, 64), stream=stream,
-                                             path={"auto": 0, "gemv": 1, "tc": 2}[args.path]))
+                                             path={"auto": 0, "gemv": 1, "tc": 2}[args.path],
+                                             deterministic=args.deterministic))
     x = I.make_tokens_torch(spec, seed=args.seed + 77 + rank + T, T=T, device=device)
     ys = [torch.empty_like(x) for _ in handles]
     ins = [x] + ys[:-1] if chain else [x] * len(handles)
@@ -713,7 +714,7 @@ def run_ours(args, rank, world, local_rank):
                           "expert_ffn": spec.ffn, "weights": kind, "layers_per_step": head["layers"],
                           "chained": chain, "router_bias": spec.bias, "residual": bool(spec.add_residual),
                           "l2": f"inputs larger than L2: {head['layers']} distinct layers' weights per step",
-                          "parallelism": f"replicas{world}", "path": args.path},
+                          "parallelism": f"replicas{world}", "path": args.path, "deterministic": bool(args.deterministic)},
                "layer": head["layer"], "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
                "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
         if sweep:
@@ -795,6 +796,8 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--deterministic", action="store_true",
+                    help="the tcgen05 paths' fixed-order combine (moe_config.deterministic)")
     ap.add_argument("--only", default=None,
                     choices=sorted(list(WORKLOADS) + list(STACK_DECODE) + list(HEAD) + list(ATTN)),
                     help="run one sweep entry alone and print its result (profiling)")
