@@ -90,19 +90,26 @@ def test_flint_prefill_ragged_with_residual(flint_bf16):
     check_layer(L, x, y, idx, gate, spec.top_k, "bf16", residual=True, tokens=np.arange(0, T, 31))
 
 
-@pytest.mark.parametrize("which", ["tensor_core_router", "simt_router"])
+@pytest.mark.parametrize("which", ["tensor_core_router", "tensor_core_router_2048", "tensor_core_router_100",
+                                   "simt_router"])
 def test_route_and_grouping_large_batch(flint_bf16, small, which):
-    if which == "tensor_core_router":
+    """Routing and grouping on every token: the tensor-core router at T = 100,
+    777 and 2048 (one, seven and sixteen 128-token blocks), the SIMT router
+    at T = 300; repeated calls give bit-identical routing."""
+    if which.startswith("tensor_core_router"):
         spec, L, dev = flint_bf16                # E = 256: tensor-core router
-        T = 777
+        T = {"tensor_core_router": 777, "tensor_core_router_2048": 2048, "tensor_core_router_100": 100}[which]
     else:
         spec, (L, dev) = SMALL, small            # E = 16: fp32 SIMT router
         T = 300
     x_np = I.make_tokens(spec, seed=55, T=T)
     layer = B.layer_from_spec(spec, dev, T)
-    idx, gate, cnt = layer.route(to_torch_x(x_np))
+    x = to_torch_x(x_np)
+    idx, gate, cnt = layer.route(x)
     offs, tos, so = layer.grouping(T, "cuda")
+    idx2, gate2, _ = layer.route(x)                  # bit-identical repeats
     torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(gate, gate2)
     W = LayerWeights(L)
     xf = (x_np.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     l = router_logits(xf, W.Wr, W.b)
